@@ -1,0 +1,721 @@
+// attn_bwd: attention backward on sm_103a, N-outer / Q-inner, recompute-P.
+//
+// Method ("反向传播算法详解" §2-§6; "解析 FlashAttention（3）" §3-§4):
+// one CTA owns a block of Bc = 128 keys of one KV head (block coordinate
+// (n_block, kv_head, batch), "反向传播算法详解" §3.3). It loads K_j, V_j once
+// (§4.5) and keeps the fp32 accumulators dK_j, dV_j in tensor memory while it
+// walks every query block i (Br = 128 rows) of every query head of the KV
+// head's group. Per (i, j) tile it runs the five GEMMs of §5.2 on the
+// tcgen05 tensor cores and the elementwise softmax backward in registers:
+//
+//   S^T  = K_j Q_i^T                (M = keys, N = queries, K = d)
+//   dP^T = V_j dO_i^T
+//   P    = exp2(S^T * tau*log2e - LSE*log2e)   [softcap: tau*S -> c tanh(tau*S/c)]
+//   dS   = P o (dP - D)              [softcap: o (1 - tanh^2)]
+//   dV_j += P^T dO_i                 (P^T taken from tensor memory)
+//   dK_j += dS^T Q_i                 (dS^T taken from tensor memory)
+//   dQ_i += dS K_j                   (dS from shared memory; fp32 atomics)
+//
+// Because S^T is computed with keys on the tensor-memory lanes, P^T and dS^T
+// already sit in the layout the dV/dK GEMMs want as their A operand, so they
+// never pass through shared memory (the analogue of feeding P/dS from
+// registers to the dK/dV GEMM, "反向传播算法详解" §8.2). dK/dV are summed over
+// the GQA group on chip (§8.5 sums them in fp32 HBM buffers instead), so they
+// need no atomics; only dQ is accumulated globally (§3.2, §6).
+//
+// Warp roles (512 threads):
+//   warp 0       TMA producer: K, V once; Q_i (+LSE_i, D_i), dO_i per tile,
+//                two-stage rings (the two pipelines of §4.3)
+//   warp 1       tcgen05 MMA issuer (one thread), tensor-memory owner
+//   warps 4-11   softmax backward: two warpgroups, one per half of the
+//                query columns; thread = key row (tensor-memory lane);
+//                afterwards the dK/dV epilogue
+//   warps 12-15  dQ drain: tensor memory -> fp32 atomic adds into dq_accum
+//
+// Tensor memory (512 columns x 128 lanes x 32 bit):
+//   [  0,128)  S^T (fp32); P^T (bf16 pairs) overwrites the read part
+//   [128,256)  dP^T (fp32); dS^T (bf16 pairs), then the dQ tile, reuse it
+//   [256,384)  dV accumulator     [384,512)  dK accumulator
+//
+// Every wait on an mbarrier is bounded: on timeout the kernel records
+// ATTN_ERR_DEVICE_TIMEOUT in the device status word and all roles return.
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "attn_common.cuh"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+namespace bwd {
+
+using namespace ptx;
+
+constexpr int kBc = 128;  // keys per CTA (tensor-memory lanes)
+constexpr int kBr = 128;  // queries per tile
+constexpr int kThreads = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr long long kWaitLimitCycles = 2000000000LL;  // about one second
+
+__device__ int g_status;  // device status word (ATTN_OK or ATTN_ERR_*)
+
+template <int D>
+struct Layout {
+  static constexpr int kTileBytes = kBr * D * 2;  // one Q / dO / K / V tile
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTileBytes;
+  static constexpr int kQ0 = kV + kTileBytes;
+  static constexpr int kQ1 = kQ0 + kTileBytes;
+  static constexpr int kDO0 = kQ1 + kTileBytes;
+  static constexpr int kDO1 = kDO0 + kTileBytes;
+  static constexpr int kDS = kDO1 + kTileBytes;     // dS^T, [key][query], 32 KB
+  static constexpr int kLSE = kDS + kBc * kBr * 2;  // 2 stages x 128 fp32 (LSE*log2e)
+  static constexpr int kDsum = kLSE + 2 * kBr * 4;  // 2 stages x 128 fp32 (D)
+  static constexpr int kBars = kDsum + 2 * kBr * 4;
+  static constexpr int kNumBars = 16;
+  static constexpr int kTmemSlot = kBars + kNumBars * 8;
+  static constexpr int kAbort = kTmemSlot + 4;
+  static constexpr int kBytes = kAbort + 12;
+};
+static_assert(Layout<128>::kBytes <= 232448, "shared memory budget");
+
+enum Bar {
+  BAR_KV = 0,
+  BAR_Q_FULL = 1,    // + stage
+  BAR_Q_EMPTY = 3,   // + stage
+  BAR_DO_FULL = 5,   // + stage
+  BAR_DO_EMPTY = 7,  // + stage
+  BAR_S_FULL = 9,
+  BAR_P_FULL = 10,
+  BAR_DP_FULL = 11,
+  BAR_DS_FULL = 12,
+  BAR_DQ_FULL = 13,
+  BAR_DQ_EMPTY = 14,
+  BAR_KV_DONE = 15,
+};
+
+struct Params {
+  const float* lse;
+  const float* dpsum;
+  float* dq_accum;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int B, H, H_kv, N;
+  int n_blocks, m_blocks;
+  float scale;
+  float softcap;
+};
+
+// Per-CTA work description.
+struct Work {
+  int b, g, n_block;
+  int G, m_start, per_head, T;
+};
+
+struct Ctx {
+  uint32_t bars;
+  volatile int* abort;
+};
+
+__device__ __forceinline__ uint32_t bar_addr(const Ctx& c, int i) { return c.bars + 8u * i; }
+
+__device__ __noinline__ void record_status(int code) { atomicCAS(&g_status, 0, code); }
+
+// Bounded wait; returns false if the kernel is aborting.
+__device__ __forceinline__ bool wait(const Ctx& c, int bar, uint32_t parity) {
+  const uint32_t a = bar_addr(c, bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const long long t0 = clock64();
+  uint32_t n = 0;
+  while (!mbar_try_wait(a, parity)) {
+    if ((++n & 63u) == 0) {
+      if (*c.abort) return false;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        *c.abort = 1;
+        record_status(ATTN_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight work).
+__device__ __forceinline__ void wait_drain(const Ctx& c, int bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar_addr(c, bar), parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) return;
+  }
+}
+
+// Tile t of a CTA: query head h = g*G + t / per_head, query block
+// m_start + t % per_head (heads outer, query blocks inner).
+__device__ __forceinline__ void tile_coord(const Work& w, int t, int& h, int& m_block) {
+  const int hh = t / w.per_head;
+  h = w.g * w.G + hh;
+  m_block = w.m_start + (t - hh * w.per_head);
+}
+
+// ------------------------------------------------------------------ producer
+template <int D>
+__device__ void producer_role(const Ctx& c, const Params& p, const Work& w, uint8_t* smem,
+                              uint32_t sbase, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                              const CUtensorMap* tm_v, const CUtensorMap* tm_do) {
+  using L = Layout<D>;
+  constexpr int kBoxes = D / 64;
+  constexpr uint32_t kTileBytes = L::kTileBytes;
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) {
+    prefetch_tmap(tm_q);
+    prefetch_tmap(tm_k);
+    prefetch_tmap(tm_v);
+    prefetch_tmap(tm_do);
+    const uint64_t once = policy_evict_first();
+    mbar_arrive_expect_tx(bar_addr(c, BAR_KV), 2 * kTileBytes);
+    const int kvh = w.b * p.H_kv + w.g;
+    for (int cb = 0; cb < kBoxes; ++cb) {
+      tma_load_3d_hint(sbase + L::kK + cb * 16384, tm_k, bar_addr(c, BAR_KV), 64 * cb,
+                       w.n_block * kBc, kvh, once);
+      tma_load_3d_hint(sbase + L::kV + cb * 16384, tm_v, bar_addr(c, BAR_KV), 64 * cb,
+                       w.n_block * kBc, kvh, once);
+    }
+  }
+  __syncwarp();
+  // Q/dO tiles are re-read by every key block of the head: keep them in L2.
+  const uint64_t reuse = policy_evict_last();
+  int issued_q = 0, issued_do = 0;
+  for (int t = 0; t < w.T; ++t) {
+    const int st = t & 1;
+    const uint32_t ph = (t >> 1) & 1;
+    int h, m_block;
+    tile_coord(w, t, h, m_block);
+    const int bh = w.b * p.H + h;
+    const int m0 = m_block * kBr;
+    if (t >= 2 && !wait(c, BAR_Q_EMPTY + st, ph ^ 1)) break;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_addr(c, BAR_Q_FULL + st), kTileBytes);
+      const uint32_t dst = sbase + (st ? L::kQ1 : L::kQ0);
+      for (int cb = 0; cb < kBoxes; ++cb)
+        tma_load_3d_hint(dst + cb * 16384, tm_q, bar_addr(c, BAR_Q_FULL + st), 64 * cb, m0, bh,
+                         reuse);
+    }
+    {
+      float* s_lse = reinterpret_cast<float*>(smem + L::kLSE) + st * kBr;
+      float* s_d = reinterpret_cast<float*>(smem + L::kDsum) + st * kBr;
+      const long long row0 = static_cast<long long>(bh) * p.N + m0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = lane + 32 * e;
+        float lv = 0.f, dv = 0.f;
+        if (m0 + i < p.N) {
+          lv = __ldg(p.lse + row0 + i);
+          dv = __ldg(p.dpsum + row0 + i);
+        }
+        s_lse[i] = lv * kLog2e;
+        s_d[i] = dv;
+      }
+      mbar_arrive(bar_addr(c, BAR_Q_FULL + st));
+    }
+    issued_q = t + 1;
+    if (t >= 2 && !wait(c, BAR_DO_EMPTY + st, ph ^ 1)) break;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_addr(c, BAR_DO_FULL + st), kTileBytes);
+      const uint32_t dst = sbase + (st ? L::kDO1 : L::kDO0);
+      for (int cb = 0; cb < kBoxes; ++cb)
+        tma_load_3d_hint(dst + cb * 16384, tm_do, bar_addr(c, BAR_DO_FULL + st), 64 * cb, m0, bh,
+                         reuse);
+    }
+    __syncwarp();
+    issued_do = t + 1;
+  }
+  // When aborting, the copies issued last must land before the CTA exits.
+  if (*c.abort) {
+    wait_drain(c, BAR_KV, 0);
+    for (int t = issued_q - 2 < 0 ? 0 : issued_q - 2; t < issued_q; ++t)
+      wait_drain(c, BAR_Q_FULL + (t & 1), (t >> 1) & 1);
+    for (int t = issued_do - 2 < 0 ? 0 : issued_do - 2; t < issued_do; ++t)
+      wait_drain(c, BAR_DO_FULL + (t & 1), (t >> 1) & 1);
+  }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+template <int D>
+__device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t tmem) {
+  using L = Layout<D>;
+  constexpr int kKSteps = D / 16;      // S, dP: reduction over d
+  constexpr int kQSteps = kBr / 16;    // dV, dK: reduction over queries
+  constexpr int kKeySteps = kBc / 16;  // dQ: reduction over keys
+  constexpr uint32_t kIdS = make_idesc_bf16(kBc, kBr, false, false);
+  constexpr uint32_t kIdKV = make_idesc_bf16(kBc, D, false, true);
+  // d = 128: dQ^T = K^T dS^T (M = d lanes, N = queries), drained coalesced
+  // d =  64: dQ   = dS K     (M = query lanes, N = d)
+  constexpr uint32_t kIdQ =
+      D == 128 ? make_idesc_bf16(D, kBr, true, true) : make_idesc_bf16(kBr, D, true, true);
+  const uint32_t tS = tmem + 0, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+  const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sDS = sbase + L::kDS;
+
+  if (wait(c, BAR_KV, 0)) {
+    tc_fence_after();
+    for (int t = 0; t < w.T; ++t) {
+      const int st = t & 1;
+      const uint32_t ph = (t >> 1) & 1;
+      const uint32_t sQ = sbase + (st ? L::kQ1 : L::kQ0);
+      const uint32_t sDO = sbase + (st ? L::kDO1 : L::kDO0);
+
+      // S^T = K Q^T. The S region held P of the previous tile, read by the
+      // dV GEMM issued before: tcgen05 MMAs of one thread run in order.
+      if (!wait(c, BAR_Q_FULL + st, ph)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < kKSteps; ++k) {
+        const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+        mma_ss(tS, make_sdesc(sK + off, 16, 1024), make_sdesc(sQ + off, 16, 1024), kIdS, k > 0);
+      }
+      mma_commit(bar_addr(c, BAR_S_FULL));
+
+      // dP^T = V dO^T, once the previous dQ tile has left the dP region.
+      if (!wait(c, BAR_DO_FULL + st, ph)) break;
+      if (t > 0 && !wait(c, BAR_DQ_EMPTY, (t - 1) & 1)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < kKSteps; ++k) {
+        const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+        mma_ss(tdP, make_sdesc(sV + off, 16, 1024), make_sdesc(sDO + off, 16, 1024), kIdS,
+               k > 0);
+      }
+      mma_commit(bar_addr(c, BAR_DP_FULL));
+
+      // dV += P^T dO (A = P^T from tensor memory, B = dO MN-major)
+      if (!wait(c, BAR_P_FULL, t & 1)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < kQSteps; ++k) {
+        const uint32_t acol = 8 * k + (k >= 4 ? 32 : 0);
+        mma_ts(tdV, tS + acol, make_sdesc(sDO + 2048 * k, 16384, 1024), kIdKV,
+               (t > 0 || k > 0) ? 1u : 0u);
+      }
+      mma_commit(bar_addr(c, BAR_DO_EMPTY + st));
+
+      // dK += dS^T Q (A = dS^T from tensor memory, B = Q MN-major)
+      if (!wait(c, BAR_DS_FULL, t & 1)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < kQSteps; ++k) {
+        const uint32_t acol = 8 * k + (k >= 4 ? 32 : 0);
+        mma_ts(tdK, tdP + acol, make_sdesc(sQ + 2048 * k, 16384, 1024), kIdKV,
+               (t > 0 || k > 0) ? 1u : 0u);
+      }
+      mma_commit(bar_addr(c, BAR_Q_EMPTY + st));
+
+      // dQ tile into the dP region (dS^T there was consumed by the dK GEMM)
+#pragma unroll
+      for (int k = 0; k < kKeySteps; ++k) {
+        if (D == 128)
+          mma_ss(tdP, make_sdesc(sK + 2048 * k, 16384, 1024),
+                 make_sdesc(sDS + 2048 * k, 16384, 1024), kIdQ, k > 0);
+        else
+          mma_ss(tdP, make_sdesc(sDS + 2048 * k, 16384, 1024),
+                 make_sdesc(sK + 2048 * k, 16384, 1024), kIdQ, k > 0);
+      }
+      mma_commit(bar_addr(c, BAR_DQ_FULL));
+    }
+  }
+  // Completion of everything issued; the epilogue waits on it.
+  mma_commit(bar_addr(c, BAR_KV_DONE));
+  if (*c.abort) wait_drain(c, BAR_KV_DONE, 0);
+}
+
+// ------------------------------------------------------------------ softmax
+// One tile, one half of its query columns. Thread = key row r (tensor-memory
+// lane r); columns [64*half, 64*half + 64).
+template <int D, bool SOFTCAP, bool CAUSAL, bool MASKED>
+__device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint8_t* smem,
+                                             uint32_t sbase, uint32_t tmem, int t, int half,
+                                             int r, int key, int m0) {
+  using L = Layout<D>;
+  const int st = t & 1;
+  const int lane = threadIdx.x & 31;
+  const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
+  const float* s_lse = reinterpret_cast<const float*>(smem + L::kLSE) + st * kBr;
+  const float* s_d = reinterpret_cast<const float*>(smem + L::kDsum) + st * kBr;
+  const float c_log2 = p.scale * kLog2e;                                  // tau*log2e
+  const float cap_in = SOFTCAP ? 2.f * kLog2e * p.scale / p.softcap : 0.f;  // 2 log2e tau/c
+  const float cap_out = SOFTCAP ? p.softcap * kLog2e : 0.f;                 // c log2e
+  float pk[64];  // P, or P (1 - tanh^2) with softcap, for this thread's 64 columns
+
+  // ---- P = exp(S - LSE) -> bf16 P^T in tensor memory
+  if (!wait(c, BAR_S_FULL, t & 1)) return false;
+  tc_fence_after();
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    const int col0 = half * 64 + ch * 16;
+    uint32_t raw[16];
+    tmem_ld16(tmem + lane_base + col0, raw);
+    float pv[16];
+#pragma unroll
+    for (int j4 = 0; j4 < 4; ++j4) {
+      const float4 l4 = *reinterpret_cast<const float4*>(s_lse + col0 + 4 * j4);
+      const float lse4[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = 4 * j4 + e;
+        const float s = __uint_as_float(raw[j]);
+        float prob, keep;
+        if (SOFTCAP) {
+          // tanh(u) = 1 - 2 / (exp(2u) + 1) with u = tau s / c
+          const float ex = ex2_approx(s * cap_in);
+          const float th = 1.f - 2.f * rcp_approx(ex + 1.f);
+          prob = ex2_approx(th * cap_out - lse4[e]);
+          keep = prob * (1.f - th * th);
+        } else {
+          prob = ex2_approx(s * c_log2 - lse4[e]);
+          keep = prob;
+        }
+        if (MASKED) {
+          const int q = m0 + col0 + j;
+          const bool ok = key < p.N && q < p.N && (!CAUSAL || key <= q);
+          prob = ok ? prob : 0.f;
+          keep = ok ? keep : 0.f;
+        }
+        pv[j] = prob;
+        pk[ch * 16 + j] = keep;
+      }
+    }
+    uint32_t packed[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) packed[u] = pack_bf16x2(pv[2 * u], pv[2 * u + 1]);
+    tmem_st8(tmem + lane_base + half * 64 + ch * 8, packed);
+  }
+  tmem_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar_addr(c, BAR_P_FULL));
+
+  // ---- dS = P o (dP - D) -> bf16 dS^T in tensor memory and shared memory
+  if (!wait(c, BAR_DP_FULL, t & 1)) return false;
+  // the previous dQ GEMM must be done reading the shared dS tile
+  if (t > 0 && !wait(c, BAR_DQ_FULL, (t - 1) & 1)) return false;
+  tc_fence_after();
+  const uint32_t ds_row = sbase + L::kDS + half * 16384 + r * 128;
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    const int col0 = half * 64 + ch * 16;
+    uint32_t raw[16];
+    tmem_ld16(tmem + lane_base + 128 + col0, raw);
+    float ds[16];
+#pragma unroll
+    for (int j4 = 0; j4 < 4; ++j4) {
+      const float4 d4 = *reinterpret_cast<const float4*>(s_d + col0 + 4 * j4);
+      const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = 4 * j4 + e;
+        ds[j] = pk[ch * 16 + j] * (__uint_as_float(raw[j]) - dd[e]);
+      }
+    }
+    uint32_t packed[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) packed[u] = pack_bf16x2(ds[2 * u], ds[2 * u + 1]);
+    tmem_st8(tmem + lane_base + 128 + half * 64 + ch * 8, packed);
+    // dS^T row r, queries [col0, col0+16): 16-byte chunks 2ch, 2ch+1 of the
+    // 128-byte row, placed by the 128-byte swizzle (chunk ^ (row & 7))
+    st_shared_v4(ds_row + (((2 * ch) ^ (r & 7)) << 4), packed[0], packed[1], packed[2],
+                 packed[3]);
+    st_shared_v4(ds_row + (((2 * ch + 1) ^ (r & 7)) << 4), packed[4], packed[5], packed[6],
+                 packed[7]);
+  }
+  fence_proxy_async_smem();
+  tmem_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar_addr(c, BAR_DS_FULL));
+  return true;
+}
+
+template <int D, bool CAUSAL, bool SOFTCAP>
+__device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8_t* smem,
+                             uint32_t sbase, uint32_t tmem) {
+  const int warp = threadIdx.x >> 5;
+  const int half = (warp - 4) >> 2;
+  const int r = ((warp & 3) << 5) + (threadIdx.x & 31);
+  const int n0 = w.n_block * kBc;
+  const int key = n0 + r;
+  const bool key_tail = n0 + kBc > p.N;
+  bool ok = true;
+  for (int t = 0; t < w.T && ok; ++t) {
+    int h, m_block;
+    tile_coord(w, t, h, m_block);
+    const int m0 = m_block * kBr;
+    if (!wait(c, BAR_Q_FULL + (t & 1), (t >> 1) & 1)) break;
+    const bool masked = (CAUSAL && m_block == w.n_block) || key_tail || (m0 + kBr > p.N);
+    if (masked)
+      ok = softmax_tile<D, SOFTCAP, CAUSAL, true>(c, p, smem, sbase, tmem, t, half, r, key, m0);
+    else
+      ok = softmax_tile<D, SOFTCAP, CAUSAL, false>(c, p, smem, sbase, tmem, t, half, r, key, m0);
+  }
+
+  // ---- epilogue: dK (x tau) and dV, fp32 tensor memory -> bf16 global.
+  // This warpgroup writes columns [half*D/2, (half+1)*D/2) of its key row.
+  if (!wait(c, BAR_KV_DONE, 0)) return;
+  tc_fence_after();
+  const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
+  const long long row = (static_cast<long long>(w.b) * p.H_kv + w.g) * p.N + key;
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    const uint32_t col_base = (which == 0 ? 256u : 384u) + half * (D / 2);
+    __nv_bfloat16* out = (which == 0 ? p.dv : p.dk) + row * D + half * (D / 2);
+    const float mul = which == 0 ? 1.f : p.scale;
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t raw[16];
+      tmem_ld16(tmem + lane_base + col_base + ch * 16, raw);
+        uint32_t packed[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        packed[u] = pack_bf16x2(__uint_as_float(raw[2 * u]) * mul,
+                                __uint_as_float(raw[2 * u + 1]) * mul);
+      if (key < p.N) {
+        uint4* dst = reinterpret_cast<uint4*>(out + ch * 16);
+        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ dQ drain
+template <int D>
+__device__ void dq_role(const Ctx& c, const Params& p, const Work& w, uint32_t tmem) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int r = ((warp & 3) << 5) + lane;
+  const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
+  for (int t = 0; t < w.T; ++t) {
+    int h, m_block;
+    tile_coord(w, t, h, m_block);
+    const int m0 = m_block * kBr;
+    const long long bh = static_cast<long long>(w.b) * p.H + h;
+    if (!wait(c, BAR_DQ_FULL, t & 1)) return;
+    tc_fence_after();
+    if (D == 128) {
+      // lane r holds dQ[m0 + i][r] in column 128 + i: one warp instruction
+      // adds 32 consecutive floats (one 128-byte line) of a dQ row.
+      float* dst = p.dq_accum + (bh * p.N + m0) * D + r;
+      const bool full = m0 + kBr <= p.N;
+#pragma unroll
+      for (int hv = 0; hv < 2; ++hv) {
+        uint32_t v[64];
+        uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+        uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+        tmem_ld32(tmem + lane_base + 128 + hv * 64, v0);
+        tmem_ld32(tmem + lane_base + 128 + hv * 64 + 32, v1);
+            if (hv == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_addr(c, BAR_DQ_EMPTY));
+        }
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const int i = hv * 64 + j;
+          if (full || m0 + i < p.N) red_add_f32(dst + static_cast<long long>(i) * D,
+                                                __uint_as_float(v[j]));
+        }
+      }
+    } else {
+      // lane r holds query row m0 + r, columns 128 + [0, 64) = dQ[m0 + r][:]
+      uint32_t v[64];
+      uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+      uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+      tmem_ld32(tmem + lane_base + 128, v0);
+      tmem_ld32(tmem + lane_base + 128 + 32, v1);
+        tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_addr(c, BAR_DQ_EMPTY));
+      if (m0 + r < p.N) {
+        float* dst = p.dq_accum + (bh * p.N + m0 + r) * D;
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          red_add_v4_f32(dst + 4 * u, __uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                         __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int D, bool CAUSAL, bool SOFTCAP>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_do, const Params p) {
+  using L = Layout<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {  // the 128-byte swizzle atoms need 1024-byte alignment
+    if (threadIdx.x == 0) record_status(ATTN_ERR_DEVICE);
+    return;
+  }
+  Ctx c;
+  c.bars = sbase + L::kBars;
+  c.abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
+
+  Work w;
+  {
+    const int per_nb = p.H_kv * p.B;
+    w.n_block = blockIdx.x / per_nb;
+    const int rem = blockIdx.x - w.n_block * per_nb;
+    w.b = rem / p.H_kv;
+    w.g = rem - w.b * p.H_kv;
+    w.G = p.H / p.H_kv;
+    w.m_start = CAUSAL ? w.n_block : 0;
+    w.per_head = p.m_blocks - w.m_start;
+    w.T = w.G * w.per_head;
+  }
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    mbar_init(bar_addr(c, BAR_KV), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_addr(c, BAR_Q_FULL + s), 33);  // expect_tx arrive + 32 LSE/D lanes
+      mbar_init(bar_addr(c, BAR_Q_EMPTY + s), 1);
+      mbar_init(bar_addr(c, BAR_DO_FULL + s), 1);
+      mbar_init(bar_addr(c, BAR_DO_EMPTY + s), 1);
+    }
+    mbar_init(bar_addr(c, BAR_S_FULL), 1);
+    mbar_init(bar_addr(c, BAR_P_FULL), 8);
+    mbar_init(bar_addr(c, BAR_DP_FULL), 1);
+    mbar_init(bar_addr(c, BAR_DS_FULL), 8);
+    mbar_init(bar_addr(c, BAR_DQ_FULL), 1);
+    mbar_init(bar_addr(c, BAR_DQ_EMPTY), 4);
+    mbar_init(bar_addr(c, BAR_KV_DONE), 1);
+    *c.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + L::kTmemSlot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
+
+  if (warp == 0) {
+    producer_role<D>(c, p, w, smem, sbase, &tm_q, &tm_k, &tm_v, &tm_do);
+  } else if (warp == 1) {
+    if ((threadIdx.x & 31) == 0) mma_role<D>(c, w, sbase, tmem);
+    __syncwarp();
+  } else if (warp >= 4 && warp < 12) {
+    softmax_role<D, CAUSAL, SOFTCAP>(c, p, w, smem, sbase, tmem);
+  } else if (warp >= 12) {
+    dq_role<D>(c, p, w, tmem);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL, bool SOFTCAP>
+int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+           const CUtensorMap& tdo, const Params& p, cudaStream_t stream) {
+  auto kern = attn_bwd_kernel<D, CAUSAL, SOFTCAP>;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Layout<D>::kBytes) != cudaSuccess)
+      return ATTN_ERR_LAUNCH;
+    configured = true;
+  }
+  const long long grid = static_cast<long long>(p.n_blocks) * p.H_kv * p.B;
+  if (grid > 0x7fffffffLL) return ATTN_ERR_TOO_LARGE;
+  kern<<<static_cast<unsigned>(grid), kThreads, Layout<D>::kBytes, stream>>>(tq, tk, tv, tdo, p);
+  return launch_status();
+}
+
+}  // namespace bwd
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                        const void* dO, const float* lse, float* dq_accum, void* dk, void* dv,
+                        int B, int H, int H_kv, int N, int d, float scale, int causal,
+                        float softcap, const float* dpsum, void* stream) {
+  (void)o;  // D = rowsum(dO o O) arrives precomputed in dpsum
+  if (!q || !k || !v || !dO || !lse || !dq_accum || !dk || !dv || !dpsum) return ATTN_ERR_NULL;
+  int rc = check_shape(B, H, H_kv, N, d);
+  if (rc != ATTN_OK) return rc;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale) || scale == 0.f || std::isnan(softcap)) return ATTN_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
+      !aligned16(dq_accum) || !aligned16(dk) || !aligned16(dv) || !aligned16(dpsum))
+    return ATTN_ERR_ALIGN;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+
+  CUtensorMap tq, tk, tv, tdo;
+  const long long hq = static_cast<long long>(B) * H, hk = static_cast<long long>(B) * H_kv;
+  if (!encode_bf16_3d(&tq, q, d, N, hq, bwd::kBr) || !encode_bf16_3d(&tk, k, d, N, hk, bwd::kBc) ||
+      !encode_bf16_3d(&tv, v, d, N, hk, bwd::kBc) ||
+      !encode_bf16_3d(&tdo, dO, d, N, hq, bwd::kBr))
+    return ATTN_ERR_LAUNCH;
+
+  bwd::Params p;
+  p.lse = lse;
+  p.dpsum = dpsum;
+  p.dq_accum = dq_accum;
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.B = B;
+  p.H = H;
+  p.H_kv = H_kv;
+  p.N = N;
+  p.n_blocks = (N + bwd::kBc - 1) / bwd::kBc;
+  p.m_blocks = (N + bwd::kBr - 1) / bwd::kBr;
+  p.scale = scale;
+  const bool cap = softcap > 0.f;
+  p.softcap = cap ? softcap : 0.f;
+  cudaStream_t s = as_stream(stream);
+  const bool cs = causal != 0;
+  if (d == 128) {
+    if (cs) return cap ? bwd::launch<128, true, true>(tq, tk, tv, tdo, p, s)
+                       : bwd::launch<128, true, false>(tq, tk, tv, tdo, p, s);
+    return cap ? bwd::launch<128, false, true>(tq, tk, tv, tdo, p, s)
+               : bwd::launch<128, false, false>(tq, tk, tv, tdo, p, s);
+  }
+  if (cs) return cap ? bwd::launch<64, true, true>(tq, tk, tv, tdo, p, s)
+                     : bwd::launch<64, true, false>(tq, tk, tv, tdo, p, s);
+  return cap ? bwd::launch<64, false, true>(tq, tk, tv, tdo, p, s)
+             : bwd::launch<64, false, false>(tq, tk, tv, tdo, p, s);
+}
+
+extern "C" int attn_device_status(int* status, int clear, void* stream) {
+  if (!status) return ATTN_ERR_NULL;
+  cudaStream_t s = as_stream(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, bwd::g_status, sizeof(int)) != cudaSuccess) return ATTN_ERR_LAUNCH;
+  *status = v;
+  if (clear) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(bwd::g_status, &zero, sizeof(int)) != cudaSuccess)
+      return ATTN_ERR_LAUNCH;
+  }
+  return ATTN_OK;
+}
+
+extern "C" const char* attn_strerror(int code) {
+  switch (code) {
+    case ATTN_OK: return "success";
+    case ATTN_ERR_NULL: return "a required pointer is NULL";
+    case ATTN_ERR_SHAPE: return "invalid shape or scalar argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported head dimension";
+    case ATTN_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case ATTN_ERR_LAUNCH: return "CUDA launch or runtime error";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel timed out waiting on a barrier";
+    case ATTN_ERR_DEVICE: return "a kernel detected an internal fault";
+    case ATTN_ERR_TOO_LARGE: return "a size exceeds the supported range";
+    default: return "unknown error code";
+  }
+}

@@ -1,0 +1,69 @@
+// Host-side helpers shared by the translation units of the library:
+// argument validation and TMA tensor-map encoding.
+#pragma once
+
+#include <cmath>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/attnbwd.h"
+
+namespace attn {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Shape checks common to all calls. Returns ATTN_OK, or an error code.
+inline int check_shape(int B, int H, int H_kv, int N, int d) {
+  if (B < 0 || H < 0 || H_kv < 0 || N < 0 || d <= 0) return ATTN_ERR_SHAPE;
+  if (H > 0 && (H_kv <= 0 || H % H_kv != 0)) return ATTN_ERR_SHAPE;
+  // element counts must stay below 2^31 per (batch, head) row block and the
+  // flat tensors below 2^40 elements (TMA strides, 64-bit offsets)
+  const long long rows = static_cast<long long>(B) * H * N;
+  if (rows * d >= (1LL << 40)) return ATTN_ERR_TOO_LARGE;
+  if (static_cast<long long>(N) * d >= (1LL << 31)) return ATTN_ERR_TOO_LARGE;
+  return ATTN_OK;
+}
+
+inline int launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no
+// link-time dependency on libcuda).
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 3-D bf16 tensor map over [heads, rows, d] (innermost d), box
+// {64, box_rows, 1}, 128-byte swizzle, zero fill outside the tensor.
+inline bool encode_bf16_3d(CUtensorMap* map, const void* base, int d, int rows, long long heads,
+                           int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace attn

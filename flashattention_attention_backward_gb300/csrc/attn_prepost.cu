@@ -1,0 +1,120 @@
+// attn_bwd_preprocess and attn_bwd_finalize: the two memory-bound steps
+// around the main backward kernel.
+//
+//  * preprocess: D_i = sum_k dO_ik O_ik ("解析 FlashAttention（3）" §2.4 eq. 6;
+//    "反向传播算法详解" §2.1(3): dPsum can be formed before the backward kernel
+//    starts) and dq_accum := 0, in one pass. One warp per row: the row of O
+//    and dO is read once (4 bf16 per lane per step), reduced with shuffles,
+//    and the matching fp32 dQ-accumulator row is cleared with 16-byte stores.
+//  * finalize: dq = bf16(tau * dq_accum) ("解析 FlashAttention（3）" eq. 7),
+//    16 bytes read / 8 bytes written per thread step.
+// Both grids are a multiple of the SM count and grid-stride over the rows.
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "attn_common.cuh"
+
+namespace attn {
+namespace prepost {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads)
+    preprocess_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
+                      float* __restrict__ dpsum, float* __restrict__ dq_accum, long long rows,
+                      int d) {
+  const int lane = threadIdx.x & 31;
+  const long long warp0 = (static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * kThreads) >> 5;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long row = warp0; row < rows; row += nwarps) {
+    const long long base = row * d;
+    float acc = 0.f;
+    for (int c = lane * 4; c < d; c += 128) {
+      const uint2 uo = __ldcs(reinterpret_cast<const uint2*>(o + base + c));
+      const uint2 ud = __ldcs(reinterpret_cast<const uint2*>(dO + base + c));
+      const uint32_t wo[2] = {uo.x, uo.y}, wd[2] = {ud.x, ud.y};
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        acc = fmaf(__uint_as_float(wo[e] << 16), __uint_as_float(wd[e] << 16), acc);
+        acc = fmaf(__uint_as_float(wo[e] & 0xffff0000u), __uint_as_float(wd[e] & 0xffff0000u),
+                   acc);
+      }
+      *reinterpret_cast<float4*>(dq_accum + base + c) = zero;
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) dpsum[row] = acc;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads)
+    finalize_kernel(const float* __restrict__ dq_accum, __nv_bfloat16* __restrict__ dq,
+                    float scale, long long n4) {
+  const long long stride = static_cast<long long>(gridDim.x) * kThreads;
+  for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < n4;
+       i += stride) {
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(dq_accum) + i);
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * scale, a.y * scale);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * scale, a.w * scale);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    __stcs(reinterpret_cast<uint2*>(dq) + i, u);
+  }
+}
+
+inline int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+  }
+  return n;
+}
+
+inline unsigned grid_for(long long work_items, int items_per_block) {
+  const long long want = (work_items + items_per_block - 1) / items_per_block;
+  const long long cap = static_cast<long long>(sm_count()) * 8;
+  return static_cast<unsigned>(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+}  // namespace prepost
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_bwd_preprocess(const void* o, const void* dO, float* dpsum, float* dq_accum,
+                                   int B, int H, int N, int d, void* stream) {
+  if (!o || !dO || !dpsum || !dq_accum) return ATTN_ERR_NULL;
+  int rc = check_shape(B, H, H > 0 ? 1 : 0, N, d);
+  if (rc != ATTN_OK) return rc;
+  if (d % 4 != 0) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(dpsum) || !aligned16(dq_accum))
+    return ATTN_ERR_ALIGN;
+  const long long rows = static_cast<long long>(B) * H * N;
+  if (rows == 0) return ATTN_OK;
+  const unsigned grid = prepost::grid_for(rows, prepost::kThreads / 32);
+  prepost::preprocess_kernel<<<grid, prepost::kThreads, 0, as_stream(stream)>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), dpsum,
+      dq_accum, rows, d);
+  return launch_status();
+}
+
+extern "C" int attn_bwd_finalize(const float* dq_accum, void* dq, float scale, int B, int H,
+                                 int N, int d, void* stream) {
+  if (!dq_accum || !dq) return ATTN_ERR_NULL;
+  int rc = check_shape(B, H, H > 0 ? 1 : 0, N, d);
+  if (rc != ATTN_OK) return rc;
+  if (d % 4 != 0) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return ATTN_ERR_SHAPE;
+  if (!aligned16(dq_accum) || !aligned16(dq)) return ATTN_ERR_ALIGN;
+  const long long n4 = static_cast<long long>(B) * H * N * d / 4;
+  if (n4 == 0) return ATTN_OK;
+  const unsigned grid = prepost::grid_for(n4, prepost::kThreads);
+  prepost::finalize_kernel<<<grid, prepost::kThreads, 0, as_stream(stream)>>>(
+      dq_accum, static_cast<__nv_bfloat16*>(dq), scale, n4);
+  return launch_status();
+}

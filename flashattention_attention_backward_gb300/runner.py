@@ -1,0 +1,53 @@
+"""Convenience wrappers that allocate device memory with torch and call the
+C ABI in stream order: forward (O, LSE), then preprocess -> attn_bwd ->
+finalize. No arithmetic happens here; torch provides memory and streams.
+"""
+import torch
+
+from . import (attn_bwd, attn_bwd_finalize, attn_bwd_preprocess, attn_fwd_ref, check)
+
+
+def _dims(q, k):
+    B, H, N, d = q.shape
+    H_kv = k.shape[1]
+    return B, H, H_kv, N, d
+
+
+def _stream(stream):
+    return stream if stream is not None else torch.cuda.current_stream()
+
+
+def forward(q, k, v, scale, causal, softcap=0.0, stream=None):
+    """O [B,H,N,d] bf16 and LSE [B,H,N] fp32 from attn_fwd_ref."""
+    B, H, H_kv, N, d = _dims(q, k)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    check(attn_fwd_ref(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap,
+                       _stream(stream)))
+    return o, lse
+
+
+class BackwardBuffers:
+    """Outputs and scratch of one backward problem, reusable across calls."""
+
+    def __init__(self, q, k):
+        B, H, H_kv, N, d = _dims(q, k)
+        dev = q.device
+        self.dq = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+        self.dk = torch.empty((B, H_kv, N, d), dtype=torch.bfloat16, device=dev)
+        self.dv = torch.empty((B, H_kv, N, d), dtype=torch.bfloat16, device=dev)
+        self.dq_accum = torch.empty((B, H, N, d), dtype=torch.float32, device=dev)
+        self.dpsum = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+
+
+def backward(q, k, v, o, do, lse, scale, causal, softcap=0.0, stream=None, bufs=None):
+    """dQ, dK, dV (bf16) via preprocess -> attn_bwd -> finalize."""
+    B, H, H_kv, N, d = _dims(q, k)
+    s = _stream(stream)
+    if bufs is None:
+        bufs = BackwardBuffers(q, k)
+    check(attn_bwd_preprocess(o, do, bufs.dpsum, bufs.dq_accum, B, H, N, d, s))
+    check(attn_bwd(q, k, v, o, do, lse, bufs.dq_accum, bufs.dk, bufs.dv, B, H, H_kv, N, d,
+                   scale, causal, softcap, bufs.dpsum, s))
+    check(attn_bwd_finalize(bufs.dq_accum, bufs.dq, scale, B, H, N, d, s))
+    return bufs.dq, bufs.dk, bufs.dv

@@ -1,0 +1,130 @@
+/*
+ * attnbwd.h: C ABI of the GB300 (sm_103a) attention backward library.
+ *
+ * The library computes the exact gradient of standard attention without
+ * ever storing the N x N probability matrix: the backward recomputes
+ * S = tau Q K^T and P = exp(S - LSE) tile by tile from the row statistic LSE
+ * saved by the forward.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [FA-v1-bwd] "解析 FlashAttention（3）：FlashAttention-v1 反向传播",
+ *               §1.1, §2.2-2.7 (eq. 1-8), §3 (eq. 9-16), §4 (Algorithm 4).
+ *   [bwd-detail] "反向传播算法详解" (Inference Cookbook), §1.2-1.3
+ *               (recompute, saved tensors), §2.1 (five gradients, dPsum,
+ *               softcap), §3 (N-outer / Q-inner loop), §6 (dQ accumulation),
+ *               §8.5 (GQA group sums).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  * Pointers are DEVICE pointers into memory the caller owns; the library
+ *    never allocates or frees caller memory.
+ *  * Layout is contiguous row-major: Q, O, dO, dQ and the dQ accumulator are
+ *    [B, H, N, d]; K, V, dK, dV are [B, H_kv, N, d]; LSE and D are [B, H, N].
+ *    bf16 tensors are passed as `void*` (IEEE bfloat16 bit patterns).
+ *  * Query head h uses KV head h / (H / H_kv) (H must be a multiple of H_kv).
+ *  * d must be 64 or 128 for attn_fwd_ref and attn_bwd; preprocess and
+ *    finalize accept any d that is a multiple of 4.
+ *  * Every pointer must be 16-byte aligned (the kernels use TMA and 16-byte
+ *    vector accesses).
+ *  * `scale` is tau (usually 1/sqrt(d)); the logit is tau * q.k.
+ *  * `softcap` > 0 enables the softcap: logit = c * tanh(tau q.k / c), whose
+ *    derivative (1 - tanh^2) multiplies dS ([bwd-detail] §2.1(3)).
+ *    softcap <= 0 disables it.
+ *  * `causal` != 0 applies the lower-triangular mask: key j is visible to
+ *    query i iff j <= i (queries and keys share the length N).
+ *  * `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Every call is asynchronous on that stream.
+ *  * Return value: ATTN_OK (0) or a negative ATTN_ERR_* code. Arguments are
+ *    validated before anything is launched, so an error return means nothing
+ *    was enqueued. B, H or N equal to 0 is a valid empty problem (no launch).
+ *  * No exception crosses this interface. The library keeps one small
+ *    device status word (see attn_device_status) and caches nothing else.
+ */
+#ifndef ATTNBWD_H_
+#define ATTNBWD_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_OK 0
+#define ATTN_ERR_NULL (-1)           /* a required pointer is NULL */
+#define ATTN_ERR_SHAPE (-2)          /* negative size, H % H_kv != 0, bad scale ... */
+#define ATTN_ERR_UNSUPPORTED (-3)    /* head dimension not supported by this call */
+#define ATTN_ERR_ALIGN (-4)          /* a pointer is not 16-byte aligned */
+#define ATTN_ERR_LAUNCH (-5)         /* CUDA reported an error at launch */
+#define ATTN_ERR_DEVICE_TIMEOUT (-6) /* a kernel gave up waiting (device status) */
+#define ATTN_ERR_DEVICE (-7)         /* a kernel detected an internal fault */
+#define ATTN_ERR_TOO_LARGE (-8)      /* a size exceeds what the kernels index */
+
+/*
+ * attn_fwd_ref: simple GPU forward producing the tensors the backward needs
+ * ([bwd-detail] §1.3 saved-tensor table; [FA-v1-bwd] §1.1):
+ *   S = tau Q K^T (softcap, causal mask), LSE_i = ln sum_j exp(S_ij),
+ *   O = softmax(S) V.
+ * In:  q [B,H,N,d] bf16, k, v [B,H_kv,N,d] bf16.
+ * Out: o [B,H,N,d] bf16 (overwritten), lse [B,H,N] fp32 natural log
+ *      (overwritten).
+ * Arithmetic is fp32 with accurate exp/log/tanh; it is a reference-quality
+ * producer of O and LSE, not a tuned kernel.
+ */
+int attn_fwd_ref(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int H_kv, int N, int d, float scale, int causal, float softcap, void* stream);
+
+/*
+ * attn_bwd_preprocess: D = rowsum(dO o O) ([FA-v1-bwd] §2.4 eq. 6;
+ * [bwd-detail] §2.1(3), "dPsum", computed before the main kernel) and
+ * dq_accum := 0.
+ * In:  o, dO [B,H,N,d] bf16.
+ * Out: dpsum [B,H,N] fp32 (overwritten); dq_accum [B,H,N,d] fp32 (zeroed).
+ */
+int attn_bwd_preprocess(const void* o, const void* dO, float* dpsum, float* dq_accum, int B,
+                        int H, int N, int d, void* stream);
+
+/*
+ * attn_bwd: main backward kernel, N-outer / Q-inner ([bwd-detail] §3,
+ * [FA-v1-bwd] §4). One CTA owns 128 keys of one KV head, keeps dK and dV
+ * in tensor memory while it walks every query block of every query head of
+ * the group, and runs the five GEMMs per tile on the tensor cores:
+ *   S^T = K Q^T, dP^T = V dO^T, P = exp(S - LSE), dS = P o (dP - D)
+ *   [o (1 - tanh^2)], dV += P^T dO, dK += dS^T Q, dQ_partial = dS K.
+ * In:  q, o, dO [B,H,N,d] bf16; k, v [B,H_kv,N,d] bf16; lse [B,H,N] fp32
+ *      (natural log, from the forward); dpsum [B,H,N] fp32 (from
+ *      attn_bwd_preprocess).
+ * In/out: dq_accum [B,H,N,d] fp32: partial dQ (without the factor tau) is
+ *      ADDED with fp32 atomics; it must be zeroed first (preprocess does).
+ * Out: dk, dv [B,H_kv,N,d] bf16, overwritten; dk includes tau; for H_kv < H
+ *      they are summed over the head group.
+ * `o` is accepted for interface completeness; D already carries its use.
+ * Order on the stream: attn_bwd_preprocess, attn_bwd, attn_bwd_finalize.
+ * dQ is summed with fp32 atomics, so it may differ in the last bits from run
+ * to run; dK and dV are summed on chip in a fixed order.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+             const float* lse, float* dq_accum, void* dk, void* dv, int B, int H, int H_kv, int N,
+             int d, float scale, int causal, float softcap, const float* dpsum, void* stream);
+
+/*
+ * attn_bwd_finalize: dq = bf16(scale * dq_accum) ([FA-v1-bwd] eq. 7: the
+ * factor tau of dQ = tau dS K is applied here).
+ * In:  dq_accum [B,H,N,d] fp32.  Out: dq [B,H,N,d] bf16, overwritten.
+ */
+int attn_bwd_finalize(const float* dq_accum, void* dq, float scale, int B, int H, int N, int d,
+                      void* stream);
+
+/*
+ * attn_device_status: waits for `stream`, then reads the library's device
+ * status word into *status (0 = no fault; ATTN_ERR_DEVICE_TIMEOUT when a
+ * kernel gave up waiting on a barrier; ATTN_ERR_DEVICE for an internal
+ * check). clear != 0 resets it to 0. Returns ATTN_OK or a launch error.
+ */
+int attn_device_status(int* status, int clear, void* stream);
+
+/* Static description of an error code; never NULL. */
+const char* attn_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTNBWD_H_ */

@@ -1,0 +1,96 @@
+"""C ABI checks that need no GPU: the library builds, exports every function
+declared in include/*.h, and rejects bad arguments before launching."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from flashattention_attention_backward_gb300.build import build
+    import flashattention_attention_backward_gb300 as attn
+
+    build()
+    return attn
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    names = _declared()
+    for want in ("attn_fwd_ref", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_finalize",
+                 "attn_device_status", "attn_strerror"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from flashattention_attention_backward_gb300.build import LIB_PATH
+
+    so = ctypes.CDLL(LIB_PATH)
+    for name in _declared():
+        assert hasattr(so, name), name
+
+
+def test_strerror(lib):
+    for code in range(0, -9, -1):
+        s = lib.attn_strerror(code)
+        assert s and s != "unknown error code"
+    assert lib.attn_strerror(-100) == "unknown error code"
+
+
+FAKE = 0x10000  # a 16-byte aligned non-null address; never dereferenced
+
+
+def test_bwd_argument_validation(lib):
+    a = FAKE
+    ok = (a, a, a, a, a, a, a, a, a)
+    # null pointer
+    assert lib.attn_bwd(0, *ok[1:], 1, 2, 2, 128, 128, 0.1, 1, 0.0, a) == lib.ATTN_ERR_NULL
+    assert lib.attn_bwd(*ok, 1, 2, 2, 128, 128, 0.1, 1, 0.0, 0) == lib.ATTN_ERR_NULL
+    # bad shapes
+    assert lib.attn_bwd(*ok, 1, 3, 2, 128, 128, 0.1, 1, 0.0, a) == lib.ATTN_ERR_SHAPE
+    assert lib.attn_bwd(*ok, -1, 2, 2, 128, 128, 0.1, 1, 0.0, a) == lib.ATTN_ERR_SHAPE
+    assert lib.attn_bwd(*ok, 1, 2, 0, 128, 128, 0.1, 1, 0.0, a) == lib.ATTN_ERR_SHAPE
+    assert lib.attn_bwd(*ok, 1, 2, 2, 128, 128, float("nan"), 1, 0.0, a) == lib.ATTN_ERR_SHAPE
+    assert lib.attn_bwd(*ok, 1, 2, 2, 128, 128, 0.0, 1, 0.0, a) == lib.ATTN_ERR_SHAPE
+    # unsupported head dim
+    assert lib.attn_bwd(*ok, 1, 2, 2, 128, 96, 0.1, 1, 0.0, a) == lib.ATTN_ERR_UNSUPPORTED
+    # misaligned pointer
+    bad = list(ok)
+    bad[0] = a + 8
+    assert lib.attn_bwd(*bad, 1, 2, 2, 128, 128, 0.1, 1, 0.0, a) == lib.ATTN_ERR_ALIGN
+    # too large
+    assert lib.attn_bwd(*ok, 1, 1, 1, 1 << 30, 128, 0.1, 1, 0.0, a) == lib.ATTN_ERR_TOO_LARGE
+    # empty problems succeed without touching the device
+    assert lib.attn_bwd(*ok, 0, 2, 2, 128, 128, 0.1, 1, 0.0, a) == lib.ATTN_OK
+    assert lib.attn_bwd(*ok, 1, 2, 2, 0, 128, 0.1, 1, 0.0, a) == lib.ATTN_OK
+
+
+def test_other_entry_points_validation(lib):
+    a = FAKE
+    assert lib.attn_fwd_ref(0, a, a, a, a, 1, 1, 1, 64, 64, 0.1, 0, 0.0) == lib.ATTN_ERR_NULL
+    assert lib.attn_fwd_ref(a, a, a, a, a, 1, 1, 1, 64, 80, 0.1, 0, 0.0) == lib.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_fwd_ref(a, a, a, a, a, 1, 4, 3, 64, 64, 0.1, 0, 0.0) == lib.ATTN_ERR_SHAPE
+    assert lib.attn_fwd_ref(a, a, a, a + 4, a, 1, 1, 1, 64, 64, 0.1, 0, 0.0) == lib.ATTN_ERR_ALIGN
+    assert lib.attn_bwd_preprocess(a, a, 0, a, 1, 1, 64, 64) == lib.ATTN_ERR_NULL
+    assert lib.attn_bwd_preprocess(a, a, a, a, 1, 1, 64, 66) == lib.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_bwd_preprocess(a, a, a, a + 2, 1, 1, 64, 64) == lib.ATTN_ERR_ALIGN
+    assert lib.attn_bwd_preprocess(a, a, a, a, 1, 1, 0, 64) == lib.ATTN_OK
+    assert lib.attn_bwd_finalize(a, 0, 0.1, 1, 1, 64, 64) == lib.ATTN_ERR_NULL
+    assert lib.attn_bwd_finalize(a, a, float("inf"), 1, 1, 64, 64) == lib.ATTN_ERR_SHAPE
+    assert lib.attn_bwd_finalize(a, a, 0.1, 1, 1, 64, 64 + 2) == lib.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_bwd_finalize(a, a, 0.1, 0, 1, 64, 64) == lib.ATTN_OK
+    rc = lib.library().attn_device_status(None, 0, None)
+    assert rc == lib.ATTN_ERR_NULL
