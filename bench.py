@@ -1,0 +1,402 @@
+"""Attention-backward benchmark on GB300.
+
+One step = one whole backward pass of the causal GQA workload
+(B=2, H=32, H_kv=8, N=4096, d=128, tau=1/sqrt(d)) through the C ABI:
+attn_bwd_preprocess -> attn_bwd -> attn_bwd_finalize, inputs resident in HBM.
+The metric is backward TFLOPS (5 GEMMs of 2 N^2 d per head, halved for
+causal) and its fraction of the measured dense bf16 peak; ms per call is
+reported alongside. The per-step working set (about 353 MiB) is larger than
+L2, so no explicit flush is done between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the host
+
+Under torchrun every rank runs its own copy of the workload on its own GPU
+(weak scaling, no data-path collective); rank 0 prints one JSON line with the
+max-over-ranks time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+_CORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+import torch  # noqa: E402
+
+METRIC = "attention-backward TFLOPS and % of GB300 bf16 tensor peak; ms per bwd call"
+UNIT = "TFLOPS"
+PEAK_FALLBACK = {"bf16_tflops": 1890.0, "hbm_gbs": 6800.0, "source": "fallback"}
+KERNEL_SOURCES = ["flashattention_attention_backward_gb300/csrc/attn_bwd.cu",
+                  "flashattention_attention_backward_gb300/csrc/sm103_ptx.cuh"]
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "attn_bwd_causal_gqa_ncu.md")
+
+
+# ---------------------------------------------------------------- helpers
+def dist_env():
+    """(rank, local_rank, world_size) from the torchrun environment."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def dist_init(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, world, device=None):
+    """Max of a float over all ranks (plain host value when world == 1)."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(base, rank):
+    """Each rank draws its own synthetic batch of the same shape."""
+    return base + 7919 * rank
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(PEAK_FALLBACK)
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    try:
+        text = open(TRAFFIC_PROFILE).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch_full_workload:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, w):
+    import flashattention_attention_backward_gb300 as attn
+    from flashattention_attention_backward_gb300 import runner
+    from flashattention_attention_backward_gb300.inputs import make_inputs
+
+    rank, local_rank, world = dist_env()
+    dist_init(world, "nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    attn.library()
+
+    w = w.with_(seed_base=rank_seed(w.seed_base, rank))
+    x = make_inputs(w)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = runner.forward(q, k, v, w.scale, w.causal, w.softcap)
+    bufs = runner.BackwardBuffers(q, k)
+    stream = torch.cuda.current_stream(dev)
+    B, H, H_kv, N, d = w.B, w.H, w.H_kv, w.N, w.d
+
+    def step(ev_pair=None):
+        attn.check(attn.attn_bwd_preprocess(o, do, bufs.dpsum, bufs.dq_accum, B, H, N, d, stream))
+        if ev_pair is not None:
+            ev_pair[0].record(stream)
+        attn.check(attn.attn_bwd(q, k, v, o, do, lse, bufs.dq_accum, bufs.dk, bufs.dv, B, H, H_kv,
+                                 N, d, w.scale, w.causal, w.softcap, bufs.dpsum, stream))
+        if ev_pair is not None:
+            ev_pair[1].record(stream)
+        attn.check(attn.attn_bwd_finalize(bufs.dq_accum, bufs.dq, w.scale, B, H, N, d, stream))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    rc, status = attn.attn_device_status(clear=True, stream=stream)
+    if rc != 0 or status != 0:
+        raise RuntimeError("device status %d after warm-up" % status)
+
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    if clocks:
+        clocks.start()
+        time.sleep(0.25)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(kev[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clock_info = clocks.stop() if clocks else None
+    ms_total = t0.elapsed_time(t1)
+    bwd_ms = [a.elapsed_time(b) for a, b in kev]
+    rc, status = attn.attn_device_status(clear=True, stream=stream)
+    if rc != 0 or status != 0:
+        raise RuntimeError("device status %d after the timed region" % status)
+    ms_total = max_over_ranks(ms_total, world, dev)
+    ms_step = ms_total / args.steps
+    flops = w.flops()
+    value = world * flops * args.steps / (ms_total * 1e-3) / 1e12
+
+    # end to end: pinned host inputs -> device, backward, results -> host
+    pin = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
+    h_o, h_lse = o.cpu().pin_memory(), lse.cpu().pin_memory()
+    h_out = {n: torch.empty_like(t, device="cpu").pin_memory()
+             for n, t in (("dq", bufs.dq), ("dk", bufs.dk), ("dv", bufs.dv))}
+    h2d = sum(t.numel() * t.element_size() for t in list(pin.values()) + [h_o, h_lse])
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        q.copy_(pin["q"], non_blocking=True)
+        k.copy_(pin["k"], non_blocking=True)
+        v.copy_(pin["v"], non_blocking=True)
+        do.copy_(pin["do"], non_blocking=True)
+        o.copy_(h_o, non_blocking=True)
+        lse.copy_(h_lse, non_blocking=True)
+        step()
+        h_out["dq"].copy_(bufs.dq, non_blocking=True)
+        h_out["dk"].copy_(bufs.dk, non_blocking=True)
+        h_out["dv"].copy_(bufs.dv, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / e2e_steps
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        return None
+    peaks = measured_peaks()
+    bwd_avg = sum(bwd_ms) / len(bwd_ms)
+    achieved = flops / (bwd_avg * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded i.i.d. normal bf16 Q/K/V/dO; O and LSE from attn_fwd_ref)",
+        "config": {
+            "workload": "%s B=%d H=%d H_kv=%d N=%d d=%d %s%s" % (
+                w.name, w.B, w.H, w.H_kv, w.N, w.d, "causal" if w.causal else "non-causal",
+                (" softcap=%g" % w.softcap) if w.softcap > 0 else ""),
+            "B": w.B, "H": w.H, "H_kv": w.H_kv, "N": w.N, "d": w.d, "causal": w.causal,
+            "softcap": w.softcap, "scale": w.scale,
+            "step": "attn_bwd_preprocess + attn_bwd + attn_bwd_finalize",
+            "flops_per_step_per_gpu": flops,
+            "l2": "inputs larger than L2 (about %d MiB touched per step), no flush" % (
+                (5 * B * H * N * d * 2 + 2 * B * H_kv * N * d * 2 + 2 * B * H * N * d * 4) >> 20),
+        },
+        "bwd_ms": bwd_avg,
+        "bwd_tflops": achieved,
+        "pct_of_bf16_peak": 100.0 * achieved / peaks["bf16_tflops"],
+        "roofline": {
+            "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+            "traffic": profiled_traffic(),
+            "kernel": "attn_bwd_kernel<128, causal>",
+            "peak_source": "%s burst dense bf16 (MEASURED_PEAKS.json)" % peaks["source"],
+        },
+        "clocks": clock_info,
+        "gpu_launches": 3 * args.steps,
+        "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    return line
+
+
+# ---------------------------------------------------------------- the oracle on the host
+def _oracle_unit(x, w, b, h, M):
+    """fp64 oracle backward of query head h (batch b) on its first M rows/keys."""
+    from oracle import attention_backward
+
+    g = h // w.G
+    q = x["q"][b:b + 1, h:h + 1, :M].double().numpy()
+    do = x["do"][b:b + 1, h:h + 1, :M].double().numpy()
+    k = x["k"][b:b + 1, g:g + 1, :M].double().numpy()
+    v = x["v"][b:b + 1, g:g + 1, :M].double().numpy()
+    attention_backward(q, k, v, do, w.scale, w.causal, w.softcap)
+    f = 5.0 * 2.0 * M * M * w.d
+    return f / 2.0 if w.causal else f
+
+
+def cpu_baseline(w, budget_s=20.0):
+    """The oracle timed on the host cores on a bounded sample: whole query
+    heads of the workload (full N), as many as fit in `budget_s`."""
+    from flashattention_attention_backward_gb300.inputs import make_inputs
+
+    x = make_inputs(w.with_(B=1, H=w.G, H_kv=1))
+    flops, heads = 0.0, 0
+    t0 = time.perf_counter()
+    while heads < w.G and (heads == 0 or time.perf_counter() - t0 < budget_s / 2):
+        flops += _oracle_unit(x, w.with_(B=1, H=w.G, H_kv=1), 0, heads, w.N)
+        heads += 1
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": _CORES, "kind": "oracle",
+            "sample": "%d query head(s) x N=%d (one KV-head group of %s), fp64 numpy, %.1f s"
+                      % (heads, w.N, w.name, dt)}
+
+
+def run_reference(args, w):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return None
+    from flashattention_attention_backward_gb300.inputs import make_inputs
+
+    x = make_inputs(w.with_(B=1, H=w.G, H_kv=1))
+    wx = w.with_(B=1, H=w.G, H_kv=1)
+    # size the per-step sample so warm-up + timed steps stay within the budget
+    t0 = time.perf_counter()
+    _oracle_unit(x, wx, 0, 0, 512)
+    t512 = max(time.perf_counter() - t0, 1e-3)
+    n_units = args.steps + args.warmup
+    M = w.N
+    while M > 256 and n_units * t512 * (M / 512.0) ** 2 > args.ref_budget:
+        M //= 2
+    for i in range(args.warmup):
+        _oracle_unit(x, wx, 0, i % w.G, M)
+    flops = 0.0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flops += _oracle_unit(x, wx, 0, i % w.G, M)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    sample = ("per step: one query head of %s, first %d queries and keys (%s), fp64 numpy"
+              % (w.name, M, "causal" if w.causal else "non-causal"))
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": "%s B=%d H=%d H_kv=%d N=%d d=%d %s" % (
+            w.name, w.B, w.H, w.H_kv, w.N, w.d, "causal" if w.causal else "non-causal"),
+            "sample_rows": M},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _CORES, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    from flashattention_attention_backward_gb300.inputs import WORKLOADS
+
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="causal_gqa", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--ref-budget", type=float, default=120.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = WORKLOADS[args.workload]
+    line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    _, _, world = dist_env()
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

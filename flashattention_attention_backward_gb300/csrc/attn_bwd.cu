@@ -23,14 +23,22 @@
 // the GQA group on chip (§8.5 sums them in fp32 HBM buffers instead), so they
 // need no atomics; only dQ is accumulated globally (§3.2, §6).
 //
-// Warp roles (512 threads):
+// Warp roles (640 threads, five warpgroups; registers rebalanced with
+// setmaxnreg):
 //   warp 0       TMA producer: K, V once; Q_i (+LSE_i, D_i), dO_i per tile,
 //                two-stage rings (the two pipelines of §4.3)
 //   warp 1       tcgen05 MMA issuer (one thread), tensor-memory owner
 //   warps 4-11   softmax backward: two warpgroups, one per half of the
 //                query columns; thread = key row (tensor-memory lane);
 //                afterwards the dK/dV epilogue
-//   warps 12-15  dQ drain: tensor memory -> fp32 atomic adds into dq_accum
+//   warps 12-19  dQ drain: two warpgroups, each loads half of the dQ tile
+//                from tensor memory, frees it, then issues the fp32 atomic
+//                adds into dq_accum while the tensor cores move on
+//
+// MMA issue order, steady state: dP_t, S_{t+1}, dK_t, dQ_t, dV_{t+1}. The
+// softmax of tile t+1 (P) and of tile t (dS) thus overlap tensor-core work,
+// and the dQ reduction (bounded by the L2 reduction rate, about 6 TB/s on
+// GB300) overlaps the next tile instead of stalling it.
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   [  0,128)  S^T (fp32); P^T (bf16 pairs) overwrites the read part
@@ -52,7 +60,10 @@ using namespace ptx;
 
 constexpr int kBc = 128;  // keys per CTA (tensor-memory lanes)
 constexpr int kBr = 128;  // queries per tile
-constexpr int kThreads = 512;
+constexpr int kThreads = 640;
+// registers per thread after setmaxnreg (launch: 640 x 96)
+constexpr int kRegsCtl = 64, kRegsSoftmax = 136, kRegsDq = 72;
+static_assert(128 * (kRegsCtl + 2 * kRegsSoftmax + 2 * kRegsDq) <= kThreads * 96, "register pool");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitLimitCycles = 2000000000LL;  // about one second
 
@@ -239,84 +250,102 @@ __device__ void producer_role(const Ctx& c, const Params& p, const Work& w, uint
 
 // ------------------------------------------------------------------ MMA issuer
 template <int D>
-__device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t tmem) {
-  using L = Layout<D>;
-  constexpr int kKSteps = D / 16;      // S, dP: reduction over d
-  constexpr int kQSteps = kBr / 16;    // dV, dK: reduction over queries
-  constexpr int kKeySteps = kBc / 16;  // dQ: reduction over keys
-  constexpr uint32_t kIdS = make_idesc_bf16(kBc, kBr, false, false);
-  constexpr uint32_t kIdKV = make_idesc_bf16(kBc, D, false, true);
+struct Mma {
+  static constexpr int kKSteps = D / 16;      // S, dP: reduction over d
+  static constexpr int kQSteps = kBr / 16;    // dV, dK: reduction over queries
+  static constexpr int kKeySteps = kBc / 16;  // dQ: reduction over keys
+  static constexpr uint32_t kIdS = make_idesc_bf16(kBc, kBr, false, false);
+  static constexpr uint32_t kIdKV = make_idesc_bf16(kBc, D, false, true);
   // d = 128: dQ^T = K^T dS^T (M = d lanes, N = queries), drained coalesced
   // d =  64: dQ   = dS K     (M = query lanes, N = d)
-  constexpr uint32_t kIdQ =
+  static constexpr uint32_t kIdQ =
       D == 128 ? make_idesc_bf16(D, kBr, true, true) : make_idesc_bf16(kBr, D, true, true);
+
+  // S^T = K Q^T or dP^T = V dO^T (both operands K-major, 128-byte swizzle)
+  static __device__ __forceinline__ void nt(uint32_t d_tmem, uint32_t sa, uint32_t sb) {
+#pragma unroll
+    for (int k = 0; k < kKSteps; ++k) {
+      const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+      mma_ss(d_tmem, make_sdesc(sa + off, 16, 1024), make_sdesc(sb + off, 16, 1024), kIdS, k > 0);
+    }
+  }
+  // dV += P^T dO or dK += dS^T Q: A (bf16 pairs) from tensor memory, B MN-major
+  static __device__ __forceinline__ void tn(uint32_t d_tmem, uint32_t a_tmem, uint32_t sb,
+                                            bool accumulate) {
+#pragma unroll
+    for (int k = 0; k < kQSteps; ++k) {
+      const uint32_t acol = 8 * k + (k >= 4 ? 32 : 0);
+      mma_ts(d_tmem, a_tmem + acol, make_sdesc(sb + 2048 * k, 16384, 1024), kIdKV,
+             (accumulate || k > 0) ? 1u : 0u);
+    }
+  }
+  // dQ tile from the shared dS^T tile and K (both MN-major)
+  static __device__ __forceinline__ void dq(uint32_t d_tmem, uint32_t sK, uint32_t sDS) {
+#pragma unroll
+    for (int k = 0; k < kKeySteps; ++k) {
+      if (D == 128)
+        mma_ss(d_tmem, make_sdesc(sK + 2048 * k, 16384, 1024),
+               make_sdesc(sDS + 2048 * k, 16384, 1024), kIdQ, k > 0);
+      else
+        mma_ss(d_tmem, make_sdesc(sDS + 2048 * k, 16384, 1024),
+               make_sdesc(sK + 2048 * k, 16384, 1024), kIdQ, k > 0);
+    }
+  }
+};
+
+// Tensor-memory reuse relies on tcgen05 MMAs of one thread running in issue
+// order: a GEMM that overwrites a region is always issued after the GEMM that
+// reads what the region held (P^T before S, dS^T before the dQ tile).
+template <int D>
+__device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t tmem) {
+  using L = Layout<D>;
+  using M = Mma<D>;
   const uint32_t tS = tmem + 0, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
   const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sDS = sbase + L::kDS;
+  auto sQ = [&](int t) { return sbase + ((t & 1) ? L::kQ1 : L::kQ0); };
+  auto sDO = [&](int t) { return sbase + ((t & 1) ? L::kDO1 : L::kDO0); };
+  auto ph = [](int t) { return static_cast<uint32_t>((t >> 1) & 1); };
 
-  if (wait(c, BAR_KV, 0)) {
+  bool ok = wait(c, BAR_KV, 0);
+  // prologue: S_0, then dV_0 once P_0 is ready
+  if (ok && (ok = wait(c, BAR_Q_FULL + 0, 0))) {
     tc_fence_after();
-    for (int t = 0; t < w.T; ++t) {
-      const int st = t & 1;
-      const uint32_t ph = (t >> 1) & 1;
-      const uint32_t sQ = sbase + (st ? L::kQ1 : L::kQ0);
-      const uint32_t sDO = sbase + (st ? L::kDO1 : L::kDO0);
-
-      // S^T = K Q^T. The S region held P of the previous tile, read by the
-      // dV GEMM issued before: tcgen05 MMAs of one thread run in order.
-      if (!wait(c, BAR_Q_FULL + st, ph)) break;
+    M::nt(tS, sK, sQ(0));
+    mma_commit(bar_addr(c, BAR_S_FULL));
+  }
+  if (ok && (ok = wait(c, BAR_DO_FULL + 0, 0)) && (ok = wait(c, BAR_P_FULL, 0))) {
+    tc_fence_after();
+    M::tn(tdV, tS, sDO(0), false);
+  }
+  for (int t = 0; ok && t < w.T; ++t) {
+    const int st = t & 1;
+    // dP_t = V dO_t^T into the dP region, once the dQ tile of t-1 has left it
+    if (t > 0 && !(ok = wait(c, BAR_DQ_EMPTY, (t - 1) & 1))) break;
+    tc_fence_after();
+    M::nt(tdP, sV, sDO(t));
+    mma_commit(bar_addr(c, BAR_DP_FULL));
+    mma_commit(bar_addr(c, BAR_DO_EMPTY + st));  // dV_t and dP_t were dO_t's readers
+    // S_{t+1} = K Q_{t+1}^T into the S region (P_t^T there was read by dV_t)
+    if (t + 1 < w.T) {
+      if (!(ok = wait(c, BAR_Q_FULL + ((t + 1) & 1), ph(t + 1)))) break;
       tc_fence_after();
-#pragma unroll
-      for (int k = 0; k < kKSteps; ++k) {
-        const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-        mma_ss(tS, make_sdesc(sK + off, 16, 1024), make_sdesc(sQ + off, 16, 1024), kIdS, k > 0);
-      }
+      M::nt(tS, sK, sQ(t + 1));
       mma_commit(bar_addr(c, BAR_S_FULL));
-
-      // dP^T = V dO^T, once the previous dQ tile has left the dP region.
-      if (!wait(c, BAR_DO_FULL + st, ph)) break;
-      if (t > 0 && !wait(c, BAR_DQ_EMPTY, (t - 1) & 1)) break;
+    }
+    // dK += dS_t^T Q_t
+    if (!(ok = wait(c, BAR_DS_FULL, t & 1))) break;
+    tc_fence_after();
+    M::tn(tdK, tdP, sQ(t), t > 0);
+    mma_commit(bar_addr(c, BAR_Q_EMPTY + st));
+    // dQ tile of t into the dP region (dS_t^T there was read by dK_t)
+    M::dq(tdP, sK, sDS);
+    mma_commit(bar_addr(c, BAR_DQ_FULL));
+    // dV += P_{t+1}^T dO_{t+1}
+    if (t + 1 < w.T) {
+      if (!(ok = wait(c, BAR_DO_FULL + ((t + 1) & 1), ph(t + 1)))) break;
+      if (!(ok = wait(c, BAR_P_FULL, (t + 1) & 1))) break;
       tc_fence_after();
-#pragma unroll
-      for (int k = 0; k < kKSteps; ++k) {
-        const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-        mma_ss(tdP, make_sdesc(sV + off, 16, 1024), make_sdesc(sDO + off, 16, 1024), kIdS,
-               k > 0);
-      }
-      mma_commit(bar_addr(c, BAR_DP_FULL));
-
-      // dV += P^T dO (A = P^T from tensor memory, B = dO MN-major)
-      if (!wait(c, BAR_P_FULL, t & 1)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int k = 0; k < kQSteps; ++k) {
-        const uint32_t acol = 8 * k + (k >= 4 ? 32 : 0);
-        mma_ts(tdV, tS + acol, make_sdesc(sDO + 2048 * k, 16384, 1024), kIdKV,
-               (t > 0 || k > 0) ? 1u : 0u);
-      }
-      mma_commit(bar_addr(c, BAR_DO_EMPTY + st));
-
-      // dK += dS^T Q (A = dS^T from tensor memory, B = Q MN-major)
-      if (!wait(c, BAR_DS_FULL, t & 1)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int k = 0; k < kQSteps; ++k) {
-        const uint32_t acol = 8 * k + (k >= 4 ? 32 : 0);
-        mma_ts(tdK, tdP + acol, make_sdesc(sQ + 2048 * k, 16384, 1024), kIdKV,
-               (t > 0 || k > 0) ? 1u : 0u);
-      }
-      mma_commit(bar_addr(c, BAR_Q_EMPTY + st));
-
-      // dQ tile into the dP region (dS^T there was consumed by the dK GEMM)
-#pragma unroll
-      for (int k = 0; k < kKeySteps; ++k) {
-        if (D == 128)
-          mma_ss(tdP, make_sdesc(sK + 2048 * k, 16384, 1024),
-                 make_sdesc(sDS + 2048 * k, 16384, 1024), kIdQ, k > 0);
-        else
-          mma_ss(tdP, make_sdesc(sDS + 2048 * k, 16384, 1024),
-                 make_sdesc(sK + 2048 * k, 16384, 1024), kIdQ, k > 0);
-      }
-      mma_commit(bar_addr(c, BAR_DQ_FULL));
+      M::tn(tdV, tS, sDO(t + 1), true);
     }
   }
   // Completion of everything issued; the epilogue waits on it.
@@ -483,10 +512,15 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8
 }
 
 // ------------------------------------------------------------------ dQ drain
+// Two warpgroups, each owning half of the dQ tile's columns. A thread loads
+// its share from tensor memory, the warp frees the region (DQ_EMPTY), and
+// only then are the fp32 atomic adds issued, so the reduction overlaps the
+// next tile's GEMMs.
 template <int D>
 __device__ void dq_role(const Ctx& c, const Params& p, const Work& w, uint32_t tmem) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int part = (warp - 12) >> 2;  // which half of the tile
   const int r = ((warp & 3) << 5) + lane;
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
   for (int t = 0; t < w.T; ++t) {
@@ -499,41 +533,36 @@ __device__ void dq_role(const Ctx& c, const Params& p, const Work& w, uint32_t t
     if (D == 128) {
       // lane r holds dQ[m0 + i][r] in column 128 + i: one warp instruction
       // adds 32 consecutive floats (one 128-byte line) of a dQ row.
-      float* dst = p.dq_accum + (bh * p.N + m0) * D + r;
-      const bool full = m0 + kBr <= p.N;
-#pragma unroll
-      for (int hv = 0; hv < 2; ++hv) {
-        uint32_t v[64];
-        uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
-        uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
-        tmem_ld32(tmem + lane_base + 128 + hv * 64, v0);
-        tmem_ld32(tmem + lane_base + 128 + hv * 64 + 32, v1);
-            if (hv == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_addr(c, BAR_DQ_EMPTY));
-        }
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int i = hv * 64 + j;
-          if (full || m0 + i < p.N) red_add_f32(dst + static_cast<long long>(i) * D,
-                                                __uint_as_float(v[j]));
-        }
-      }
-    } else {
-      // lane r holds query row m0 + r, columns 128 + [0, 64) = dQ[m0 + r][:]
       uint32_t v[64];
       uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
       uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
-      tmem_ld32(tmem + lane_base + 128, v0);
-      tmem_ld32(tmem + lane_base + 128 + 32, v1);
-        tc_fence_before();
+      tmem_ld32(tmem + lane_base + 128 + part * 64, v0);
+      tmem_ld32(tmem + lane_base + 128 + part * 64 + 32, v1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_addr(c, BAR_DQ_EMPTY));
+      const int i0 = m0 + part * 64;
+      float* dst = p.dq_accum + (bh * p.N + i0) * D + r;
+      if (i0 + 64 <= p.N) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          red_add_f32(dst + static_cast<long long>(j) * D, __uint_as_float(v[j]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          if (i0 + j < p.N) red_add_f32(dst + static_cast<long long>(j) * D, __uint_as_float(v[j]));
+      }
+    } else {
+      // lane r holds query row m0 + r; columns 128 + [0, 64) are dQ[m0 + r][:]
+      uint32_t v[32];
+      tmem_ld32(tmem + lane_base + 128 + part * 32, v);
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_addr(c, BAR_DQ_EMPTY));
       if (m0 + r < p.N) {
-        float* dst = p.dq_accum + (bh * p.N + m0 + r) * D;
+        float* dst = p.dq_accum + (bh * p.N + m0 + r) * D + part * 32;
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
+        for (int u = 0; u < 8; ++u)
           red_add_v4_f32(dst + 4 * u, __uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
                          __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
       }
@@ -585,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_addr(c, BAR_DP_FULL), 1);
     mbar_init(bar_addr(c, BAR_DS_FULL), 8);
     mbar_init(bar_addr(c, BAR_DQ_FULL), 1);
-    mbar_init(bar_addr(c, BAR_DQ_EMPTY), 4);
+    mbar_init(bar_addr(c, BAR_DQ_EMPTY), 8);
     mbar_init(bar_addr(c, BAR_KV_DONE), 1);
     *c.abort = 0;
     fence_barrier_init();
@@ -599,14 +628,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
 
-  if (warp == 0) {
-    producer_role<D>(c, p, w, smem, sbase, &tm_q, &tm_k, &tm_v, &tm_do);
-  } else if (warp == 1) {
-    if ((threadIdx.x & 31) == 0) mma_role<D>(c, w, sbase, tmem);
-    __syncwarp();
-  } else if (warp >= 4 && warp < 12) {
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsCtl>();
+    if (warp == 0) {
+      producer_role<D>(c, p, w, smem, sbase, &tm_q, &tm_k, &tm_v, &tm_do);
+    } else if (warp == 1) {
+      if ((threadIdx.x & 31) == 0) mma_role<D>(c, w, sbase, tmem);
+      __syncwarp();
+    }
+  } else if (warp < 12) {
+    setmaxnreg_inc<kRegsSoftmax>();
     softmax_role<D, CAUSAL, SOFTCAP>(c, p, w, smem, sbase, tmem);
-  } else if (warp >= 12) {
+  } else {
+    setmaxnreg_dec<kRegsDq>();
     dq_role<D>(c, p, w, tmem);
   }
   tc_fence_before();
