@@ -13,13 +13,13 @@
 //   P    = exp2(S^T * tau*log2e - LSE*log2e)   [softcap: tau*S -> c tanh(tau*S/c)]
 //   dS   = P o (dP - D)              [softcap: o (1 - tanh^2)]
 //   dV_j += P^T dO_i                 (P^T taken from tensor memory)
-//   dK_j += dS^T Q_i                 (dS^T taken from tensor memory)
+//   dK_j += dS^T Q_i                 (dS^T from shared memory)
 //   dQ_i += dS K_j                   (dS from shared memory; fp32 atomics)
 //
-// Because S^T is computed with keys on the tensor-memory lanes, P^T and dS^T
-// already sit in the layout the dV/dK GEMMs want as their A operand, so they
-// never pass through shared memory (the analogue of feeding P/dS from
-// registers to the dK/dV GEMM, "反向传播算法详解" §8.2). dK/dV are summed over
+// Because S^T is computed with keys on the tensor-memory lanes, P^T already
+// sits in the layout the dV GEMM wants as its A operand and never passes
+// through shared memory (the analogue of feeding P from registers to the dV
+// GEMM, "反向传播算法详解" §8.2). dK/dV are summed over
 // the GQA group on chip (§8.5 sums them in fp32 HBM buffers instead), so they
 // need no atomics; only dQ is accumulated globally (§3.2, §6).
 //
@@ -35,15 +35,18 @@
 //                from tensor memory, frees it, then issues the fp32 atomic
 //                adds into dq_accum while the tensor cores move on
 //
-// MMA issue order, steady state: dP_t, S_{t+1}, dK_t, dQ_t, dV_{t+1}. The
-// softmax of tile t+1 (P) and of tile t (dS) thus overlap tensor-core work,
-// and the dQ reduction (bounded by the L2 reduction rate, about 6 TB/s on
-// GB300) overlaps the next tile instead of stalling it.
+// MMA issue order per tile: dP_t, dV_t, S_{t+1}, dQ_t, dK_t. The P phase of
+// tile t+1 overlaps dQ_t/dK_t, dK_t overlaps the dQ drain, and only
+// dP -> dS -> dQ -> drain forms the per-tile dependency chain. The dQ atomic
+// reduction (bounded by the L2 reduction rate, about 6 TB/s on GB300)
+// overlaps the next tile instead of stalling it.
 //
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   [  0,128)  S^T (fp32); P^T (bf16 pairs) overwrites the read part
-//   [128,256)  dP^T (fp32); dS^T (bf16 pairs), then the dQ tile, reuse it
+//   [128,256)  dP^T (fp32), then the dQ tile of the same query block
 //   [256,384)  dV accumulator     [384,512)  dK accumulator
+// dS^T goes to shared memory only ([key][query], 128-byte swizzle): it is the
+// K-major A operand of dK += dS^T Q and the MN-major B operand of the dQ GEMM.
 //
 // Every wait on an mbarrier is bounded: on timeout the kernel records
 // ATTN_ERR_DEVICE_TIMEOUT in the device status word and all roles return.
@@ -82,7 +85,7 @@ struct Layout {
   static constexpr int kLSE = kDS + kBc * kBr * 2;  // 2 stages x 128 fp32 (LSE*log2e)
   static constexpr int kDsum = kLSE + 2 * kBr * 4;  // 2 stages x 128 fp32 (D)
   static constexpr int kBars = kDsum + 2 * kBr * 4;
-  static constexpr int kNumBars = 16;
+  static constexpr int kNumBars = 17;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kBytes = kAbort + 12;
@@ -102,6 +105,7 @@ enum Bar {
   BAR_DQ_FULL = 13,
   BAR_DQ_EMPTY = 14,
   BAR_KV_DONE = 15,
+  BAR_DS_FREE = 16,
 };
 
 struct Params {
@@ -260,35 +264,48 @@ struct Mma {
   // d =  64: dQ   = dS K     (M = query lanes, N = d)
   static constexpr uint32_t kIdQ =
       D == 128 ? make_idesc_bf16(D, kBr, true, true) : make_idesc_bf16(kBr, D, true, true);
-
-  // S^T = K Q^T or dP^T = V dO^T (both operands K-major, 128-byte swizzle)
-  static __device__ __forceinline__ void nt(uint32_t d_tmem, uint32_t sa, uint32_t sb) {
-#pragma unroll
-    for (int k = 0; k < kKSteps; ++k) {
-      const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-      mma_ss(d_tmem, make_sdesc(sa + off, 16, 1024), make_sdesc(sb + off, 16, 1024), kIdS, k > 0);
-    }
+  // byte offset of K-step k in a K-major 128-byte-swizzled tile (64 elements
+  // per 16 KB column block) and in an MN-major one (16 rows = 2 KB per step)
+  static __device__ __forceinline__ constexpr uint32_t kmaj(int k) {
+    return ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
   }
-  // dV += P^T dO or dK += dS^T Q: A (bf16 pairs) from tensor memory, B MN-major
-  static __device__ __forceinline__ void tn(uint32_t d_tmem, uint32_t a_tmem, uint32_t sb,
+  static __device__ __forceinline__ constexpr uint32_t mnmaj(int k) { return (2048 * k) >> 4; }
+
+  // S^T = K Q^T or dP^T = V dO^T (both operands K-major); a, b = low words
+  static __device__ __forceinline__ void nt(uint32_t d_tmem, uint32_t a, uint32_t b) {
+#pragma unroll
+    for (int k = 0; k < kKSteps; ++k)
+      mma_ss(d_tmem, sdesc_from_lo(a + kmaj(k)), sdesc_from_lo(b + kmaj(k)), kIdS, k > 0);
+  }
+  // dV += P^T dO: A (bf16 pairs) from tensor memory, B MN-major
+  static __device__ __forceinline__ void tn(uint32_t d_tmem, uint32_t a_tmem, uint32_t b,
                                             bool accumulate) {
 #pragma unroll
     for (int k = 0; k < kQSteps; ++k) {
       const uint32_t acol = 8 * k + (k >= 4 ? 32 : 0);
-      mma_ts(d_tmem, a_tmem + acol, make_sdesc(sb + 2048 * k, 16384, 1024), kIdKV,
+      mma_ts(d_tmem, a_tmem + acol, sdesc_from_lo(b + mnmaj(k)), kIdKV,
              (accumulate || k > 0) ? 1u : 0u);
     }
   }
-  // dQ tile from the shared dS^T tile and K (both MN-major)
-  static __device__ __forceinline__ void dq(uint32_t d_tmem, uint32_t sK, uint32_t sDS) {
+  // dK += dS^T Q: A = dS^T from the shared tile ([key][query], which is the
+  // K-major layout of an M = keys, K = queries operand), B = Q MN-major
+  static __device__ __forceinline__ void dk(uint32_t d_tmem, uint32_t ds_k, uint32_t q_mn,
+                                            bool accumulate) {
+#pragma unroll
+    for (int k = 0; k < kQSteps; ++k)
+      mma_ss(d_tmem, sdesc_from_lo(ds_k + kmaj(k)), sdesc_from_lo(q_mn + mnmaj(k)), kIdKV,
+             (accumulate || k > 0) ? 1u : 0u);
+  }
+  // dQ tile from the shared dS^T tile and K (both MN-major low words)
+  static __device__ __forceinline__ void dq(uint32_t d_tmem, uint32_t k_mn, uint32_t ds_mn) {
 #pragma unroll
     for (int k = 0; k < kKeySteps; ++k) {
       if (D == 128)
-        mma_ss(d_tmem, make_sdesc(sK + 2048 * k, 16384, 1024),
-               make_sdesc(sDS + 2048 * k, 16384, 1024), kIdQ, k > 0);
+        mma_ss(d_tmem, sdesc_from_lo(k_mn + mnmaj(k)), sdesc_from_lo(ds_mn + mnmaj(k)), kIdQ,
+               k > 0);
       else
-        mma_ss(d_tmem, make_sdesc(sDS + 2048 * k, 16384, 1024),
-               make_sdesc(sK + 2048 * k, 16384, 1024), kIdQ, k > 0);
+        mma_ss(d_tmem, sdesc_from_lo(ds_mn + mnmaj(k)), sdesc_from_lo(k_mn + mnmaj(k)), kIdQ,
+               k > 0);
     }
   }
 };
@@ -296,56 +313,66 @@ struct Mma {
 // Tensor-memory reuse relies on tcgen05 MMAs of one thread running in issue
 // order: a GEMM that overwrites a region is always issued after the GEMM that
 // reads what the region held (P^T before S, dS^T before the dQ tile).
+// Descriptor low words are formed once; the loop only adds constants, which
+// keeps the single issuing thread ahead of the tensor cores.
 template <int D>
 __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t tmem) {
   using L = Layout<D>;
   using M = Mma<D>;
   const uint32_t tS = tmem + 0, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
-  const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sDS = sbase + L::kDS;
-  auto sQ = [&](int t) { return sbase + ((t & 1) ? L::kQ1 : L::kQ0); };
-  auto sDO = [&](int t) { return sbase + ((t & 1) ? L::kDO1 : L::kDO0); };
+  const uint32_t kK = sdesc_lo(sbase + L::kK, 16), kV = sdesc_lo(sbase + L::kV, 16);
+  const uint32_t kQ0 = sdesc_lo(sbase + L::kQ0, 16), kQ1 = sdesc_lo(sbase + L::kQ1, 16);
+  const uint32_t kO0 = sdesc_lo(sbase + L::kDO0, 16), kO1 = sdesc_lo(sbase + L::kDO1, 16);
+  const uint32_t mK = sdesc_lo(sbase + L::kK, 16384), mDS = sdesc_lo(sbase + L::kDS, 16384);
+  const uint32_t kDS = sdesc_lo(sbase + L::kDS, 16);
+  const uint32_t mQ0 = sdesc_lo(sbase + L::kQ0, 16384), mQ1 = sdesc_lo(sbase + L::kQ1, 16384);
+  const uint32_t mO0 = sdesc_lo(sbase + L::kDO0, 16384), mO1 = sdesc_lo(sbase + L::kDO1, 16384);
   auto ph = [](int t) { return static_cast<uint32_t>((t >> 1) & 1); };
 
   bool ok = wait(c, BAR_KV, 0);
-  // prologue: S_0, then dV_0 once P_0 is ready
+  // prologue: S_0, dP_0
   if (ok && (ok = wait(c, BAR_Q_FULL + 0, 0))) {
     tc_fence_after();
-    M::nt(tS, sK, sQ(0));
+    M::nt(tS, kK, kQ0);
     mma_commit(bar_addr(c, BAR_S_FULL));
   }
-  if (ok && (ok = wait(c, BAR_DO_FULL + 0, 0)) && (ok = wait(c, BAR_P_FULL, 0))) {
+  if (ok && (ok = wait(c, BAR_DO_FULL + 0, 0))) {
     tc_fence_after();
-    M::tn(tdV, tS, sDO(0), false);
+    M::nt(tdP, kV, kO0);
+    mma_commit(bar_addr(c, BAR_DP_FULL));
   }
   for (int t = 0; ok && t < w.T; ++t) {
     const int st = t & 1;
-    // dP_t = V dO_t^T into the dP region, once the dQ tile of t-1 has left it
-    if (t > 0 && !(ok = wait(c, BAR_DQ_EMPTY, (t - 1) & 1))) break;
+    const uint32_t kQn = st ? kQ0 : kQ1, kOn = st ? kO0 : kO1;
+    const uint32_t mQ = st ? mQ1 : mQ0, mO = st ? mO1 : mO0;
+    // dV += P_t^T dO_t (A = P_t^T in the S region)
+    if (!(ok = wait(c, BAR_P_FULL, t & 1))) break;
     tc_fence_after();
-    M::nt(tdP, sV, sDO(t));
-    mma_commit(bar_addr(c, BAR_DP_FULL));
-    mma_commit(bar_addr(c, BAR_DO_EMPTY + st));  // dV_t and dP_t were dO_t's readers
+    M::tn(tdV, tS, mO, t > 0);
+    mma_commit(bar_addr(c, BAR_DO_EMPTY + st));  // dP_t and dV_t were dO_t's readers
     // S_{t+1} = K Q_{t+1}^T into the S region (P_t^T there was read by dV_t)
     if (t + 1 < w.T) {
-      if (!(ok = wait(c, BAR_Q_FULL + ((t + 1) & 1), ph(t + 1)))) break;
+      if (!(ok = wait(c, BAR_Q_FULL + (st ^ 1), ph(t + 1)))) break;
       tc_fence_after();
-      M::nt(tS, sK, sQ(t + 1));
+      M::nt(tS, kK, kQn);
       mma_commit(bar_addr(c, BAR_S_FULL));
     }
-    // dK += dS_t^T Q_t
+    // dQ tile of t into the dP region (the softmax has read dP_t), then
+    // dK += dS_t^T Q_t, both from the shared dS tile
     if (!(ok = wait(c, BAR_DS_FULL, t & 1))) break;
     tc_fence_after();
-    M::tn(tdK, tdP, sQ(t), t > 0);
-    mma_commit(bar_addr(c, BAR_Q_EMPTY + st));
-    // dQ tile of t into the dP region (dS_t^T there was read by dK_t)
-    M::dq(tdP, sK, sDS);
+    M::dq(tdP, mK, mDS);
     mma_commit(bar_addr(c, BAR_DQ_FULL));
-    // dV += P_{t+1}^T dO_{t+1}
+    M::dk(tdK, kDS, mQ, t > 0);
+    mma_commit(bar_addr(c, BAR_Q_EMPTY + st));
+    mma_commit(bar_addr(c, BAR_DS_FREE));
+    // dP_{t+1} = V dO_{t+1}^T once the dQ tile has been drained
     if (t + 1 < w.T) {
-      if (!(ok = wait(c, BAR_DO_FULL + ((t + 1) & 1), ph(t + 1)))) break;
-      if (!(ok = wait(c, BAR_P_FULL, (t + 1) & 1))) break;
+      if (!(ok = wait(c, BAR_DO_FULL + (st ^ 1), ph(t + 1)))) break;
+      if (!(ok = wait(c, BAR_DQ_EMPTY, t & 1))) break;
       tc_fence_after();
-      M::tn(tdV, tS, sDO(t + 1), true);
+      M::nt(tdP, kV, kOn);
+      mma_commit(bar_addr(c, BAR_DP_FULL));
     }
   }
   // Completion of everything issued; the epilogue waits on it.
@@ -374,15 +401,12 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
   // ---- P = exp(S - LSE) -> bf16 P^T in tensor memory
   if (!wait(c, BAR_S_FULL, t & 1)) return false;
   tc_fence_after();
+  {
+    uint32_t raw[64];
+    tmem_ld32x2(tmem + lane_base + half * 64, tmem + lane_base + half * 64 + 32, raw);
 #pragma unroll
-  for (int ch = 0; ch < 4; ++ch) {
-    const int col0 = half * 64 + ch * 16;
-    uint32_t raw[16];
-    tmem_ld16(tmem + lane_base + col0, raw);
-    float pv[16];
-#pragma unroll
-    for (int j4 = 0; j4 < 4; ++j4) {
-      const float4 l4 = *reinterpret_cast<const float4*>(s_lse + col0 + 4 * j4);
+    for (int j4 = 0; j4 < 16; ++j4) {
+      const float4 l4 = *reinterpret_cast<const float4*>(s_lse + half * 64 + 4 * j4);
       const float lse4[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -400,60 +424,68 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
           keep = prob;
         }
         if (MASKED) {
-          const int q = m0 + col0 + j;
+          const int q = m0 + half * 64 + j;
           const bool ok = key < p.N && q < p.N && (!CAUSAL || key <= q);
           prob = ok ? prob : 0.f;
           keep = ok ? keep : 0.f;
         }
-        pv[j] = prob;
-        pk[ch * 16 + j] = keep;
+        raw[j] = __float_as_uint(prob);
+        pk[j] = keep;
       }
     }
-    uint32_t packed[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) packed[u] = pack_bf16x2(pv[2 * u], pv[2 * u + 1]);
-    tmem_st8(tmem + lane_base + half * 64 + ch * 8, packed);
+    for (int ch = 0; ch < 4; ++ch) {
+      uint32_t packed[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        packed[u] = pack_bf16x2(__uint_as_float(raw[16 * ch + 2 * u]),
+                                __uint_as_float(raw[16 * ch + 2 * u + 1]));
+      tmem_st8(tmem + lane_base + half * 64 + ch * 8, packed);
+    }
   }
   tmem_wait_st();
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(bar_addr(c, BAR_P_FULL));
 
-  // ---- dS = P o (dP - D) -> bf16 dS^T in tensor memory and shared memory
+  // ---- dS = P o (dP - D) -> bf16 dS^T in shared memory
   if (!wait(c, BAR_DP_FULL, t & 1)) return false;
-  // the previous dQ GEMM must be done reading the shared dS tile
-  if (t > 0 && !wait(c, BAR_DQ_FULL, (t - 1) & 1)) return false;
+  // the previous tile's dQ and dK GEMMs must be done reading the shared dS tile
+  if (t > 0 && !wait(c, BAR_DS_FREE, (t - 1) & 1)) return false;
   tc_fence_after();
   const uint32_t ds_row = sbase + L::kDS + half * 16384 + r * 128;
 #pragma unroll
-  for (int ch = 0; ch < 4; ++ch) {
-    const int col0 = half * 64 + ch * 16;
-    uint32_t raw[16];
-    tmem_ld16(tmem + lane_base + 128 + col0, raw);
-    float ds[16];
+  for (int hh = 0; hh < 2; ++hh) {
+    const int col0 = half * 64 + hh * 32;
+    uint32_t raw[32];
+    tmem_ld32(tmem + lane_base + 128 + col0, raw);
 #pragma unroll
-    for (int j4 = 0; j4 < 4; ++j4) {
+    for (int j4 = 0; j4 < 8; ++j4) {
       const float4 d4 = *reinterpret_cast<const float4*>(s_d + col0 + 4 * j4);
       const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int j = 4 * j4 + e;
-        ds[j] = pk[ch * 16 + j] * (__uint_as_float(raw[j]) - dd[e]);
+        raw[j] = __float_as_uint(pk[hh * 32 + j] * (__uint_as_float(raw[j]) - dd[e]));
       }
     }
-    uint32_t packed[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) packed[u] = pack_bf16x2(ds[2 * u], ds[2 * u + 1]);
-    tmem_st8(tmem + lane_base + 128 + half * 64 + ch * 8, packed);
-    // dS^T row r, queries [col0, col0+16): 16-byte chunks 2ch, 2ch+1 of the
-    // 128-byte row, placed by the 128-byte swizzle (chunk ^ (row & 7))
-    st_shared_v4(ds_row + (((2 * ch) ^ (r & 7)) << 4), packed[0], packed[1], packed[2],
-                 packed[3]);
-    st_shared_v4(ds_row + (((2 * ch + 1) ^ (r & 7)) << 4), packed[4], packed[5], packed[6],
-                 packed[7]);
+    for (int ch = 0; ch < 2; ++ch) {
+      uint32_t packed[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        packed[u] = pack_bf16x2(__uint_as_float(raw[16 * ch + 2 * u]),
+                                __uint_as_float(raw[16 * ch + 2 * u + 1]));
+      const int c16 = hh * 2 + ch;  // 16-query chunk within this half
+      // dS^T row r, queries [16 c16, 16 c16 + 16) of this half: 16-byte chunks
+      // 2 c16, 2 c16 + 1 of the 128-byte row, placed by the 128-byte swizzle
+      st_shared_v4(ds_row + (((2 * c16) ^ (r & 7)) << 4), packed[0], packed[1], packed[2],
+                   packed[3]);
+      st_shared_v4(ds_row + (((2 * c16 + 1) ^ (r & 7)) << 4), packed[4], packed[5], packed[6],
+                   packed[7]);
+    }
   }
   fence_proxy_async_smem();
-  tmem_wait_st();
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(bar_addr(c, BAR_DS_FULL));
@@ -534,10 +566,7 @@ __device__ void dq_role(const Ctx& c, const Params& p, const Work& w, uint32_t t
       // lane r holds dQ[m0 + i][r] in column 128 + i: one warp instruction
       // adds 32 consecutive floats (one 128-byte line) of a dQ row.
       uint32_t v[64];
-      uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
-      uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
-      tmem_ld32(tmem + lane_base + 128 + part * 64, v0);
-      tmem_ld32(tmem + lane_base + 128 + part * 64 + 32, v1);
+      tmem_ld32x2(tmem + lane_base + 128 + part * 64, tmem + lane_base + 128 + part * 64 + 32, v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_addr(c, BAR_DQ_EMPTY));
@@ -616,6 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_addr(c, BAR_DQ_FULL), 1);
     mbar_init(bar_addr(c, BAR_DQ_EMPTY), 8);
     mbar_init(bar_addr(c, BAR_KV_DONE), 1);
+    mbar_init(bar_addr(c, BAR_DS_FREE), 1);
     *c.abort = 0;
     fence_barrier_init();
   }
