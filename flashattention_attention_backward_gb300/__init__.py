@@ -15,7 +15,7 @@ from .build import LIB_PATH
 
 __all__ = [
     "AttnError", "check", "library", "attn_fwd_ref", "attn_bwd_preprocess", "attn_bwd",
-    "attn_bwd_finalize", "attn_device_status", "attn_strerror",
+    "attn_bwd_finalize", "attn_bwd_noalloc", "attn_device_status", "attn_strerror",
     "ATTN_OK", "ATTN_ERR_NULL", "ATTN_ERR_SHAPE", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_ALIGN",
     "ATTN_ERR_LAUNCH", "ATTN_ERR_DEVICE_TIMEOUT", "ATTN_ERR_DEVICE", "ATTN_ERR_TOO_LARGE",
 ]
@@ -40,6 +40,7 @@ _SIGNATURES = {
     "attn_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _F, _P, _P],
     "attn_bwd_finalize": [_P, _P, _F, _I, _I, _I, _I, _P],
     "attn_device_status": [ctypes.POINTER(ctypes.c_int), _I, _P],
+    "attn_bwd_noalloc": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _F, _P],
 }
 
 _lib = None
@@ -112,6 +113,13 @@ def attn_bwd(q, k, v, o, dO, lse, dq_accum, dk, dv, B, H, H_kv, N, d, scale, cau
 def attn_bwd_finalize(dq_accum, dq, scale, B, H, N, d, stream=None):
     return library().attn_bwd_finalize(_ptr(dq_accum), _ptr(dq), scale, B, H, N, d,
                                        _stream(stream))
+
+
+def attn_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, B, H, H_kv, N, d, scale, causal, softcap,
+                     stream=None):
+    return library().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
+                                      _ptr(dq), _ptr(dk), _ptr(dv), B, H, H_kv, N, d, scale,
+                                      int(causal), softcap, _stream(stream))
 
 
 def attn_device_status(clear=True, stream=None):

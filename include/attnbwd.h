@@ -38,7 +38,8 @@
  *    validated before anything is launched, so an error return means nothing
  *    was enqueued. B, H or N equal to 0 is a valid empty problem (no launch).
  *  * No exception crosses this interface. The library keeps one small
- *    device status word (see attn_device_status) and caches nothing else.
+ *    device status word (see attn_device_status) and, for
+ *    attn_bwd_noalloc, one fixed scratch array; it caches nothing else.
  */
 #ifndef ATTNBWD_H_
 #define ATTNBWD_H_
@@ -111,6 +112,27 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
  */
 int attn_bwd_finalize(const float* dq_accum, void* dq, float scale, int B, int H, int N, int d,
                       void* stream);
+
+/*
+ * attn_bwd_noalloc: the whole backward (attn_bwd_preprocess, attn_bwd,
+ * attn_bwd_finalize) in one call that allocates nothing. The pages have no
+ * counterpart for it: it exists for callers that cannot allocate device
+ * memory (graph-captured code where allocation is not allowed, plugins that
+ * are handed fixed buffers, runtimes whose allocator must not be re-entered).
+ * Arguments mean what they mean for attn_bwd; dq [B,H,N,d] bf16 receives the
+ * finished dQ (tau applied), dk, dv as for attn_bwd.
+ * Scratch: the fp32 dQ accumulator and D live in one file-scope device array
+ * of 8,388,608 floats (32 MiB) that every device loading the library keeps
+ * until the process exits. A problem needs B*H*N*d + B*H*N floats; larger
+ * problems return ATTN_ERR_TOO_LARGE and nothing is launched.
+ * All calls share that array: calls whose GPU work overlaps (unordered
+ * streams, several host threads) race and give wrong results. The first call
+ * on a device looks up the array's address with that device current; make it
+ * before any stream capture.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int H_kv,
+                     int N, int d, float scale, int causal, float softcap, void* stream);
 
 /*
  * attn_device_status: waits for `stream`, then reads the library's device
