@@ -32,8 +32,9 @@
 //                query columns; thread = key row (tensor-memory lane);
 //                afterwards the dK/dV epilogue
 //   warps 12-19  dQ drain: two warpgroups, each loads half of the dQ tile
-//                from tensor memory, frees it, then issues the fp32 atomic
-//                adds into dq_accum while the tensor cores move on
+//                from tensor memory and frees it; for d = 128 it then stages
+//                the half in shared memory and adds it into dq_accum with
+//                TMA reductions, for d = 64 with fp32 vector atomics
 //
 // MMA issue order per tile: dP_t, dV_t, S_{t+1}, dQ_t, dK_t. The P phase of
 // tile t+1 overlaps dQ_t/dK_t, dK_t overlaps the dQ drain, and only
@@ -79,10 +80,16 @@ struct Layout {
   static constexpr int kV = kK + kTileBytes;
   static constexpr int kQ0 = kV + kTileBytes;
   static constexpr int kQ1 = kQ0 + kTileBytes;
+  // d = 128: one dO stage, and the freed 32 KB stage the dQ tile for TMA
+  // reductions (two 16 KB buffers, [32 queries][128 d] fp32). d = 64: two
+  // dO stages and no staging (its dQ goes out with 16-byte atomics).
+  static constexpr int kDOStages = D == 128 ? 1 : 2;
   static constexpr int kDO0 = kQ1 + kTileBytes;
-  static constexpr int kDO1 = kDO0 + kTileBytes;
-  static constexpr int kDS = kDO1 + kTileBytes;     // dS^T, [key][query], 32 KB
-  static constexpr int kLSE = kDS + kBc * kBr * 2;  // 2 stages x 128 fp32 (LSE*log2e)
+  static constexpr int kDO1 = kDO0 + (kDOStages - 1) * kTileBytes;
+  static constexpr int kDS = kDO0 + kDOStages * kTileBytes;  // dS^T, [key][query], 32 KB
+  static constexpr int kDQS = kDS + kBc * kBr * 2;            // dQ staging (d = 128)
+  static constexpr int kDQSBytes = D == 128 ? 2 * 16384 : 0;
+  static constexpr int kLSE = kDQS + kDQSBytes;  // 2 stages x 128 fp32 (LSE*log2e)
   static constexpr int kDsum = kLSE + 2 * kBr * 4;  // 2 stages x 128 fp32 (D)
   static constexpr int kBars = kDsum + 2 * kBr * 4;
   static constexpr int kNumBars = 17;
@@ -231,12 +238,14 @@ __device__ void producer_role(const Ctx& c, const Params& p, const Work& w, uint
       mbar_arrive(bar_addr(c, BAR_Q_FULL + st));
     }
     issued_q = t + 1;
-    if (t >= 2 && !wait(c, BAR_DO_EMPTY + st, ph ^ 1)) break;
+    const int ost = t % L::kDOStages;
+    const uint32_t oph = (t / L::kDOStages) & 1;
+    if (t >= L::kDOStages && !wait(c, BAR_DO_EMPTY + ost, oph ^ 1)) break;
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar_addr(c, BAR_DO_FULL + st), kTileBytes);
-      const uint32_t dst = sbase + (st ? L::kDO1 : L::kDO0);
+      mbar_arrive_expect_tx(bar_addr(c, BAR_DO_FULL + ost), kTileBytes);
+      const uint32_t dst = sbase + (ost ? L::kDO1 : L::kDO0);
       for (int cb = 0; cb < kBoxes; ++cb)
-        tma_load_3d_hint(dst + cb * 16384, tm_do, bar_addr(c, BAR_DO_FULL + st), 64 * cb, m0, bh,
+        tma_load_3d_hint(dst + cb * 16384, tm_do, bar_addr(c, BAR_DO_FULL + ost), 64 * cb, m0, bh,
                          reuse);
     }
     __syncwarp();
@@ -247,8 +256,8 @@ __device__ void producer_role(const Ctx& c, const Params& p, const Work& w, uint
     wait_drain(c, BAR_KV, 0);
     for (int t = issued_q - 2 < 0 ? 0 : issued_q - 2; t < issued_q; ++t)
       wait_drain(c, BAR_Q_FULL + (t & 1), (t >> 1) & 1);
-    for (int t = issued_do - 2 < 0 ? 0 : issued_do - 2; t < issued_do; ++t)
-      wait_drain(c, BAR_DO_FULL + (t & 1), (t >> 1) & 1);
+    for (int t = issued_do - L::kDOStages < 0 ? 0 : issued_do - L::kDOStages; t < issued_do; ++t)
+      wait_drain(c, BAR_DO_FULL + t % L::kDOStages, (t / L::kDOStages) & 1);
   }
 }
 
@@ -343,13 +352,14 @@ __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t t
   }
   for (int t = 0; ok && t < w.T; ++t) {
     const int st = t & 1;
-    const uint32_t kQn = st ? kQ0 : kQ1, kOn = st ? kO0 : kO1;
-    const uint32_t mQ = st ? mQ1 : mQ0, mO = st ? mO1 : mO0;
+    const int ost = t % L::kDOStages, ostn = (t + 1) % L::kDOStages;
+    const uint32_t kQn = st ? kQ0 : kQ1, kOn = ostn ? kO1 : kO0;
+    const uint32_t mQ = st ? mQ1 : mQ0, mO = ost ? mO1 : mO0;
     // dV += P_t^T dO_t (A = P_t^T in the S region)
     if (!(ok = wait(c, BAR_P_FULL, t & 1))) break;
     tc_fence_after();
     M::tn(tdV, tS, mO, t > 0);
-    mma_commit(bar_addr(c, BAR_DO_EMPTY + st));  // dP_t and dV_t were dO_t's readers
+    mma_commit(bar_addr(c, BAR_DO_EMPTY + ost));  // dP_t and dV_t were dO_t's readers
     // S_{t+1} = K Q_{t+1}^T into the S region (P_t^T there was read by dV_t)
     if (t + 1 < w.T) {
       if (!(ok = wait(c, BAR_Q_FULL + (st ^ 1), ph(t + 1)))) break;
@@ -368,7 +378,7 @@ __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t t
     mma_commit(bar_addr(c, BAR_DS_FREE));
     // dP_{t+1} = V dO_{t+1}^T once the dQ tile has been drained
     if (t + 1 < w.T) {
-      if (!(ok = wait(c, BAR_DO_FULL + (st ^ 1), ph(t + 1)))) break;
+      if (!(ok = wait(c, BAR_DO_FULL + ostn, ((t + 1) / L::kDOStages) & 1))) break;
       if (!(ok = wait(c, BAR_DQ_EMPTY, t & 1))) break;
       tc_fence_after();
       M::nt(tdP, kV, kOn);
@@ -549,37 +559,56 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8
 // only then are the fp32 atomic adds issued, so the reduction overlaps the
 // next tile's GEMMs.
 template <int D>
-__device__ void dq_role(const Ctx& c, const Params& p, const Work& w, uint32_t tmem) {
+__device__ void dq_role(const Ctx& c, const Params& p, const Work& w, uint8_t* smem,
+                        uint32_t sbase, uint32_t tmem, const CUtensorMap* tm_dq) {
+  using L = Layout<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int part = (warp - 12) >> 2;  // which half of the tile
   const int r = ((warp & 3) << 5) + lane;
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
+  // d = 128: this warpgroup's staging buffer and the thread that issues its
+  // TMA reductions (the bulk async-group is per thread)
+  const uint32_t stage = sbase + L::kDQS + part * 16384;
+  const bool leader = (warp & 3) == 0 && lane == 0;
+  (void)smem;
   for (int t = 0; t < w.T; ++t) {
     int h, m_block;
     tile_coord(w, t, h, m_block);
     const int m0 = m_block * kBr;
     const long long bh = static_cast<long long>(w.b) * p.H + h;
-    if (!wait(c, BAR_DQ_FULL, t & 1)) return;
+    {
+      // d = 128: the whole warpgroup takes the same decision (its members
+      // meet at named barriers below)
+      const bool ok = wait(c, BAR_DQ_FULL, t & 1);
+      if (D == 128 ? !named_bar_and(1 + part, 128, ok) : !ok) break;
+    }
     tc_fence_after();
     if (D == 128) {
-      // lane r holds dQ[m0 + i][r] in column 128 + i: one warp instruction
-      // adds 32 consecutive floats (one 128-byte line) of a dQ row.
+      // lane r holds dQ[m0 + i][r] in column 128 + i. The tile leaves tensor
+      // memory at once; each 32-query chunk is then written to the staging
+      // buffer as rows of 128 floats and added into dq_accum by one TMA
+      // reduction, which keeps the atomics off the load/store path the
+      // softmax warps use.
       uint32_t v[64];
       tmem_ld32x2(tmem + lane_base + 128 + part * 64, tmem + lane_base + 128 + part * 64 + 32, v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_addr(c, BAR_DQ_EMPTY));
-      const int i0 = m0 + part * 64;
-      float* dst = p.dq_accum + (bh * p.N + i0) * D + r;
-      if (i0 + 64 <= p.N) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j)
-          red_add_f32(dst + static_cast<long long>(j) * D, __uint_as_float(v[j]));
-      } else {
+      for (int ch = 0; ch < 2; ++ch) {
+        if (leader) bulk_wait_read_all();  // previous reduction has read the buffer
+        named_bar_sync(1 + part, 128);
 #pragma unroll
-        for (int j = 0; j < 64; ++j)
-          if (i0 + j < p.N) red_add_f32(dst + static_cast<long long>(j) * D, __uint_as_float(v[j]));
+        for (int q = 0; q < 32; ++q)
+          st_shared_f32(stage + q * 512 + r * 4, __uint_as_float(v[ch * 32 + q]));
+        fence_proxy_async_smem();
+        named_bar_sync(1 + part, 128);
+        const int row = m0 + part * 64 + ch * 32;
+        if (leader && row < p.N) {
+          tma_reduce_add_3d(tm_dq, stage, 0, row, static_cast<int>(bh));
+          bulk_commit_group();
+        }
       }
     } else {
       // lane r holds query row m0 + r; columns 128 + [0, 64) are dQ[m0 + r][:]
@@ -597,6 +626,8 @@ __device__ void dq_role(const Ctx& c, const Params& p, const Work& w, uint32_t t
       }
     }
   }
+  // the reductions must complete before the CTA exits
+  if (D == 128 && leader) bulk_wait_all();
 }
 
 // ------------------------------------------------------------------ kernel
@@ -605,7 +636,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_do, const Params p) {
+                    const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dq, const Params p) {
   using L = Layout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -671,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     softmax_role<D, CAUSAL, SOFTCAP>(c, p, w, smem, sbase, tmem);
   } else {
     setmaxnreg_dec<kRegsDq>();
-    dq_role<D>(c, p, w, tmem);
+    dq_role<D>(c, p, w, smem, sbase, tmem, &tm_dq);
   }
   tc_fence_before();
   __syncthreads();
@@ -683,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool CAUSAL, bool SOFTCAP>
 int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-           const CUtensorMap& tdo, const Params& p, cudaStream_t stream) {
+           const CUtensorMap& tdo, const CUtensorMap& tdq, const Params& p, cudaStream_t stream) {
   auto kern = attn_bwd_kernel<D, CAUSAL, SOFTCAP>;
   static bool configured = false;
   if (!configured) {
@@ -694,7 +726,7 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
   }
   const long long grid = static_cast<long long>(p.n_blocks) * p.H_kv * p.B;
   if (grid > 0x7fffffffLL) return ATTN_ERR_TOO_LARGE;
-  kern<<<static_cast<unsigned>(grid), kThreads, Layout<D>::kBytes, stream>>>(tq, tk, tv, tdo, p);
+  kern<<<static_cast<unsigned>(grid), kThreads, Layout<D>::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
   return launch_status();
 }
 
@@ -718,11 +750,12 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     return ATTN_ERR_ALIGN;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
 
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   const long long hq = static_cast<long long>(B) * H, hk = static_cast<long long>(B) * H_kv;
   if (!encode_bf16_3d(&tq, q, d, N, hq, bwd::kBr) || !encode_bf16_3d(&tk, k, d, N, hk, bwd::kBc) ||
       !encode_bf16_3d(&tv, v, d, N, hk, bwd::kBc) ||
-      !encode_bf16_3d(&tdo, dO, d, N, hq, bwd::kBr))
+      !encode_bf16_3d(&tdo, dO, d, N, hq, bwd::kBr) ||
+      !encode_f32_3d(&tdq, dq_accum, d, N, hq, 32))
     return ATTN_ERR_LAUNCH;
 
   bwd::Params p;
@@ -743,15 +776,15 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   cudaStream_t s = as_stream(stream);
   const bool cs = causal != 0;
   if (d == 128) {
-    if (cs) return cap ? bwd::launch<128, true, true>(tq, tk, tv, tdo, p, s)
-                       : bwd::launch<128, true, false>(tq, tk, tv, tdo, p, s);
-    return cap ? bwd::launch<128, false, true>(tq, tk, tv, tdo, p, s)
-               : bwd::launch<128, false, false>(tq, tk, tv, tdo, p, s);
+    if (cs) return cap ? bwd::launch<128, true, true>(tq, tk, tv, tdo, tdq, p, s)
+                       : bwd::launch<128, true, false>(tq, tk, tv, tdo, tdq, p, s);
+    return cap ? bwd::launch<128, false, true>(tq, tk, tv, tdo, tdq, p, s)
+               : bwd::launch<128, false, false>(tq, tk, tv, tdo, tdq, p, s);
   }
-  if (cs) return cap ? bwd::launch<64, true, true>(tq, tk, tv, tdo, p, s)
-                     : bwd::launch<64, true, false>(tq, tk, tv, tdo, p, s);
-  return cap ? bwd::launch<64, false, true>(tq, tk, tv, tdo, p, s)
-             : bwd::launch<64, false, false>(tq, tk, tv, tdo, p, s);
+  if (cs) return cap ? bwd::launch<64, true, true>(tq, tk, tv, tdo, tdq, p, s)
+                     : bwd::launch<64, true, false>(tq, tk, tv, tdo, tdq, p, s);
+  return cap ? bwd::launch<64, false, true>(tq, tk, tv, tdo, tdq, p, s)
+             : bwd::launch<64, false, false>(tq, tk, tv, tdo, tdq, p, s);
 }
 
 extern "C" int attn_device_status(int* status, int clear, void* stream) {
