@@ -66,7 +66,7 @@ constexpr int kBc = 128;  // keys per CTA (tensor-memory lanes)
 constexpr int kBr = 128;  // queries per tile
 constexpr int kThreads = 640;
 // registers per thread after setmaxnreg (launch: 640 x 96)
-constexpr int kRegsCtl = 64, kRegsSoftmax = 136, kRegsDq = 72;
+constexpr int kRegsCtl = 80, kRegsSoftmax = 128, kRegsDq = 72;
 static_assert(128 * (kRegsCtl + 2 * kRegsSoftmax + 2 * kRegsDq) <= kThreads * 96, "register pool");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitLimitCycles = 2000000000LL;  // about one second
@@ -92,7 +92,7 @@ struct Layout {
   static constexpr int kLSE = kDQS + kDQSBytes;  // 2 stages x 128 fp32 (LSE*log2e)
   static constexpr int kDsum = kLSE + 2 * kBr * 4;  // 2 stages x 128 fp32 (D)
   static constexpr int kBars = kDsum + 2 * kBr * 4;
-  static constexpr int kNumBars = 17;
+  static constexpr int kNumBars = 19;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kBytes = kAbort + 12;
@@ -100,7 +100,7 @@ struct Layout {
 static_assert(Layout<128>::kBytes <= 232448, "shared memory budget");
 
 enum Bar {
-  BAR_KV = 0,
+  BAR_K_FULL = 0,
   BAR_Q_FULL = 1,    // + stage
   BAR_Q_EMPTY = 3,   // + stage
   BAR_DO_FULL = 5,   // + stage
@@ -111,8 +111,10 @@ enum Bar {
   BAR_DS_FULL = 12,
   BAR_DQ_FULL = 13,
   BAR_DQ_EMPTY = 14,
-  BAR_KV_DONE = 15,
+  BAR_UNIT_DONE = 15,  // every GEMM of a unit done: the epilogue may read dK, dV
   BAR_DS_FREE = 16,
+  BAR_V_FULL = 17,
+  BAR_DRAIN = 18,      // abort path only: completion of everything issued
 };
 
 struct Params {
@@ -123,15 +125,41 @@ struct Params {
   __nv_bfloat16* dv;
   int B, H, H_kv, N;
   int n_blocks, m_blocks;
+  int n_units;  // n_blocks * H_kv * B
   float scale;
   float softcap;
 };
 
-// Per-CTA work description.
+// One unit of work: a block of 128 keys of one KV head of one batch entry,
+// with the query tiles it visits.
 struct Work {
   int b, g, n_block;
   int G, m_start, per_head, T;
 };
+
+// Units in heaviest-first order are u = n_block * (H_kv * B) + b * H_kv + g
+// (for a causal mask, key block 0 sees every query block). A persistent CTA
+// takes one unit per pass in snake order (pass r visits CTAs 0..grid-1 when
+// r is even, grid-1..0 when odd), which balances the shrinking causal units.
+__device__ __forceinline__ int unit_of(int r, int n_units) {
+  const int grid = static_cast<int>(gridDim.x);
+  const int cta = static_cast<int>(blockIdx.x);
+  const int u = r * grid + ((r & 1) ? grid - 1 - cta : cta);
+  return u < n_units ? u : -1;
+}
+
+template <bool CAUSAL>
+__device__ __forceinline__ void unit_work(const Params& p, int u, Work& w) {
+  const int per_nb = p.H_kv * p.B;
+  w.n_block = u / per_nb;
+  const int rem = u - w.n_block * per_nb;
+  w.b = rem / p.H_kv;
+  w.g = rem - w.b * p.H_kv;
+  w.G = p.H / p.H_kv;
+  w.m_start = CAUSAL ? w.n_block : 0;
+  w.per_head = p.m_blocks - w.m_start;
+  w.T = w.G * w.per_head;
+}
 
 struct Ctx {
   uint32_t bars;
@@ -178,9 +206,13 @@ __device__ __forceinline__ void tile_coord(const Work& w, int t, int& h, int& m_
 }
 
 // ------------------------------------------------------------------ producer
-template <int D>
-__device__ void producer_role(const Ctx& c, const Params& p, const Work& w, uint8_t* smem,
-                              uint32_t sbase, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+// Streams, per tile, Q (+LSE, D) and dO into two-stage rings, and per unit K
+// and V. A unit's V is requested as soon as the previous unit's last dP GEMM
+// has completed and its K as soon as the last dQ GEMM has, so the loads
+// overlap the previous unit's final GEMMs and its dK/dV epilogue.
+template <int D, bool CAUSAL>
+__device__ void producer_role(const Ctx& c, const Params& p, uint8_t* smem, uint32_t sbase,
+                              const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                               const CUtensorMap* tm_v, const CUtensorMap* tm_do) {
   using L = Layout<D>;
   constexpr int kBoxes = D / 64;
@@ -191,69 +223,96 @@ __device__ void producer_role(const Ctx& c, const Params& p, const Work& w, uint
     prefetch_tmap(tm_k);
     prefetch_tmap(tm_v);
     prefetch_tmap(tm_do);
-    const uint64_t once = policy_evict_first();
-    mbar_arrive_expect_tx(bar_addr(c, BAR_KV), 2 * kTileBytes);
-    const int kvh = w.b * p.H_kv + w.g;
-    for (int cb = 0; cb < kBoxes; ++cb) {
-      tma_load_3d_hint(sbase + L::kK + cb * 16384, tm_k, bar_addr(c, BAR_KV), 64 * cb,
-                       w.n_block * kBc, kvh, once);
-      tma_load_3d_hint(sbase + L::kV + cb * 16384, tm_v, bar_addr(c, BAR_KV), 64 * cb,
-                       w.n_block * kBc, kvh, once);
-    }
   }
-  __syncwarp();
+  const uint64_t once = policy_evict_first();
   // Q/dO tiles are re-read by every key block of the head: keep them in L2.
   const uint64_t reuse = policy_evict_last();
-  int issued_q = 0, issued_do = 0;
-  for (int t = 0; t < w.T; ++t) {
-    const int st = t & 1;
-    const uint32_t ph = (t >> 1) & 1;
-    int h, m_block;
-    tile_coord(w, t, h, m_block);
-    const int bh = w.b * p.H + h;
-    const int m0 = m_block * kBr;
-    if (t >= 2 && !wait(c, BAR_Q_EMPTY + st, ph ^ 1)) break;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar_addr(c, BAR_Q_FULL + st), kTileBytes);
-      const uint32_t dst = sbase + (st ? L::kQ1 : L::kQ0);
-      for (int cb = 0; cb < kBoxes; ++cb)
-        tma_load_3d_hint(dst + cb * 16384, tm_q, bar_addr(c, BAR_Q_FULL + st), 64 * cb, m0, bh,
-                         reuse);
-    }
-    {
-      float* s_lse = reinterpret_cast<float*>(smem + L::kLSE) + st * kBr;
-      float* s_d = reinterpret_cast<float*>(smem + L::kDsum) + st * kBr;
-      const long long row0 = static_cast<long long>(bh) * p.N + m0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = lane + 32 * e;
-        float lv = 0.f, dv = 0.f;
-        if (m0 + i < p.N) {
-          lv = __ldg(p.lse + row0 + i);
-          dv = __ldg(p.dpsum + row0 + i);
-        }
-        s_lse[i] = lv * kLog2e;
-        s_d[i] = dv;
+  int issued_q = 0, issued_do = 0, issued_k = 0, issued_v = 0;
+  bool ok = true;
+  int tg = 0;  // tiles of all earlier units
+  for (int r = 0; ok; ++r) {
+    const int u = unit_of(r, p.n_units);
+    if (u < 0) break;
+    Work w;
+    unit_work<CAUSAL>(p, u, w);
+    for (int tl = 0; tl < w.T; ++tl) {
+      const int t = tg + tl;
+      const int st = t & 1;
+      const uint32_t ph = (t >> 1) & 1;
+      int h, m_block;
+      tile_coord(w, tl, h, m_block);
+      const int bh = w.b * p.H + h;
+      const int m0 = m_block * kBr;
+      if (t >= 2 && !(ok = wait(c, BAR_Q_EMPTY + st, ph ^ 1))) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar_addr(c, BAR_Q_FULL + st), kTileBytes);
+        const uint32_t dst = sbase + (st ? L::kQ1 : L::kQ0);
+        for (int cb = 0; cb < kBoxes; ++cb)
+          tma_load_3d_hint(dst + cb * 16384, tm_q, bar_addr(c, BAR_Q_FULL + st), 64 * cb, m0, bh,
+                           reuse);
       }
-      mbar_arrive(bar_addr(c, BAR_Q_FULL + st));
+      {
+        float* s_lse = reinterpret_cast<float*>(smem + L::kLSE) + st * kBr;
+        float* s_d = reinterpret_cast<float*>(smem + L::kDsum) + st * kBr;
+        const long long row0 = static_cast<long long>(bh) * p.N + m0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = lane + 32 * e;
+          float lv = 0.f, dv = 0.f;
+          if (m0 + i < p.N) {
+            lv = __ldg(p.lse + row0 + i);
+            dv = __ldg(p.dpsum + row0 + i);
+          }
+          s_lse[i] = lv * kLog2e;
+          s_d[i] = dv;
+        }
+        mbar_arrive(bar_addr(c, BAR_Q_FULL + st));
+      }
+      issued_q = t + 1;
+      const int kvh = w.b * p.H_kv + w.g;
+      if (tl == 0) {
+        // V of this unit once the previous unit's last dP GEMM has read V.
+        // (Q_EMPTY of tile t-2, waited above, implies dP of t-2 is complete,
+        // so the parity below cannot match an older phase.)
+        if (t > 0 && !(ok = wait(c, BAR_DP_FULL, (t - 1) & 1))) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar_addr(c, BAR_V_FULL), kTileBytes);
+          for (int cb = 0; cb < kBoxes; ++cb)
+            tma_load_3d_hint(sbase + L::kV + cb * 16384, tm_v, bar_addr(c, BAR_V_FULL), 64 * cb,
+                             w.n_block * kBc, kvh, once);
+        }
+        issued_v = r + 1;
+      }
+      const int ost = t % L::kDOStages;
+      const uint32_t oph = (t / L::kDOStages) & 1;
+      if (t >= L::kDOStages && !(ok = wait(c, BAR_DO_EMPTY + ost, oph ^ 1))) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar_addr(c, BAR_DO_FULL + ost), kTileBytes);
+        const uint32_t dst = sbase + (ost ? L::kDO1 : L::kDO0);
+        for (int cb = 0; cb < kBoxes; ++cb)
+          tma_load_3d_hint(dst + cb * 16384, tm_do, bar_addr(c, BAR_DO_FULL + ost), 64 * cb, m0,
+                           bh, reuse);
+      }
+      issued_do = t + 1;
+      if (tl == 0) {
+        // K of this unit once the previous unit's last dQ GEMM has read K
+        if (t > 0 && !(ok = wait(c, BAR_DQ_FULL, (t - 1) & 1))) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar_addr(c, BAR_K_FULL), kTileBytes);
+          for (int cb = 0; cb < kBoxes; ++cb)
+            tma_load_3d_hint(sbase + L::kK + cb * 16384, tm_k, bar_addr(c, BAR_K_FULL), 64 * cb,
+                             w.n_block * kBc, kvh, once);
+        }
+        issued_k = r + 1;
+      }
+      __syncwarp();
     }
-    issued_q = t + 1;
-    const int ost = t % L::kDOStages;
-    const uint32_t oph = (t / L::kDOStages) & 1;
-    if (t >= L::kDOStages && !wait(c, BAR_DO_EMPTY + ost, oph ^ 1)) break;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar_addr(c, BAR_DO_FULL + ost), kTileBytes);
-      const uint32_t dst = sbase + (ost ? L::kDO1 : L::kDO0);
-      for (int cb = 0; cb < kBoxes; ++cb)
-        tma_load_3d_hint(dst + cb * 16384, tm_do, bar_addr(c, BAR_DO_FULL + ost), 64 * cb, m0, bh,
-                         reuse);
-    }
-    __syncwarp();
-    issued_do = t + 1;
+    tg += w.T;
   }
   // When aborting, the copies issued last must land before the CTA exits.
   if (*c.abort) {
-    wait_drain(c, BAR_KV, 0);
+    if (issued_k > 0) wait_drain(c, BAR_K_FULL, (issued_k - 1) & 1);
+    if (issued_v > 0) wait_drain(c, BAR_V_FULL, (issued_v - 1) & 1);
     for (int t = issued_q - 2 < 0 ? 0 : issued_q - 2; t < issued_q; ++t)
       wait_drain(c, BAR_Q_FULL + (t & 1), (t >> 1) & 1);
     for (int t = issued_do - L::kDOStages < 0 ? 0 : issued_do - L::kDOStages; t < issued_do; ++t)
@@ -324,8 +383,15 @@ struct Mma {
 // reads what the region held (P^T before S, dS^T before the dQ tile).
 // Descriptor low words are formed once; the loop only adds constants, which
 // keeps the single issuing thread ahead of the tensor cores.
-template <int D>
-__device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t tmem) {
+//
+// Tiles are numbered t over all units of the CTA, so every per-tile barrier
+// keeps one phase per tile across unit boundaries. A unit starts with dP of
+// its first tile (V and dO usually land before K); its first dV and dK
+// overwrite the accumulators, which is safe because the softmax warps read
+// the previous unit's dK, dV in the epilogue before they arrive on P_FULL of
+// the unit's first tile, and dV waits on P_FULL.
+template <int D, bool CAUSAL>
+__device__ void mma_role(const Ctx& c, const Params& p, uint32_t sbase, uint32_t tmem) {
   using L = Layout<D>;
   using M = Mma<D>;
   const uint32_t tS = tmem + 0, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
@@ -337,57 +403,77 @@ __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t t
   const uint32_t mQ0 = sdesc_lo(sbase + L::kQ0, 16384), mQ1 = sdesc_lo(sbase + L::kQ1, 16384);
   const uint32_t mO0 = sdesc_lo(sbase + L::kDO0, 16384), mO1 = sdesc_lo(sbase + L::kDO1, 16384);
   auto ph = [](int t) { return static_cast<uint32_t>((t >> 1) & 1); };
+  auto oph = [](int t) { return static_cast<uint32_t>((t / L::kDOStages) & 1); };
 
-  bool ok = wait(c, BAR_KV, 0);
-  // prologue: S_0, dP_0
-  if (ok && (ok = wait(c, BAR_Q_FULL + 0, 0))) {
-    tc_fence_after();
-    M::nt(tS, kK, kQ0);
-    mma_commit(bar_addr(c, BAR_S_FULL));
-  }
-  if (ok && (ok = wait(c, BAR_DO_FULL + 0, 0))) {
-    tc_fence_after();
-    M::nt(tdP, kV, kO0);
-    mma_commit(bar_addr(c, BAR_DP_FULL));
-  }
-  for (int t = 0; ok && t < w.T; ++t) {
-    const int st = t & 1;
-    const int ost = t % L::kDOStages, ostn = (t + 1) % L::kDOStages;
-    const uint32_t kQn = st ? kQ0 : kQ1, kOn = ostn ? kO1 : kO0;
-    const uint32_t mQ = st ? mQ1 : mQ0, mO = ost ? mO1 : mO0;
-    // dV += P_t^T dO_t (A = P_t^T in the S region)
-    if (!(ok = wait(c, BAR_P_FULL, t & 1))) break;
-    tc_fence_after();
-    M::tn(tdV, tS, mO, t > 0);
-    mma_commit(bar_addr(c, BAR_DO_EMPTY + ost));  // dP_t and dV_t were dO_t's readers
-    // S_{t+1} = K Q_{t+1}^T into the S region (P_t^T there was read by dV_t)
-    if (t + 1 < w.T) {
-      if (!(ok = wait(c, BAR_Q_FULL + (st ^ 1), ph(t + 1)))) break;
+  bool ok = true;
+  int tg = 0;
+  for (int r = 0; ok; ++r) {
+    const int u = unit_of(r, p.n_units);
+    if (u < 0) break;
+    Work w;
+    unit_work<CAUSAL>(p, u, w);
+    // unit prologue: dP of the first tile, then S
+    {
+      const int ost = tg % L::kDOStages;
+      if (!(ok = wait(c, BAR_V_FULL, r & 1))) break;
+      if (!(ok = wait(c, BAR_DO_FULL + ost, oph(tg)))) break;
+      if (tg > 0 && !(ok = wait(c, BAR_DQ_EMPTY, (tg - 1) & 1))) break;
       tc_fence_after();
-      M::nt(tS, kK, kQn);
+      M::nt(tdP, kV, ost ? kO1 : kO0);
+      mma_commit(bar_addr(c, BAR_DP_FULL));
+      if (!(ok = wait(c, BAR_K_FULL, r & 1))) break;
+      if (!(ok = wait(c, BAR_Q_FULL + (tg & 1), ph(tg)))) break;
+      tc_fence_after();
+      M::nt(tS, kK, (tg & 1) ? kQ1 : kQ0);
       mma_commit(bar_addr(c, BAR_S_FULL));
     }
-    // dQ tile of t into the dP region (the softmax has read dP_t), then
-    // dK += dS_t^T Q_t, both from the shared dS tile
-    if (!(ok = wait(c, BAR_DS_FULL, t & 1))) break;
-    tc_fence_after();
-    M::dq(tdP, mK, mDS);
-    mma_commit(bar_addr(c, BAR_DQ_FULL));
-    M::dk(tdK, kDS, mQ, t > 0);
-    mma_commit(bar_addr(c, BAR_Q_EMPTY + st));
-    mma_commit(bar_addr(c, BAR_DS_FREE));
-    // dP_{t+1} = V dO_{t+1}^T once the dQ tile has been drained
-    if (t + 1 < w.T) {
-      if (!(ok = wait(c, BAR_DO_FULL + ostn, ((t + 1) / L::kDOStages) & 1))) break;
-      if (!(ok = wait(c, BAR_DQ_EMPTY, t & 1))) break;
+    for (int tl = 0; tl < w.T; ++tl) {
+      const int t = tg + tl;
+      const bool more = tl + 1 < w.T;
+      const int st = t & 1;
+      const int ost = t % L::kDOStages, ostn = (t + 1) % L::kDOStages;
+      const uint32_t kQn = st ? kQ0 : kQ1, kOn = ostn ? kO1 : kO0;
+      const uint32_t mQ = st ? mQ1 : mQ0, mO = ost ? mO1 : mO0;
+      // dV += P_t^T dO_t (A = P_t^T in the S region)
+      if (!(ok = wait(c, BAR_P_FULL, t & 1))) break;
       tc_fence_after();
-      M::nt(tdP, kV, kOn);
-      mma_commit(bar_addr(c, BAR_DP_FULL));
+      M::tn(tdV, tS, mO, tl > 0);
+      mma_commit(bar_addr(c, BAR_DO_EMPTY + ost));  // dP_t and dV_t were dO_t's readers
+      // S_{t+1} = K Q_{t+1}^T into the S region (P_t^T there was read by dV_t)
+      if (more) {
+        if (!(ok = wait(c, BAR_Q_FULL + (st ^ 1), ph(t + 1)))) break;
+        tc_fence_after();
+        M::nt(tS, kK, kQn);
+        mma_commit(bar_addr(c, BAR_S_FULL));
+      }
+      // dQ tile of t into the dP region (the softmax has read dP_t), then
+      // dK += dS_t^T Q_t, both from the shared dS tile
+      if (!(ok = wait(c, BAR_DS_FULL, t & 1))) break;
+      tc_fence_after();
+      M::dq(tdP, mK, mDS);
+      mma_commit(bar_addr(c, BAR_DQ_FULL));
+      M::dk(tdK, kDS, mQ, tl > 0);
+      mma_commit(bar_addr(c, BAR_Q_EMPTY + st));
+      mma_commit(bar_addr(c, BAR_DS_FREE));
+      // dP_{t+1} = V dO_{t+1}^T once the dQ tile has been drained
+      if (more) {
+        if (!(ok = wait(c, BAR_DO_FULL + ostn, oph(t + 1)))) break;
+        if (!(ok = wait(c, BAR_DQ_EMPTY, t & 1))) break;
+        tc_fence_after();
+        M::nt(tdP, kV, kOn);
+        mma_commit(bar_addr(c, BAR_DP_FULL));
+      }
     }
+    if (!ok) break;
+    // completion of the unit's GEMMs: the epilogue may read dK, dV
+    mma_commit(bar_addr(c, BAR_UNIT_DONE));
+    tg += w.T;
   }
-  // Completion of everything issued; the epilogue waits on it.
-  mma_commit(bar_addr(c, BAR_KV_DONE));
-  if (*c.abort) wait_drain(c, BAR_KV_DONE, 0);
+  if (*c.abort) {
+    // completion of everything issued before tensor memory is released
+    mma_commit(bar_addr(c, BAR_DRAIN));
+    wait_drain(c, BAR_DRAIN, 0);
+  }
 }
 
 // ------------------------------------------------------------------ softmax
@@ -502,32 +588,12 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
   return true;
 }
 
-template <int D, bool CAUSAL, bool SOFTCAP>
-__device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8_t* smem,
-                             uint32_t sbase, uint32_t tmem) {
-  const int warp = threadIdx.x >> 5;
-  const int half = (warp - 4) >> 2;
-  const int r = ((warp & 3) << 5) + (threadIdx.x & 31);
-  const int n0 = w.n_block * kBc;
-  const int key = n0 + r;
-  const bool key_tail = n0 + kBc > p.N;
-  bool ok = true;
-  for (int t = 0; t < w.T && ok; ++t) {
-    int h, m_block;
-    tile_coord(w, t, h, m_block);
-    const int m0 = m_block * kBr;
-    if (!wait(c, BAR_Q_FULL + (t & 1), (t >> 1) & 1)) break;
-    const bool masked = (CAUSAL && m_block == w.n_block) || key_tail || (m0 + kBr > p.N);
-    if (masked)
-      ok = softmax_tile<D, SOFTCAP, CAUSAL, true>(c, p, smem, sbase, tmem, t, half, r, key, m0);
-    else
-      ok = softmax_tile<D, SOFTCAP, CAUSAL, false>(c, p, smem, sbase, tmem, t, half, r, key, m0);
-  }
-
-  // ---- epilogue: dK (x tau) and dV, fp32 tensor memory -> bf16 global.
-  // This warpgroup writes columns [half*D/2, (half+1)*D/2) of its key row.
-  if (!wait(c, BAR_KV_DONE, 0)) return;
-  tc_fence_after();
+// dK (x tau) and dV of a finished unit, fp32 tensor memory -> bf16 global.
+// This warpgroup writes columns [half*D/2, (half+1)*D/2) of its key row.
+template <int D>
+__device__ __forceinline__ void epilogue(const Params& p, const Work& w, uint32_t tmem, int half,
+                                         int r) {
+  const int key = w.n_block * kBc + r;
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
   const long long row = (static_cast<long long>(w.b) * p.H_kv + w.g) * p.N + key;
 #pragma unroll
@@ -539,7 +605,7 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8
     for (int ch = 0; ch < D / 32; ++ch) {
       uint32_t raw[16];
       tmem_ld16(tmem + lane_base + col_base + ch * 16, raw);
-        uint32_t packed[8];
+      uint32_t packed[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u)
         packed[u] = pack_bf16x2(__uint_as_float(raw[2 * u]) * mul,
@@ -553,14 +619,53 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8
   }
 }
 
+template <int D, bool CAUSAL, bool SOFTCAP>
+__device__ void softmax_role(const Ctx& c, const Params& p, uint8_t* smem, uint32_t sbase,
+                             uint32_t tmem) {
+  const int warp = threadIdx.x >> 5;
+  const int half = (warp - 4) >> 2;
+  const int r = ((warp & 3) << 5) + (threadIdx.x & 31);
+  bool ok = true;
+  int tg = 0;
+  for (int ur = 0; ok; ++ur) {
+    const int u = unit_of(ur, p.n_units);
+    if (u < 0) break;
+    Work w;
+    unit_work<CAUSAL>(p, u, w);
+    const int n0 = w.n_block * kBc;
+    const int key = n0 + r;
+    const bool key_tail = n0 + kBc > p.N;
+    for (int tl = 0; tl < w.T && ok; ++tl) {
+      const int t = tg + tl;
+      int h, m_block;
+      tile_coord(w, tl, h, m_block);
+      const int m0 = m_block * kBr;
+      if (!(ok = wait(c, BAR_Q_FULL + (t & 1), (t >> 1) & 1))) break;
+      const bool masked = (CAUSAL && m_block == w.n_block) || key_tail || (m0 + kBr > p.N);
+      if (masked)
+        ok = softmax_tile<D, SOFTCAP, CAUSAL, true>(c, p, smem, sbase, tmem, t, half, r, key, m0);
+      else
+        ok = softmax_tile<D, SOFTCAP, CAUSAL, false>(c, p, smem, sbase, tmem, t, half, r, key,
+                                                     m0);
+    }
+    if (!ok || !(ok = wait(c, BAR_UNIT_DONE, ur & 1))) break;
+    tc_fence_after();
+    epilogue<D>(p, w, tmem, half, r);
+    // the next unit's first dV and dK overwrite the accumulators after
+    // P_FULL of its first tile, which these warps arrive on only after this
+    tc_fence_before();
+    tg += w.T;
+  }
+}
+
 // ------------------------------------------------------------------ dQ drain
 // Two warpgroups, each owning half of the dQ tile's columns. A thread loads
 // its share from tensor memory, the warp frees the region (DQ_EMPTY), and
 // only then are the fp32 atomic adds issued, so the reduction overlaps the
 // next tile's GEMMs.
-template <int D>
-__device__ void dq_role(const Ctx& c, const Params& p, const Work& w, uint8_t* smem,
-                        uint32_t sbase, uint32_t tmem, const CUtensorMap* tm_dq) {
+template <int D, bool CAUSAL>
+__device__ void dq_role(const Ctx& c, const Params& p, uint8_t* smem, uint32_t sbase,
+                        uint32_t tmem, const CUtensorMap* tm_dq) {
   using L = Layout<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -572,16 +677,29 @@ __device__ void dq_role(const Ctx& c, const Params& p, const Work& w, uint8_t* s
   const uint32_t stage = sbase + L::kDQS + part * 16384;
   const bool leader = (warp & 3) == 0 && lane == 0;
   (void)smem;
-  for (int t = 0; t < w.T; ++t) {
+  bool ok = true;
+  int tg = 0;
+  Work w;
+  w.T = 0;
+  for (int ur = 0, tl = 0; ok; ++tl) {
+    if (tl == w.T) {  // next unit
+      tg += w.T;
+      tl = 0;
+      const int u = unit_of(ur++, p.n_units);
+      if (u < 0) break;
+      unit_work<CAUSAL>(p, u, w);
+    }
+    const int t = tg + tl;
     int h, m_block;
-    tile_coord(w, t, h, m_block);
+    tile_coord(w, tl, h, m_block);
     const int m0 = m_block * kBr;
     const long long bh = static_cast<long long>(w.b) * p.H + h;
     {
       // d = 128: the whole warpgroup takes the same decision (its members
       // meet at named barriers below)
-      const bool ok = wait(c, BAR_DQ_FULL, t & 1);
-      if (D == 128 ? !named_bar_and(1 + part, 128, ok) : !ok) break;
+      ok = wait(c, BAR_DQ_FULL, t & 1);
+      if (D == 128) ok = named_bar_and(1 + part, 128, ok);
+      if (!ok) break;
     }
     tc_fence_after();
     if (D == 128) {
@@ -649,21 +767,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   c.bars = sbase + L::kBars;
   c.abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
 
-  Work w;
-  {
-    const int per_nb = p.H_kv * p.B;
-    w.n_block = blockIdx.x / per_nb;
-    const int rem = blockIdx.x - w.n_block * per_nb;
-    w.b = rem / p.H_kv;
-    w.g = rem - w.b * p.H_kv;
-    w.G = p.H / p.H_kv;
-    w.m_start = CAUSAL ? w.n_block : 0;
-    w.per_head = p.m_blocks - w.m_start;
-    w.T = w.G * w.per_head;
-  }
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    mbar_init(bar_addr(c, BAR_KV), 1);
+    mbar_init(bar_addr(c, BAR_K_FULL), 1);
+    mbar_init(bar_addr(c, BAR_V_FULL), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar_addr(c, BAR_Q_FULL + s), 33);  // expect_tx arrive + 32 LSE/D lanes
       mbar_init(bar_addr(c, BAR_Q_EMPTY + s), 1);
@@ -676,8 +783,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_addr(c, BAR_DS_FULL), 8);
     mbar_init(bar_addr(c, BAR_DQ_FULL), 1);
     mbar_init(bar_addr(c, BAR_DQ_EMPTY), 8);
-    mbar_init(bar_addr(c, BAR_KV_DONE), 1);
+    mbar_init(bar_addr(c, BAR_UNIT_DONE), 1);
     mbar_init(bar_addr(c, BAR_DS_FREE), 1);
+    mbar_init(bar_addr(c, BAR_DRAIN), 1);
     *c.abort = 0;
     fence_barrier_init();
   }
@@ -693,17 +801,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     setmaxnreg_dec<kRegsCtl>();
     if (warp == 0) {
-      producer_role<D>(c, p, w, smem, sbase, &tm_q, &tm_k, &tm_v, &tm_do);
+      producer_role<D, CAUSAL>(c, p, smem, sbase, &tm_q, &tm_k, &tm_v, &tm_do);
     } else if (warp == 1) {
-      if ((threadIdx.x & 31) == 0) mma_role<D>(c, w, sbase, tmem);
+      if ((threadIdx.x & 31) == 0) mma_role<D, CAUSAL>(c, p, sbase, tmem);
       __syncwarp();
     }
   } else if (warp < 12) {
     setmaxnreg_inc<kRegsSoftmax>();
-    softmax_role<D, CAUSAL, SOFTCAP>(c, p, w, smem, sbase, tmem);
+    softmax_role<D, CAUSAL, SOFTCAP>(c, p, smem, sbase, tmem);
   } else {
     setmaxnreg_dec<kRegsDq>();
-    dq_role<D>(c, p, w, smem, sbase, tmem, &tm_dq);
+    dq_role<D, CAUSAL>(c, p, smem, sbase, tmem, &tm_dq);
   }
   tc_fence_before();
   __syncthreads();
@@ -724,9 +832,11 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
       return ATTN_ERR_LAUNCH;
     configured = true;
   }
-  const long long grid = static_cast<long long>(p.n_blocks) * p.H_kv * p.B;
-  if (grid > 0x7fffffffLL) return ATTN_ERR_TOO_LARGE;
-  kern<<<static_cast<unsigned>(grid), kThreads, Layout<D>::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
+  // persistent: one CTA per SM (or per unit, if there are fewer units)
+  const int sms = sm_count();
+  if (sms <= 0) return ATTN_ERR_LAUNCH;
+  const int grid = p.n_units < sms ? p.n_units : sms;
+  kern<<<grid, kThreads, Layout<D>::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
   return launch_status();
 }
 
@@ -770,6 +880,9 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   p.N = N;
   p.n_blocks = (N + bwd::kBc - 1) / bwd::kBc;
   p.m_blocks = (N + bwd::kBr - 1) / bwd::kBr;
+  const long long units = static_cast<long long>(p.n_blocks) * H_kv * B;
+  if (units > 0x7fffffffLL) return ATTN_ERR_TOO_LARGE;
+  p.n_units = static_cast<int>(units);
   p.scale = scale;
   const bool cap = softcap > 0.f;
   p.softcap = cap ? softcap : 0.f;

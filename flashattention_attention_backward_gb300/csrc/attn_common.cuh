@@ -2,6 +2,7 @@
 // argument validation and TMA tensor-map encoding.
 #pragma once
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cuda.h>
@@ -26,6 +27,23 @@ inline int check_shape(int B, int H, int H_kv, int N, int d) {
   if (rows * d >= (1LL << 40)) return ATTN_ERR_TOO_LARGE;
   if (static_cast<long long>(N) * d >= (1LL << 31)) return ATTN_ERR_TOO_LARGE;
   return ATTN_OK;
+}
+
+// Number of SMs of the current device (cached per device); 0 on error.
+inline int sm_count() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int n = cache[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 0;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 inline int launch_status() {

@@ -64,20 +64,10 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-inline int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 152;
-  }
-  return n;
-}
-
 inline unsigned grid_for(long long work_items, int items_per_block) {
   const long long want = (work_items + items_per_block - 1) / items_per_block;
-  const long long cap = static_cast<long long>(sm_count()) * 8;
+  const int sms = sm_count();
+  const long long cap = static_cast<long long>(sms > 0 ? sms : 1) * 8;
   return static_cast<unsigned>(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
