@@ -197,6 +197,11 @@ __device__ __forceinline__ void wait_drain(const Ctx& c, int bar, uint32_t parit
   }
 }
 
+// wait() taken by a whole warp with one outcome for all lanes.
+__device__ __forceinline__ bool wait_warp(const Ctx& c, int bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, wait(c, bar, parity));
+}
+
 // Tile t of a CTA: query head h = g*G + t / per_head, query block
 // m_start + t % per_head (heads outer, query blocks inner).
 __device__ __forceinline__ void tile_coord(const Work& w, int t, int& h, int& m_block) {
@@ -404,6 +409,9 @@ __device__ void mma_role(const Ctx& c, const Params& p, uint32_t sbase, uint32_t
   const uint32_t mO0 = sdesc_lo(sbase + L::kDO0, 16384), mO1 = sdesc_lo(sbase + L::kDO1, 16384);
   auto ph = [](int t) { return static_cast<uint32_t>((t >> 1) & 1); };
   auto oph = [](int t) { return static_cast<uint32_t>((t / L::kDOStages) & 1); };
+  // The whole warp runs the loop, so descriptor arithmetic stays warp-uniform;
+  // one elected lane issues the tensor-core instructions.
+  const bool leader = elect_one_sync() != 0;
 
   bool ok = true;
   int tg = 0;
@@ -415,17 +423,17 @@ __device__ void mma_role(const Ctx& c, const Params& p, uint32_t sbase, uint32_t
     // unit prologue: dP of the first tile, then S
     {
       const int ost = tg % L::kDOStages;
-      if (!(ok = wait(c, BAR_V_FULL, r & 1))) break;
-      if (!(ok = wait(c, BAR_DO_FULL + ost, oph(tg)))) break;
-      if (tg > 0 && !(ok = wait(c, BAR_DQ_EMPTY, (tg - 1) & 1))) break;
+      if (!(ok = wait_warp(c, BAR_V_FULL, r & 1))) break;
+      if (!(ok = wait_warp(c, BAR_DO_FULL + ost, oph(tg)))) break;
+      if (tg > 0 && !(ok = wait_warp(c, BAR_DQ_EMPTY, (tg - 1) & 1))) break;
       tc_fence_after();
-      M::nt(tdP, kV, ost ? kO1 : kO0);
-      mma_commit(bar_addr(c, BAR_DP_FULL));
-      if (!(ok = wait(c, BAR_K_FULL, r & 1))) break;
-      if (!(ok = wait(c, BAR_Q_FULL + (tg & 1), ph(tg)))) break;
+      if (leader) M::nt(tdP, kV, ost ? kO1 : kO0);
+      if (leader) mma_commit(bar_addr(c, BAR_DP_FULL));
+      if (!(ok = wait_warp(c, BAR_K_FULL, r & 1))) break;
+      if (!(ok = wait_warp(c, BAR_Q_FULL + (tg & 1), ph(tg)))) break;
       tc_fence_after();
-      M::nt(tS, kK, (tg & 1) ? kQ1 : kQ0);
-      mma_commit(bar_addr(c, BAR_S_FULL));
+      if (leader) M::nt(tS, kK, (tg & 1) ? kQ1 : kQ0);
+      if (leader) mma_commit(bar_addr(c, BAR_S_FULL));
     }
     for (int tl = 0; tl < w.T; ++tl) {
       const int t = tg + tl;
@@ -435,45 +443,46 @@ __device__ void mma_role(const Ctx& c, const Params& p, uint32_t sbase, uint32_t
       const uint32_t kQn = st ? kQ0 : kQ1, kOn = ostn ? kO1 : kO0;
       const uint32_t mQ = st ? mQ1 : mQ0, mO = ost ? mO1 : mO0;
       // dV += P_t^T dO_t (A = P_t^T in the S region)
-      if (!(ok = wait(c, BAR_P_FULL, t & 1))) break;
+      if (!(ok = wait_warp(c, BAR_P_FULL, t & 1))) break;
       tc_fence_after();
-      M::tn(tdV, tS, mO, tl > 0);
-      mma_commit(bar_addr(c, BAR_DO_EMPTY + ost));  // dP_t and dV_t were dO_t's readers
+      if (leader) M::tn(tdV, tS, mO, tl > 0);
+      if (leader) mma_commit(bar_addr(c, BAR_DO_EMPTY + ost));  // dP_t and dV_t were dO_t's readers
       // S_{t+1} = K Q_{t+1}^T into the S region (P_t^T there was read by dV_t)
       if (more) {
-        if (!(ok = wait(c, BAR_Q_FULL + (st ^ 1), ph(t + 1)))) break;
+        if (!(ok = wait_warp(c, BAR_Q_FULL + (st ^ 1), ph(t + 1)))) break;
         tc_fence_after();
-        M::nt(tS, kK, kQn);
-        mma_commit(bar_addr(c, BAR_S_FULL));
+        if (leader) M::nt(tS, kK, kQn);
+        if (leader) mma_commit(bar_addr(c, BAR_S_FULL));
       }
       // dQ tile of t into the dP region (the softmax has read dP_t), then
       // dK += dS_t^T Q_t, both from the shared dS tile
-      if (!(ok = wait(c, BAR_DS_FULL, t & 1))) break;
+      if (!(ok = wait_warp(c, BAR_DS_FULL, t & 1))) break;
       tc_fence_after();
-      M::dq(tdP, mK, mDS);
-      mma_commit(bar_addr(c, BAR_DQ_FULL));
-      M::dk(tdK, kDS, mQ, tl > 0);
-      mma_commit(bar_addr(c, BAR_Q_EMPTY + st));
-      mma_commit(bar_addr(c, BAR_DS_FREE));
+      if (leader) M::dq(tdP, mK, mDS);
+      if (leader) mma_commit(bar_addr(c, BAR_DQ_FULL));
+      if (leader) M::dk(tdK, kDS, mQ, tl > 0);
+      if (leader) mma_commit(bar_addr(c, BAR_Q_EMPTY + st));
+      if (leader) mma_commit(bar_addr(c, BAR_DS_FREE));
       // dP_{t+1} = V dO_{t+1}^T once the dQ tile has been drained
       if (more) {
-        if (!(ok = wait(c, BAR_DO_FULL + ostn, oph(t + 1)))) break;
-        if (!(ok = wait(c, BAR_DQ_EMPTY, t & 1))) break;
+        if (!(ok = wait_warp(c, BAR_DO_FULL + ostn, oph(t + 1)))) break;
+        if (!(ok = wait_warp(c, BAR_DQ_EMPTY, t & 1))) break;
         tc_fence_after();
-        M::nt(tdP, kV, kOn);
-        mma_commit(bar_addr(c, BAR_DP_FULL));
+        if (leader) M::nt(tdP, kV, kOn);
+        if (leader) mma_commit(bar_addr(c, BAR_DP_FULL));
       }
     }
     if (!ok) break;
     // completion of the unit's GEMMs: the epilogue may read dK, dV
-    mma_commit(bar_addr(c, BAR_UNIT_DONE));
+    if (leader) mma_commit(bar_addr(c, BAR_UNIT_DONE));
     tg += w.T;
   }
-  if (*c.abort) {
+  if (__any_sync(0xffffffffu, *c.abort != 0)) {
     // completion of everything issued before tensor memory is released
-    mma_commit(bar_addr(c, BAR_DRAIN));
+    if (leader) mma_commit(bar_addr(c, BAR_DRAIN));
     wait_drain(c, BAR_DRAIN, 0);
   }
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ softmax
@@ -803,8 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       producer_role<D, CAUSAL>(c, p, smem, sbase, &tm_q, &tm_k, &tm_v, &tm_do);
     } else if (warp == 1) {
-      if ((threadIdx.x & 31) == 0) mma_role<D, CAUSAL>(c, p, sbase, tmem);
-      __syncwarp();
+      mma_role<D, CAUSAL>(c, p, sbase, tmem);
     }
   } else if (warp < 12) {
     setmaxnreg_inc<kRegsSoftmax>();

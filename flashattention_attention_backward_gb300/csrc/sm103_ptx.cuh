@@ -121,6 +121,17 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 }
 
 // Named barrier that also ANDs a flag over the participating threads.
+// 1 in exactly one lane of the (fully converged) warp, 0 in the others.
+__device__ __forceinline__ uint32_t elect_one_sync() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred;
+}
+
 __device__ __forceinline__ bool named_bar_and(int id, int count, bool flag) {
   uint32_t out;
   asm volatile(
