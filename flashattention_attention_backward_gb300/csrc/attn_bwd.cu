@@ -121,8 +121,6 @@ struct Params {
   const float* lse;
   const float* dpsum;
   float* dq_accum;
-  __nv_bfloat16* dk;
-  __nv_bfloat16* dv;
   int B, H, H_kv, N;
   int n_blocks, m_blocks;
   int n_units;  // n_blocks * H_kv * B
@@ -202,12 +200,15 @@ __device__ __forceinline__ bool wait_warp(const Ctx& c, int bar, uint32_t parity
   return __all_sync(0xffffffffu, wait(c, bar, parity));
 }
 
-// Tile t of a CTA: query head h = g*G + t / per_head, query block
-// m_start + t % per_head (heads outer, query blocks inner).
+// Tile t of a unit: query blocks from the last one down to m_start, the G
+// query heads of the group inner. Units that start together then visit the
+// same query block of the same heads at the same time, so the Q and dO tiles
+// they share and the dQ accumulator rows they all add into are touched
+// within a short window and stay in L2.
 __device__ __forceinline__ void tile_coord(const Work& w, int t, int& h, int& m_block) {
-  const int hh = t / w.per_head;
-  h = w.g * w.G + hh;
-  m_block = w.m_start + (t - hh * w.per_head);
+  const int mi = t / w.G;
+  h = w.g * w.G + (t - mi * w.G);
+  m_block = w.m_start + w.per_head - 1 - mi;
 }
 
 // ------------------------------------------------------------------ producer
@@ -597,40 +598,86 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
   return true;
 }
 
-// dK (x tau) and dV of a finished unit, fp32 tensor memory -> bf16 global.
-// This warpgroup writes columns [half*D/2, (half+1)*D/2) of its key row.
+// Named barriers of the softmax warpgroups (ids 1, 2 belong to the dQ drain).
+constexpr int kBarSoftmaxHalf = 3;  // + half, 128 threads
+constexpr int kBarSoftmaxAll = 5;   // 256 threads
+
+// dK (x tau) and dV of a finished unit: fp32 tensor memory -> bf16 rows in
+// the shared dS buffer (free once the unit's GEMMs are done) -> TMA tensor
+// stores, which write whole lines instead of one 16-byte piece per row and
+// keep the store traffic off the load/store path. The buffer holds 128 rows
+// x 128 bytes per 64-column box with the 128-byte swizzle of the tensor maps.
+//   d = 128: two rounds (dV, then dK); warpgroup `half` stages and stores
+//            box `half` (columns 64*half ..) of each matrix.
+//   d =  64: one round; dV in the first 16 KB, dK in the second, each row
+//            split between the warpgroups (32 columns each).
+// On return the buffer may be written again (the stores have read it).
 template <int D>
-__device__ __forceinline__ void epilogue(const Params& p, const Work& w, uint32_t tmem, int half,
-                                         int r) {
-  const int key = w.n_block * kBc + r;
+__device__ __forceinline__ void epilogue(const Params& p, const Work& w, uint32_t sbase,
+                                         uint32_t tmem, int half, int r,
+                                         const CUtensorMap* tm_dk, const CUtensorMap* tm_dv) {
+  using L = Layout<D>;
+  const int lane = threadIdx.x & 31;
+  const bool leader = ((threadIdx.x >> 5) & 3) == 0 && lane == 0;  // one per warpgroup
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
-  const long long row = (static_cast<long long>(w.b) * p.H_kv + w.g) * p.N + key;
+  const int kvh = w.b * p.H_kv + w.g;
+  const int row0 = w.n_block * kBc;
+  constexpr int kRounds = D == 128 ? 2 : 1;
 #pragma unroll
-  for (int which = 0; which < 2; ++which) {
-    const uint32_t col_base = (which == 0 ? 256u : 384u) + half * (D / 2);
-    __nv_bfloat16* out = (which == 0 ? p.dv : p.dk) + row * D + half * (D / 2);
-    const float mul = which == 0 ? 1.f : p.scale;
+  for (int round = 0; round < kRounds; ++round) {
 #pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) {
-      uint32_t raw[16];
-      tmem_ld16(tmem + lane_base + col_base + ch * 16, raw);
-      uint32_t packed[8];
+    for (int m = 0; m < 2; ++m) {
+      const int which = D == 128 ? round : m;  // 0 = dV, 1 = dK
+      if (D == 128 && m == 1) break;
+      const uint32_t col_base = (which == 0 ? 256u : 384u) + half * (D / 2);
+      const float mul = which == 0 ? 1.f : p.scale;
+      // this thread's row in its box, and the 16-byte chunk of the row where
+      // its columns start
+      const uint32_t box = sbase + L::kDS + (D == 128 ? half * 16384 : which * 16384);
+      const uint32_t row_addr = box + r * 128;
+      const int chunk0 = D == 128 ? 0 : 4 * half;
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        packed[u] = pack_bf16x2(__uint_as_float(raw[2 * u]) * mul,
-                                __uint_as_float(raw[2 * u + 1]) * mul);
-      if (key < p.N) {
-        uint4* dst = reinterpret_cast<uint4*>(out + ch * 16);
-        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t raw[16];
+        tmem_ld16(tmem + lane_base + col_base + ch * 16, raw);
+        uint32_t packed[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          packed[u] = pack_bf16x2(__uint_as_float(raw[2 * u]) * mul,
+                                  __uint_as_float(raw[2 * u + 1]) * mul);
+        const int c0 = chunk0 + 2 * ch;
+        st_shared_v4(row_addr + ((c0 ^ (r & 7)) << 4), packed[0], packed[1], packed[2],
+                     packed[3]);
+        st_shared_v4(row_addr + (((c0 + 1) ^ (r & 7)) << 4), packed[4], packed[5], packed[6],
+                     packed[7]);
       }
+    }
+    fence_proxy_async_smem();
+    if (D == 128) {
+      named_bar_sync(kBarSoftmaxHalf + half, 128);
+      if (leader) {
+        tma_store_3d(round == 0 ? tm_dv : tm_dk, sbase + L::kDS + half * 16384, 64 * half, row0,
+                     kvh);
+        bulk_commit_group();
+        bulk_wait_read_all();
+      }
+      named_bar_sync(kBarSoftmaxHalf + half, 128);
+    } else {
+      named_bar_sync(kBarSoftmaxAll, 256);
+      if (leader && half == 0) {
+        tma_store_3d(tm_dv, sbase + L::kDS, 0, row0, kvh);
+        tma_store_3d(tm_dk, sbase + L::kDS + 16384, 0, row0, kvh);
+        bulk_commit_group();
+        bulk_wait_read_all();
+      }
+      named_bar_sync(kBarSoftmaxAll, 256);
     }
   }
 }
 
 template <int D, bool CAUSAL, bool SOFTCAP>
 __device__ void softmax_role(const Ctx& c, const Params& p, uint8_t* smem, uint32_t sbase,
-                             uint32_t tmem) {
+                             uint32_t tmem, const CUtensorMap* tm_dk, const CUtensorMap* tm_dv) {
   const int warp = threadIdx.x >> 5;
   const int half = (warp - 4) >> 2;
   const int r = ((warp & 3) << 5) + (threadIdx.x & 31);
@@ -657,14 +704,20 @@ __device__ void softmax_role(const Ctx& c, const Params& p, uint8_t* smem, uint3
         ok = softmax_tile<D, SOFTCAP, CAUSAL, false>(c, p, smem, sbase, tmem, t, half, r, key,
                                                      m0);
     }
-    if (!ok || !(ok = wait(c, BAR_UNIT_DONE, ur & 1))) break;
+    if (ok) ok = wait(c, BAR_UNIT_DONE, ur & 1);
+    // the threads that meet at the epilogue's named barriers decide together
+    ok = D == 128 ? named_bar_and(kBarSoftmaxHalf + half, 128, ok)
+                  : named_bar_and(kBarSoftmaxAll, 256, ok);
+    if (!ok) break;
     tc_fence_after();
-    epilogue<D>(p, w, tmem, half, r);
+    epilogue<D>(p, w, sbase, tmem, half, r, tm_dk, tm_dv);
     // the next unit's first dV and dK overwrite the accumulators after
     // P_FULL of its first tile, which these warps arrive on only after this
     tc_fence_before();
     tg += w.T;
   }
+  // the last tensor stores must complete before the CTA exits
+  if ((warp & 3) == 0 && (threadIdx.x & 31) == 0) bulk_wait_all();
 }
 
 // ------------------------------------------------------------------ dQ drain
@@ -764,7 +817,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_do,
-                    const __grid_constant__ CUtensorMap tm_dq, const Params p) {
+                    const __grid_constant__ CUtensorMap tm_dq,
+                    const __grid_constant__ CUtensorMap tm_dk,
+                    const __grid_constant__ CUtensorMap tm_dv, const Params p) {
   using L = Layout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -816,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 12) {
     setmaxnreg_inc<kRegsSoftmax>();
-    softmax_role<D, CAUSAL, SOFTCAP>(c, p, smem, sbase, tmem);
+    softmax_role<D, CAUSAL, SOFTCAP>(c, p, smem, sbase, tmem, &tm_dk, &tm_dv);
   } else {
     setmaxnreg_dec<kRegsDq>();
     dq_role<D, CAUSAL>(c, p, smem, sbase, tmem, &tm_dq);
@@ -829,9 +884,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Tensor maps of one call: loads of Q, K, V, dO; reductions into dq_accum;
+// stores of dK, dV.
+struct Maps {
+  CUtensorMap q, k, v, dO, dq, dk, dv;
+};
+
 template <int D, bool CAUSAL, bool SOFTCAP>
-int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-           const CUtensorMap& tdo, const CUtensorMap& tdq, const Params& p, cudaStream_t stream) {
+int launch(const Maps& m, const Params& p, cudaStream_t stream) {
   auto kern = attn_bwd_kernel<D, CAUSAL, SOFTCAP>;
   static bool configured = false;
   if (!configured) {
@@ -844,7 +904,7 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
   const int sms = sm_count();
   if (sms <= 0) return ATTN_ERR_LAUNCH;
   const int grid = p.n_units < sms ? p.n_units : sms;
-  kern<<<grid, kThreads, Layout<D>::kBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
+  kern<<<grid, kThreads, Layout<D>::kBytes, stream>>>(m.q, m.k, m.v, m.dO, m.dq, m.dk, m.dv, p);
   return launch_status();
 }
 
@@ -868,20 +928,21 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
     return ATTN_ERR_ALIGN;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
 
-  CUtensorMap tq, tk, tv, tdo, tdq;
+  bwd::Maps m;
   const long long hq = static_cast<long long>(B) * H, hk = static_cast<long long>(B) * H_kv;
-  if (!encode_bf16_3d(&tq, q, d, N, hq, bwd::kBr) || !encode_bf16_3d(&tk, k, d, N, hk, bwd::kBc) ||
-      !encode_bf16_3d(&tv, v, d, N, hk, bwd::kBc) ||
-      !encode_bf16_3d(&tdo, dO, d, N, hq, bwd::kBr) ||
-      !encode_f32_3d(&tdq, dq_accum, d, N, hq, 32))
+  if (!encode_bf16_3d(&m.q, q, d, N, hq, bwd::kBr) ||
+      !encode_bf16_3d(&m.k, k, d, N, hk, bwd::kBc) ||
+      !encode_bf16_3d(&m.v, v, d, N, hk, bwd::kBc) ||
+      !encode_bf16_3d(&m.dO, dO, d, N, hq, bwd::kBr) ||
+      !encode_f32_3d(&m.dq, dq_accum, d, N, hq, 32) ||
+      !encode_bf16_3d(&m.dk, dk, d, N, hk, bwd::kBc) ||
+      !encode_bf16_3d(&m.dv, dv, d, N, hk, bwd::kBc))
     return ATTN_ERR_LAUNCH;
 
   bwd::Params p;
   p.lse = lse;
   p.dpsum = dpsum;
   p.dq_accum = dq_accum;
-  p.dk = static_cast<__nv_bfloat16*>(dk);
-  p.dv = static_cast<__nv_bfloat16*>(dv);
   p.B = B;
   p.H = H;
   p.H_kv = H_kv;
@@ -897,15 +958,15 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   cudaStream_t s = as_stream(stream);
   const bool cs = causal != 0;
   if (d == 128) {
-    if (cs) return cap ? bwd::launch<128, true, true>(tq, tk, tv, tdo, tdq, p, s)
-                       : bwd::launch<128, true, false>(tq, tk, tv, tdo, tdq, p, s);
-    return cap ? bwd::launch<128, false, true>(tq, tk, tv, tdo, tdq, p, s)
-               : bwd::launch<128, false, false>(tq, tk, tv, tdo, tdq, p, s);
+    if (cs) return cap ? bwd::launch<128, true, true>(m, p, s)
+                       : bwd::launch<128, true, false>(m, p, s);
+    return cap ? bwd::launch<128, false, true>(m, p, s)
+               : bwd::launch<128, false, false>(m, p, s);
   }
-  if (cs) return cap ? bwd::launch<64, true, true>(tq, tk, tv, tdo, tdq, p, s)
-                     : bwd::launch<64, true, false>(tq, tk, tv, tdo, tdq, p, s);
-  return cap ? bwd::launch<64, false, true>(tq, tk, tv, tdo, tdq, p, s)
-             : bwd::launch<64, false, false>(tq, tk, tv, tdo, tdq, p, s);
+  if (cs) return cap ? bwd::launch<64, true, true>(m, p, s)
+                     : bwd::launch<64, true, false>(m, p, s);
+  return cap ? bwd::launch<64, false, true>(m, p, s)
+             : bwd::launch<64, false, false>(m, p, s);
 }
 
 extern "C" int attn_device_status(int* status, int clear, void* stream) {

@@ -103,6 +103,15 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src
       "r"(src), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// TMA tensor store shared -> global (bulk async-group completion).
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
