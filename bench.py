@@ -300,7 +300,51 @@ def run_ours(args, w):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    if world == 1 and not args.no_all_configs:
+        del q, k, v, do, o, lse, bufs, pin, h_o, h_lse, h_out
+        torch.cuda.empty_cache()
+        line["all_configs"] = all_configs(dev, peaks["bf16_tflops"])
     return line
+
+
+def all_configs(dev, peak, iters=20, warmup=3):
+    """attn_bwd alone on each named workload (CUDA events around each launch,
+    median of `iters`): ms, TFLOP/s and the fraction of the bf16 peak."""
+    import flashattention_attention_backward_gb300 as attn
+    from flashattention_attention_backward_gb300 import runner
+    from flashattention_attention_backward_gb300.inputs import WORKLOADS, make_inputs
+
+    out = {}
+    stream = torch.cuda.current_stream(dev)
+    for name, w in WORKLOADS.items():
+        x = make_inputs(w)
+        q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+        o, lse = runner.forward(q, k, v, w.scale, w.causal, w.softcap)
+        bufs = runner.BackwardBuffers(q, k)
+        times = []
+        for i in range(warmup + iters):
+            attn.check(attn.attn_bwd_preprocess(o, do, bufs.dpsum, bufs.dq_accum, w.B, w.H, w.N,
+                                                w.d, stream))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            attn.check(attn.attn_bwd(q, k, v, o, do, lse, bufs.dq_accum, bufs.dk, bufs.dv, w.B,
+                                     w.H, w.H_kv, w.N, w.d, w.scale, w.causal, w.softcap,
+                                     bufs.dpsum, stream))
+            e1.record(stream)
+            if i >= warmup:
+                times.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        rc, status = attn.attn_device_status(clear=True, stream=stream)
+        if rc != 0 or status != 0:
+            raise RuntimeError("device status %d on %s" % (status, name))
+        ms = sorted(a.elapsed_time(b) for a, b in times)[len(times) // 2]
+        tf = w.flops() / (ms * 1e-3) / 1e12
+        out[name] = {"B": w.B, "H": w.H, "H_kv": w.H_kv, "N": w.N, "d": w.d,
+                     "causal": w.causal, "softcap": w.softcap, "bwd_ms": ms,
+                     "tflops": tf, "frac_of_peak": tf / peak}
+        del x, q, k, v, do, o, lse, bufs
+        torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------- the oracle on the host
@@ -387,6 +431,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="causal_gqa", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-all-configs", action="store_true",
+                    help="skip the per-workload attn_bwd timings added to the line")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=120.0)
     args = ap.parse_args(argv)

@@ -92,7 +92,7 @@ struct Layout {
   static constexpr int kLSE = kDQS + kDQSBytes;  // 2 stages x 128 fp32 (LSE*log2e)
   static constexpr int kDsum = kLSE + 2 * kBr * 4;  // 2 stages x 128 fp32 (D)
   static constexpr int kBars = kDsum + 2 * kBr * 4;
-  static constexpr int kNumBars = 19;
+  static constexpr int kNumBars = 21;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kBytes = kAbort + 12;
@@ -115,6 +115,8 @@ enum Bar {
   BAR_DS_FREE = 16,
   BAR_V_FULL = 17,
   BAR_DRAIN = 18,      // abort path only: completion of everything issued
+  BAR_ACC_FREE = 19,   // dK, dV of the previous unit read out: the next may overwrite them
+  BAR_DSBUF_FREE = 20, // the epilogue's stores have read the dS buffer
 };
 
 struct Params {
@@ -393,9 +395,8 @@ struct Mma {
 // Tiles are numbered t over all units of the CTA, so every per-tile barrier
 // keeps one phase per tile across unit boundaries. A unit starts with dP of
 // its first tile (V and dO usually land before K); its first dV and dK
-// overwrite the accumulators, which is safe because the softmax warps read
-// the previous unit's dK, dV in the epilogue before they arrive on P_FULL of
-// the unit's first tile, and dV waits on P_FULL.
+// overwrite the accumulators only after ACC_FREE, i.e. once the drain warps
+// have read the previous unit's dK, dV out of tensor memory.
 template <int D, bool CAUSAL>
 __device__ void mma_role(const Ctx& c, const Params& p, uint32_t sbase, uint32_t tmem) {
   using L = Layout<D>;
@@ -445,6 +446,9 @@ __device__ void mma_role(const Ctx& c, const Params& p, uint32_t sbase, uint32_t
       const uint32_t mQ = st ? mQ1 : mQ0, mO = ost ? mO1 : mO0;
       // dV += P_t^T dO_t (A = P_t^T in the S region)
       if (!(ok = wait_warp(c, BAR_P_FULL, t & 1))) break;
+      // the first dV and dK of a unit overwrite the accumulators: the
+      // previous unit's epilogue must have read them out
+      if (tl == 0 && r > 0 && !(ok = wait_warp(c, BAR_ACC_FREE, (r - 1) & 1))) break;
       tc_fence_after();
       if (leader) M::tn(tdV, tS, mO, tl > 0);
       if (leader) mma_commit(bar_addr(c, BAR_DO_EMPTY + ost));  // dP_t and dV_t were dO_t's readers
@@ -492,7 +496,7 @@ __device__ void mma_role(const Ctx& c, const Params& p, uint32_t sbase, uint32_t
 template <int D, bool SOFTCAP, bool CAUSAL, bool MASKED>
 __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint8_t* smem,
                                              uint32_t sbase, uint32_t tmem, int t, int half,
-                                             int r, int key, int m0) {
+                                             int r, int key, int m0, int dsbuf_parity) {
   using L = Layout<D>;
   const int st = t & 1;
   const int lane = threadIdx.x & 31;
@@ -558,6 +562,10 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
   if (!wait(c, BAR_DP_FULL, t & 1)) return false;
   // the previous tile's dQ and dK GEMMs must be done reading the shared dS tile
   if (t > 0 && !wait(c, BAR_DS_FREE, (t - 1) & 1)) return false;
+  // first tile of a unit: the previous unit's dK/dV stores must have read
+  // the buffer first
+  if (dsbuf_parity >= 0 && !wait(c, BAR_DSBUF_FREE, static_cast<uint32_t>(dsbuf_parity)))
+    return false;
   tc_fence_after();
   const uint32_t ds_row = sbase + L::kDS + half * 16384 + r * 128;
 #pragma unroll
@@ -598,86 +606,9 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
   return true;
 }
 
-// Named barriers of the softmax warpgroups (ids 1, 2 belong to the dQ drain).
-constexpr int kBarSoftmaxHalf = 3;  // + half, 128 threads
-constexpr int kBarSoftmaxAll = 5;   // 256 threads
-
-// dK (x tau) and dV of a finished unit: fp32 tensor memory -> bf16 rows in
-// the shared dS buffer (free once the unit's GEMMs are done) -> TMA tensor
-// stores, which write whole lines instead of one 16-byte piece per row and
-// keep the store traffic off the load/store path. The buffer holds 128 rows
-// x 128 bytes per 64-column box with the 128-byte swizzle of the tensor maps.
-//   d = 128: two rounds (dV, then dK); warpgroup `half` stages and stores
-//            box `half` (columns 64*half ..) of each matrix.
-//   d =  64: one round; dV in the first 16 KB, dK in the second, each row
-//            split between the warpgroups (32 columns each).
-// On return the buffer may be written again (the stores have read it).
-template <int D>
-__device__ __forceinline__ void epilogue(const Params& p, const Work& w, uint32_t sbase,
-                                         uint32_t tmem, int half, int r,
-                                         const CUtensorMap* tm_dk, const CUtensorMap* tm_dv) {
-  using L = Layout<D>;
-  const int lane = threadIdx.x & 31;
-  const bool leader = ((threadIdx.x >> 5) & 3) == 0 && lane == 0;  // one per warpgroup
-  const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
-  const int kvh = w.b * p.H_kv + w.g;
-  const int row0 = w.n_block * kBc;
-  constexpr int kRounds = D == 128 ? 2 : 1;
-#pragma unroll
-  for (int round = 0; round < kRounds; ++round) {
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {
-      const int which = D == 128 ? round : m;  // 0 = dV, 1 = dK
-      if (D == 128 && m == 1) break;
-      const uint32_t col_base = (which == 0 ? 256u : 384u) + half * (D / 2);
-      const float mul = which == 0 ? 1.f : p.scale;
-      // this thread's row in its box, and the 16-byte chunk of the row where
-      // its columns start
-      const uint32_t box = sbase + L::kDS + (D == 128 ? half * 16384 : which * 16384);
-      const uint32_t row_addr = box + r * 128;
-      const int chunk0 = D == 128 ? 0 : 4 * half;
-#pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t raw[16];
-        tmem_ld16(tmem + lane_base + col_base + ch * 16, raw);
-        uint32_t packed[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          packed[u] = pack_bf16x2(__uint_as_float(raw[2 * u]) * mul,
-                                  __uint_as_float(raw[2 * u + 1]) * mul);
-        const int c0 = chunk0 + 2 * ch;
-        st_shared_v4(row_addr + ((c0 ^ (r & 7)) << 4), packed[0], packed[1], packed[2],
-                     packed[3]);
-        st_shared_v4(row_addr + (((c0 + 1) ^ (r & 7)) << 4), packed[4], packed[5], packed[6],
-                     packed[7]);
-      }
-    }
-    fence_proxy_async_smem();
-    if (D == 128) {
-      named_bar_sync(kBarSoftmaxHalf + half, 128);
-      if (leader) {
-        tma_store_3d(round == 0 ? tm_dv : tm_dk, sbase + L::kDS + half * 16384, 64 * half, row0,
-                     kvh);
-        bulk_commit_group();
-        bulk_wait_read_all();
-      }
-      named_bar_sync(kBarSoftmaxHalf + half, 128);
-    } else {
-      named_bar_sync(kBarSoftmaxAll, 256);
-      if (leader && half == 0) {
-        tma_store_3d(tm_dv, sbase + L::kDS, 0, row0, kvh);
-        tma_store_3d(tm_dk, sbase + L::kDS + 16384, 0, row0, kvh);
-        bulk_commit_group();
-        bulk_wait_read_all();
-      }
-      named_bar_sync(kBarSoftmaxAll, 256);
-    }
-  }
-}
-
 template <int D, bool CAUSAL, bool SOFTCAP>
 __device__ void softmax_role(const Ctx& c, const Params& p, uint8_t* smem, uint32_t sbase,
-                             uint32_t tmem, const CUtensorMap* tm_dk, const CUtensorMap* tm_dv) {
+                             uint32_t tmem) {
   const int warp = threadIdx.x >> 5;
   const int half = (warp - 4) >> 2;
   const int r = ((warp & 3) << 5) + (threadIdx.x & 31);
@@ -698,22 +629,14 @@ __device__ void softmax_role(const Ctx& c, const Params& p, uint8_t* smem, uint3
       const int m0 = m_block * kBr;
       if (!(ok = wait(c, BAR_Q_FULL + (t & 1), (t >> 1) & 1))) break;
       const bool masked = (CAUSAL && m_block == w.n_block) || key_tail || (m0 + kBr > p.N);
+      const int dsbuf = (tl == 0 && ur > 0) ? ((ur - 1) & 1) : -1;
       if (masked)
-        ok = softmax_tile<D, SOFTCAP, CAUSAL, true>(c, p, smem, sbase, tmem, t, half, r, key, m0);
+        ok = softmax_tile<D, SOFTCAP, CAUSAL, true>(c, p, smem, sbase, tmem, t, half, r, key, m0,
+                                                    dsbuf);
       else
         ok = softmax_tile<D, SOFTCAP, CAUSAL, false>(c, p, smem, sbase, tmem, t, half, r, key,
-                                                     m0);
+                                                     m0, dsbuf);
     }
-    if (ok) ok = wait(c, BAR_UNIT_DONE, ur & 1);
-    // the threads that meet at the epilogue's named barriers decide together
-    ok = D == 128 ? named_bar_and(kBarSoftmaxHalf + half, 128, ok)
-                  : named_bar_and(kBarSoftmaxAll, 256, ok);
-    if (!ok) break;
-    tc_fence_after();
-    epilogue<D>(p, w, sbase, tmem, half, r, tm_dk, tm_dv);
-    // the next unit's first dV and dK overwrite the accumulators after
-    // P_FULL of its first tile, which these warps arrive on only after this
-    tc_fence_before();
     tg += w.T;
   }
   // the last tensor stores must complete before the CTA exits
@@ -723,11 +646,101 @@ __device__ void softmax_role(const Ctx& c, const Params& p, uint8_t* smem, uint3
 // ------------------------------------------------------------------ dQ drain
 // Two warpgroups, each owning half of the dQ tile's columns. A thread loads
 // its share from tensor memory, the warp frees the region (DQ_EMPTY), and
-// only then are the fp32 atomic adds issued, so the reduction overlaps the
-// next tile's GEMMs.
+// only then is the share added into dq_accum, so the reduction overlaps the
+// next tile's GEMMs. After a unit's last tile the same warps write its dK and
+// dV (the epilogue), so the softmax warps go on with the next unit at once.
+
+constexpr int kBarDqAll = 3;  // named barrier of both drain warpgroups (ids 1, 2: one each)
+
+// 16-column pieces of this thread's tensor-memory row -> bf16 -> 16-byte
+// chunks chunk0, chunk0 + 1, ... of a 128-byte shared-memory row, placed by
+// the 128-byte swizzle (chunk c of row r at c ^ (r & 7)).
+template <int COLS>
+__device__ __forceinline__ void stage_row_bf16(uint32_t taddr, float mul, uint32_t row_addr,
+                                               int chunk0, int r) {
+#pragma unroll
+  for (int ch = 0; ch < COLS / 16; ++ch) {
+    uint32_t raw[16];
+    tmem_ld16(taddr + ch * 16, raw);
+    uint32_t packed[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      packed[u] = pack_bf16x2(__uint_as_float(raw[2 * u]) * mul,
+                              __uint_as_float(raw[2 * u + 1]) * mul);
+    const int c0 = chunk0 + 2 * ch;
+    st_shared_v4(row_addr + ((c0 ^ (r & 7)) << 4), packed[0], packed[1], packed[2], packed[3]);
+    st_shared_v4(row_addr + (((c0 + 1) ^ (r & 7)) << 4), packed[4], packed[5], packed[6],
+                 packed[7]);
+  }
+}
+
+// dK (x tau) and dV of a finished unit: fp32 tensor memory -> bf16 rows in
+// shared memory -> TMA tensor stores, which write whole lines. Thread = key
+// row r (tensor-memory lane). Each 64-column box is 128 rows x 128 bytes with
+// the swizzle of the tensor maps.
+//   d = 128: warpgroup `part` handles box `part` (columns 64*part ..) of each
+//            matrix: dV into the dS buffer (free once the unit's GEMMs are
+//            done), dK into its own dQ staging buffer (once its last
+//            reduction has read it).
+//   d =  64: dV and dK fill the two halves of the dS buffer; warpgroup
+//            `part` writes 32 columns of each row.
+// ACC_FREE is arrived on as soon as tensor memory has been read; DSBUF_FREE
+// once the stores have read the dS buffer. Returns false when aborting.
+template <int D>
+__device__ __forceinline__ bool dq_epilogue(const Ctx& c, const Params& p, int kvh, int row0,
+                                            uint32_t sbase, uint32_t tmem, uint32_t stage,
+                                            int part, int r, int ur, bool leader,
+                                            const CUtensorMap* tm_dk, const CUtensorMap* tm_dv) {
+  using L = Layout<D>;
+  const int lane = threadIdx.x & 31;
+  const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
+  // the threads that meet at the named barriers below decide together
+  bool ok = wait(c, BAR_UNIT_DONE, ur & 1);
+  ok = D == 128 ? named_bar_and(1 + part, 128, ok) : named_bar_and(kBarDqAll, 256, ok);
+  if (!ok) return false;
+  tc_fence_after();
+  if (D == 128) {
+    stage_row_bf16<64>(tmem + lane_base + 256 + part * 64, 1.f,
+                       sbase + L::kDS + part * 16384 + r * 128, 0, r);
+    if (leader) bulk_wait_read_all();  // the last dQ reduction has read the staging buffer
+    named_bar_sync(1 + part, 128);
+    stage_row_bf16<64>(tmem + lane_base + 384 + part * 64, p.scale, stage + r * 128, 0, r);
+  } else {
+    stage_row_bf16<32>(tmem + lane_base + 256 + part * 32, 1.f, sbase + L::kDS + r * 128,
+                       4 * part, r);
+    stage_row_bf16<32>(tmem + lane_base + 384 + part * 32, p.scale,
+                       sbase + L::kDS + 16384 + r * 128, 4 * part, r);
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar_addr(c, BAR_ACC_FREE));
+  fence_proxy_async_smem();
+  if (D == 128) {
+    named_bar_sync(1 + part, 128);
+    if (leader) {
+      tma_store_3d(tm_dv, sbase + L::kDS + part * 16384, 64 * part, row0, kvh);
+      tma_store_3d(tm_dk, stage, 64 * part, row0, kvh);
+      bulk_commit_group();
+      bulk_wait_read_all();
+      mbar_arrive(bar_addr(c, BAR_DSBUF_FREE));
+    }
+  } else {
+    named_bar_sync(kBarDqAll, 256);
+    if (leader && part == 0) {
+      tma_store_3d(tm_dv, sbase + L::kDS, 0, row0, kvh);
+      tma_store_3d(tm_dk, sbase + L::kDS + 16384, 0, row0, kvh);
+      bulk_commit_group();
+      bulk_wait_read_all();
+      mbar_arrive(bar_addr(c, BAR_DSBUF_FREE));
+    }
+  }
+  return true;
+}
+
 template <int D, bool CAUSAL>
 __device__ void dq_role(const Ctx& c, const Params& p, uint8_t* smem, uint32_t sbase,
-                        uint32_t tmem, const CUtensorMap* tm_dq) {
+                        uint32_t tmem, const CUtensorMap* tm_dq, const CUtensorMap* tm_dk,
+                        const CUtensorMap* tm_dv) {
   using L = Layout<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -735,79 +748,92 @@ __device__ void dq_role(const Ctx& c, const Params& p, uint8_t* smem, uint32_t s
   const int r = ((warp & 3) << 5) + lane;
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
   // d = 128: this warpgroup's staging buffer and the thread that issues its
-  // TMA reductions (the bulk async-group is per thread)
+  // TMA reductions and stores (the bulk async-group is per thread)
   const uint32_t stage = sbase + L::kDQS + part * 16384;
   const bool leader = (warp & 3) == 0 && lane == 0;
   (void)smem;
   bool ok = true;
-  int tg = 0;
-  Work w;
-  w.T = 0;
+  int tg = 0, T = 0, head0 = 0, kvh = 0, row0 = 0, hh = 0, m_block = 0;
+  const int G = p.H / p.H_kv;
   for (int ur = 0, tl = 0; ok; ++tl) {
-    if (tl == w.T) {  // next unit
-      tg += w.T;
+    if (tl == T) {  // unit boundary: epilogue of the finished unit, then the next unit
+      if (ur > 0 && !(ok = dq_epilogue<D>(c, p, kvh, row0, sbase, tmem, stage, part, r, ur - 1,
+                                          leader, tm_dk, tm_dv)))
+        break;
+      tg += T;
       tl = 0;
       const int u = unit_of(ur++, p.n_units);
       if (u < 0) break;
+      Work w;
       unit_work<CAUSAL>(p, u, w);
+      kvh = w.b * p.H_kv + w.g;
+      row0 = w.n_block * kBc;
+      T = w.T;
+      head0 = w.b * p.H + w.g * G;
+      hh = 0;
+      m_block = p.m_blocks - 1;
     }
-    const int t = tg + tl;
-    int h, m_block;
-    tile_coord(w, tl, h, m_block);
-    const int m0 = m_block * kBr;
-    const long long bh = static_cast<long long>(w.b) * p.H + h;
     {
-      // d = 128: the whole warpgroup takes the same decision (its members
-      // meet at named barriers below)
-      ok = wait(c, BAR_DQ_FULL, t & 1);
-      if (D == 128) ok = named_bar_and(1 + part, 128, ok);
-      if (!ok) break;
-    }
-    tc_fence_after();
-    if (D == 128) {
-      // lane r holds dQ[m0 + i][r] in column 128 + i. The tile leaves tensor
-      // memory at once; each 32-query chunk is then written to the staging
-      // buffer as rows of 128 floats and added into dq_accum by one TMA
-      // reduction, which keeps the atomics off the load/store path the
-      // softmax warps use.
-      uint32_t v[64];
-      tmem_ld32x2(tmem + lane_base + 128 + part * 64, tmem + lane_base + 128 + part * 64 + 32, v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(c, BAR_DQ_EMPTY));
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        if (leader) bulk_wait_read_all();  // previous reduction has read the buffer
-        named_bar_sync(1 + part, 128);
-#pragma unroll
-        for (int q = 0; q < 32; ++q)
-          st_shared_f32(stage + q * 512 + r * 4, __uint_as_float(v[ch * 32 + q]));
-        fence_proxy_async_smem();
-        named_bar_sync(1 + part, 128);
-        const int row = m0 + part * 64 + ch * 32;
-        if (leader && row < p.N) {
-          tma_reduce_add_3d(tm_dq, stage, 0, row, static_cast<int>(bh));
-          bulk_commit_group();
-        }
+      const int t = tg + tl;
+      const int m0 = m_block * kBr;
+      const long long bh = head0 + hh;
+      if (++hh == G) {
+        hh = 0;
+        --m_block;
       }
-    } else {
-      // lane r holds query row m0 + r; columns 128 + [0, 64) are dQ[m0 + r][:]
-      uint32_t v[32];
-      tmem_ld32(tmem + lane_base + 128 + part * 32, v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(c, BAR_DQ_EMPTY));
-      if (m0 + r < p.N) {
-        float* dst = p.dq_accum + (bh * p.N + m0 + r) * D + part * 32;
+      // the threads that meet at named barriers (each warpgroup for d = 128,
+      // both in the d = 64 epilogue) take the same decision
+      ok = wait(c, BAR_DQ_FULL, t & 1);
+      ok = D == 128 ? named_bar_and(1 + part, 128, ok) : named_bar_and(kBarDqAll, 256, ok);
+      if (!ok) break;
+      tc_fence_after();
+      if (D == 128) {
+        // lane r holds dQ[m0 + i][r] in column 128 + i. The tile leaves tensor
+        // memory at once; each 32-query chunk is then written to the staging
+        // buffer as rows of 128 floats and added into dq_accum by one TMA
+        // reduction, which keeps the atomics off the load/store path the
+        // softmax warps use.
+        uint32_t v[64];
+        tmem_ld32x2(tmem + lane_base + 128 + part * 64, tmem + lane_base + 128 + part * 64 + 32,
+                    v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_addr(c, BAR_DQ_EMPTY));
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          red_add_v4_f32(dst + 4 * u, __uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                         __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+        for (int ch = 0; ch < 2; ++ch) {
+          if (leader) bulk_wait_read_all();  // previous reduction has read the buffer
+          named_bar_sync(1 + part, 128);
+#pragma unroll
+          for (int q = 0; q < 32; ++q)
+            st_shared_f32(stage + q * 512 + r * 4, __uint_as_float(v[ch * 32 + q]));
+          fence_proxy_async_smem();
+          named_bar_sync(1 + part, 128);
+          const int row = m0 + part * 64 + ch * 32;
+          if (leader && row < p.N) {
+            tma_reduce_add_3d(tm_dq, stage, 0, row, static_cast<int>(bh));
+            bulk_commit_group();
+          }
+        }
+      } else {
+        // lane r holds query row m0 + r; columns 128 + [0, 64) are dQ[m0 + r][:]
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + 128 + part * 32, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_addr(c, BAR_DQ_EMPTY));
+        if (m0 + r < p.N) {
+          float* dst = p.dq_accum + (bh * p.N + m0 + r) * D + part * 32;
+#pragma unroll
+          for (int u4 = 0; u4 < 8; ++u4)
+            red_add_v4_f32(dst + 4 * u4, __uint_as_float(v[4 * u4]),
+                           __uint_as_float(v[4 * u4 + 1]), __uint_as_float(v[4 * u4 + 2]),
+                           __uint_as_float(v[4 * u4 + 3]));
+        }
       }
     }
   }
-  // the reductions must complete before the CTA exits
-  if (D == 128 && leader) bulk_wait_all();
+  // the reductions and stores must complete before the CTA exits
+  if (leader) bulk_wait_all();
 }
 
 // ------------------------------------------------------------------ kernel
@@ -850,6 +876,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_addr(c, BAR_UNIT_DONE), 1);
     mbar_init(bar_addr(c, BAR_DS_FREE), 1);
     mbar_init(bar_addr(c, BAR_DRAIN), 1);
+    mbar_init(bar_addr(c, BAR_ACC_FREE), 8);                   // the 8 drain warps
+    mbar_init(bar_addr(c, BAR_DSBUF_FREE), D == 128 ? 2 : 1);  // the store-issuing threads
     *c.abort = 0;
     fence_barrier_init();
   }
@@ -871,10 +899,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 12) {
     setmaxnreg_inc<kRegsSoftmax>();
-    softmax_role<D, CAUSAL, SOFTCAP>(c, p, smem, sbase, tmem, &tm_dk, &tm_dv);
+    softmax_role<D, CAUSAL, SOFTCAP>(c, p, smem, sbase, tmem);
   } else {
     setmaxnreg_dec<kRegsDq>();
-    dq_role<D, CAUSAL>(c, p, smem, sbase, tmem, &tm_dq);
+    dq_role<D, CAUSAL>(c, p, smem, sbase, tmem, &tm_dq, &tm_dk, &tm_dv);
   }
   tc_fence_before();
   __syncthreads();
