@@ -82,13 +82,13 @@ struct Layout {
   static constexpr int kQ1 = kQ0 + kTileBytes;
   // d = 128: one dO stage, and the freed 32 KB stage the dQ tile for TMA
   // reductions (two 16 KB buffers, [32 queries][128 d] fp32). d = 64: two
-  // dO stages and no staging (its dQ goes out with 16-byte atomics).
+  // dO stages and two 4 KB buffers per drain warp ([32 queries][32 d] fp32).
   static constexpr int kDOStages = D == 128 ? 1 : 2;
   static constexpr int kDO0 = kQ1 + kTileBytes;
   static constexpr int kDO1 = kDO0 + (kDOStages - 1) * kTileBytes;
   static constexpr int kDS = kDO0 + kDOStages * kTileBytes;  // dS^T, [key][query], 32 KB
-  static constexpr int kDQS = kDS + kBc * kBr * 2;            // dQ staging (d = 128)
-  static constexpr int kDQSBytes = D == 128 ? 2 * 16384 : 0;
+  static constexpr int kDQS = kDS + kBc * kBr * 2;            // dQ staging
+  static constexpr int kDQSBytes = D == 128 ? 2 * 16384 : 8 * 2 * 4096;
   static constexpr int kLSE = kDQS + kDQSBytes;  // 2 stages x 128 fp32 (LSE*log2e)
   static constexpr int kDsum = kLSE + 2 * kBr * 4;  // 2 stages x 128 fp32 (D)
   static constexpr int kBars = kDsum + 2 * kBr * 4;
@@ -511,12 +511,25 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
   // ---- P = exp(S - LSE) -> bf16 P^T in tensor memory
   if (!wait(c, BAR_S_FULL, t & 1)) return false;
   tc_fence_after();
-  {
-    uint32_t raw[64];
-    tmem_ld32x2(tmem + lane_base + half * 64, tmem + lane_base + half * 64 + 32, raw);
+  // In kPasses column groups: with a softcap each element takes three MUFU
+  // operations in a dependent chain, and loading half the row at a time
+  // leaves the registers for more of those chains in flight. P^T of a group
+  // (bf16 pairs) lands in columns whose S values were read by this or an
+  // earlier group.
+  constexpr int kPasses = SOFTCAP ? 2 : 1;
+  constexpr int kCols = 64 / kPasses;
 #pragma unroll
-    for (int j4 = 0; j4 < 16; ++j4) {
-      const float4 l4 = *reinterpret_cast<const float4*>(s_lse + half * 64 + 4 * j4);
+  for (int pass = 0; pass < kPasses; ++pass) {
+    uint32_t raw[kCols];
+    const uint32_t src = tmem + lane_base + half * 64 + pass * kCols;
+    if constexpr (kPasses == 1)
+      tmem_ld32x2(src, src + 32, raw);
+    else
+      tmem_ld32(src, raw);
+#pragma unroll
+    for (int j4 = 0; j4 < kCols / 4; ++j4) {
+      const float4 l4 =
+          *reinterpret_cast<const float4*>(s_lse + half * 64 + pass * kCols + 4 * j4);
       const float lse4[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -534,23 +547,23 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
           keep = prob;
         }
         if (MASKED) {
-          const int q = m0 + half * 64 + j;
+          const int q = m0 + half * 64 + pass * kCols + j;
           const bool ok = key < p.N && q < p.N && (!CAUSAL || key <= q);
           prob = ok ? prob : 0.f;
           keep = ok ? keep : 0.f;
         }
         raw[j] = __float_as_uint(prob);
-        pk[j] = keep;
+        pk[pass * kCols + j] = keep;
       }
     }
 #pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
+    for (int ch = 0; ch < kCols / 16; ++ch) {
       uint32_t packed[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u)
         packed[u] = pack_bf16x2(__uint_as_float(raw[16 * ch + 2 * u]),
                                 __uint_as_float(raw[16 * ch + 2 * u + 1]));
-      tmem_st8(tmem + lane_base + half * 64 + ch * 8, packed);
+      tmem_st8(tmem + lane_base + half * 64 + pass * (kCols / 2) + ch * 8, packed);
     }
   }
   tmem_wait_st();
@@ -639,8 +652,6 @@ __device__ void softmax_role(const Ctx& c, const Params& p, uint8_t* smem, uint3
     }
     tg += w.T;
   }
-  // the last tensor stores must complete before the CTA exits
-  if ((warp & 3) == 0 && (threadIdx.x & 31) == 0) bulk_wait_all();
 }
 
 // ------------------------------------------------------------------ dQ drain
@@ -821,19 +832,28 @@ __device__ void dq_role(const Ctx& c, const Params& p, uint8_t* smem, uint32_t s
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_addr(c, BAR_DQ_EMPTY));
-        if (m0 + r < p.N) {
-          float* dst = p.dq_accum + (bh * p.N + m0 + r) * D + part * 32;
+        // the warp's 32 rows x 32 columns go to one of its two 4 KB buffers
+        // (128-byte rows, 128-byte swizzle) and out with one TMA reduce-add
+        const uint32_t buf = sbase + L::kDQS + ((warp - 12) * 2 + (t & 1)) * 4096;
+        if (lane == 0) bulk_wait_read_1();  // the reduction of two tiles ago has read it
+        __syncwarp();
 #pragma unroll
-          for (int u4 = 0; u4 < 8; ++u4)
-            red_add_v4_f32(dst + 4 * u4, __uint_as_float(v[4 * u4]),
-                           __uint_as_float(v[4 * u4 + 1]), __uint_as_float(v[4 * u4 + 2]),
-                           __uint_as_float(v[4 * u4 + 3]));
+        for (int c4 = 0; c4 < 8; ++c4)
+          st_shared_v4(buf + lane * 128 + ((c4 ^ (lane & 7)) << 4), v[4 * c4], v[4 * c4 + 1],
+                       v[4 * c4 + 2], v[4 * c4 + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int row = m0 + 32 * (warp & 3);
+          if (row < p.N) tma_reduce_add_3d(tm_dq, buf, 32 * part, row, static_cast<int>(bh));
+          bulk_commit_group();  // one group per tile, empty or not
         }
       }
     }
   }
-  // the reductions and stores must complete before the CTA exits
-  if (leader) bulk_wait_all();
+  // the reductions and stores must complete before the CTA exits (each
+  // lane 0 may have issued some)
+  if (lane == 0) bulk_wait_all();
 }
 
 // ------------------------------------------------------------------ kernel
@@ -962,7 +982,7 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
       !encode_bf16_3d(&m.k, k, d, N, hk, bwd::kBc) ||
       !encode_bf16_3d(&m.v, v, d, N, hk, bwd::kBc) ||
       !encode_bf16_3d(&m.dO, dO, d, N, hq, bwd::kBr) ||
-      !encode_f32_3d(&m.dq, dq_accum, d, N, hq, 32) ||
+      !encode_f32_3d(&m.dq, dq_accum, d, N, hq, 32, d == 128 ? d : 32) ||
       !encode_bf16_3d(&m.dk, dk, d, N, hk, bwd::kBc) ||
       !encode_bf16_3d(&m.dv, dv, d, N, hk, bwd::kBc))
     return ATTN_ERR_LAUNCH;

@@ -85,20 +85,23 @@ inline bool encode_bf16_3d(CUtensorMap* map, const void* base, int d, int rows, 
 }
 
 // 3-D fp32 tensor map over [heads, rows, d] (innermost d), box
-// {d, box_rows, 1}, no swizzle; used for TMA reductions into dQaccum
-// (rows past the end of a head are clipped, never written).
+// {box_cols, box_rows, 1}; used for TMA reductions into dQaccum (rows past
+// the end of a head are clipped, never written). box_cols = d: no swizzle;
+// box_cols = 32 (128-byte rows): 128-byte swizzle.
 inline bool encode_f32_3d(CUtensorMap* map, const void* base, int d, int rows, long long heads,
-                          int box_rows) {
+                          int box_rows, int box_cols = 0) {
+  if (box_cols == 0) box_cols = d;
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
                         static_cast<cuuint64_t>(heads)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
                            static_cast<cuuint64_t>(d) * 4 * static_cast<cuuint64_t>(rows)};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
-                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   box_cols * 4 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
