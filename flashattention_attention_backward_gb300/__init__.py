@@ -16,6 +16,7 @@ from .build import LIB_PATH
 __all__ = [
     "AttnError", "check", "library", "attn_fwd_ref", "attn_bwd_preprocess", "attn_bwd",
     "attn_bwd_finalize", "attn_bwd_noalloc", "attn_device_status", "attn_strerror",
+    "attn_selftest_wait_timeout",
     "ATTN_OK", "ATTN_ERR_NULL", "ATTN_ERR_SHAPE", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_ALIGN",
     "ATTN_ERR_LAUNCH", "ATTN_ERR_DEVICE_TIMEOUT", "ATTN_ERR_DEVICE", "ATTN_ERR_TOO_LARGE",
 ]
@@ -40,6 +41,7 @@ _SIGNATURES = {
     "attn_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _F, _P, _P],
     "attn_bwd_finalize": [_P, _P, _F, _I, _I, _I, _I, _P],
     "attn_device_status": [ctypes.POINTER(ctypes.c_int), _I, _P],
+    "attn_selftest_wait_timeout": [ctypes.POINTER(ctypes.c_int), _P],
     "attn_bwd_noalloc": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _F, _P],
 }
 
@@ -126,6 +128,14 @@ def attn_device_status(clear=True, stream=None):
     """Returns (rc, status): the library's device status word."""
     v = ctypes.c_int(0)
     rc = library().attn_device_status(ctypes.byref(v), int(clear), _stream(stream))
+    return rc, v.value
+
+
+def attn_selftest_wait_timeout(stream=None):
+    """Returns (rc, status) of the device-side bounded-wait self test; the
+    status is ATTN_ERR_DEVICE_TIMEOUT when waits give up as designed."""
+    v = ctypes.c_int(0)
+    rc = library().attn_selftest_wait_timeout(ctypes.byref(v), _stream(stream))
     return rc, v.value
 
 

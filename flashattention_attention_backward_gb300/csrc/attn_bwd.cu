@@ -170,8 +170,11 @@ __device__ __forceinline__ uint32_t bar_addr(const Ctx& c, int i) { return c.bar
 
 __device__ __noinline__ void record_status(int code) { atomicCAS(&g_status, 0, code); }
 
-// Bounded wait; returns false if the kernel is aborting.
-__device__ __forceinline__ bool wait(const Ctx& c, int bar, uint32_t parity) {
+// Bounded wait; returns false if the kernel is aborting (another role gave
+// up) or if this wait ran out (it then raises the abort flag and records
+// ATTN_ERR_DEVICE_TIMEOUT).
+__device__ __forceinline__ bool wait(const Ctx& c, int bar, uint32_t parity,
+                                     long long limit = kWaitLimitCycles) {
   const uint32_t a = bar_addr(c, bar);
   if (mbar_try_wait(a, parity)) return true;
   const long long t0 = clock64();
@@ -179,7 +182,7 @@ __device__ __forceinline__ bool wait(const Ctx& c, int bar, uint32_t parity) {
   while (!mbar_try_wait(a, parity)) {
     if ((++n & 63u) == 0) {
       if (*c.abort) return false;
-      if (clock64() - t0 > kWaitLimitCycles) {
+      if (clock64() - t0 > limit) {
         *c.abort = 1;
         record_status(ATTN_ERR_DEVICE_TIMEOUT);
         return false;
@@ -932,6 +935,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Exercises the bounded wait of the kernels above on the device: warp 0
+// waits on an mbarrier that nothing arrives on, gives up after
+// `limit_cycles`, raises the abort flag and records ATTN_ERR_DEVICE_TIMEOUT;
+// warp 1, waiting on another such barrier with a far longer limit, returns
+// on the abort flag. Nothing faults or traps; the context stays usable.
+__global__ void __launch_bounds__(64, 1) wait_timeout_probe(long long limit_cycles) {
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ int abort_flag;
+  Ctx c;
+  c.bars = smem_u32(bars);
+  c.abort = &abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(c.bars, 1);
+    mbar_init(c.bars + 8, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x < 32)
+    (void)wait(c, 0, 0, limit_cycles);
+  else
+    (void)wait(c, 1, 0, 64 * limit_cycles);
+  __syncthreads();
+}
+
 // Tensor maps of one call: loads of Q, K, V, dO; reductions into dq_accum;
 // stores of dK, dV.
 struct Maps {
@@ -1030,6 +1058,19 @@ extern "C" int attn_device_status(int* status, int clear, void* stream) {
       return ATTN_ERR_LAUNCH;
   }
   return ATTN_OK;
+}
+
+extern "C" int attn_selftest_wait_timeout(int* status, void* stream) {
+  if (!status) return ATTN_ERR_NULL;
+  cudaStream_t s = as_stream(stream);
+  const int zero = 0;
+  if (cudaMemcpyToSymbolAsync(bwd::g_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s) !=
+      cudaSuccess)
+    return ATTN_ERR_LAUNCH;
+  bwd::wait_timeout_probe<<<1, 64, 0, s>>>(1000000LL);  // about half a millisecond
+  const int rc = launch_status();
+  if (rc != ATTN_OK) return rc;
+  return attn_device_status(status, 1, stream);
 }
 
 extern "C" const char* attn_strerror(int code) {

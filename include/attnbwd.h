@@ -142,6 +142,19 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
  */
 int attn_device_status(int* status, int clear, void* stream);
 
+/*
+ * attn_selftest_wait_timeout: runs, on `stream`, a one-block kernel that
+ * takes the bounded mbarrier wait the backward kernels use on a barrier that
+ * nothing arrives on, with a limit of about half a millisecond instead of
+ * the kernels' one second. The wait gives up, raises the block's abort flag
+ * (a second warp waiting on another barrier returns on it) and records
+ * ATTN_ERR_DEVICE_TIMEOUT. The device status word is cleared first; on
+ * return *status holds what the kernel recorded (ATTN_ERR_DEVICE_TIMEOUT
+ * when the mechanism works) and the word is cleared again. Nothing faults
+ * or traps, so the context stays usable. Returns ATTN_OK or a launch error.
+ */
+int attn_selftest_wait_timeout(int* status, void* stream);
+
 /* Static description of an error code; never NULL. */
 const char* attn_strerror(int code);
 
