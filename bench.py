@@ -227,37 +227,72 @@ def run_ours(args, w):
     flops = w.flops()
     value = world * flops * args.steps / (ms_total * 1e-3) / 1e12
 
-    # end to end: pinned host inputs -> device, backward, results -> host
+    # end to end: pinned host inputs -> device, backward, results -> host,
+    # every step. Steps are streamed as a user would: two device copies of
+    # the inputs and outputs, so that the host->device copy of step i+1 and
+    # the device->host copy of step i-1 run on their own streams while step i
+    # computes. Events order each buffer's reuse.
     pin = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
-    h_o, h_lse = o.cpu().pin_memory(), lse.cpu().pin_memory()
+    pin["o"], pin["lse"] = o.cpu().pin_memory(), lse.cpu().pin_memory()
     h_out = {n: torch.empty_like(t, device="cpu").pin_memory()
              for n, t in (("dq", bufs.dq), ("dk", bufs.dk), ("dv", bufs.dv))}
-    h2d = sum(t.numel() * t.element_size() for t in list(pin.values()) + [h_o, h_lse])
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
-    e2e_steps = max(3, min(args.steps, 20))
+    e2e_steps = max(4, min(args.steps, 20))
+    dins = [{"q": q, "k": k, "v": v, "do": do, "o": o, "lse": lse},
+            {n: torch.empty_like(t) for n, t in (("q", q), ("k", k), ("v", v), ("do", do),
+                                                   ("o", o), ("lse", lse))}]
+    dbufs = [bufs, runner.BackwardBuffers(q, k)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def e2e_step():
-        q.copy_(pin["q"], non_blocking=True)
-        k.copy_(pin["k"], non_blocking=True)
-        v.copy_(pin["v"], non_blocking=True)
-        do.copy_(pin["do"], non_blocking=True)
-        o.copy_(h_o, non_blocking=True)
-        lse.copy_(h_lse, non_blocking=True)
-        step()
-        h_out["dq"].copy_(bufs.dq, non_blocking=True)
-        h_out["dk"].copy_(bufs.dk, non_blocking=True)
-        h_out["dv"].copy_(bufs.dv, non_blocking=True)
+    def run_e2e(n_steps):
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        in_ready, computed, out_done = {}, {}, {}
+        for i in range(n_steps):
+            j = i & 1
+            a = dins[j]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(computed[i - 2])  # step i-2 has read these inputs
+                for n in pin:
+                    a[n].copy_(pin[n], non_blocking=True)
+                in_ready[i] = ev()
+                in_ready[i].record(s_in)
+            stream.wait_event(in_ready[i])
+            if i >= 2:
+                stream.wait_event(out_done[i - 2])  # step i-2's results are on the host
+            bb = dbufs[j]
+            attn.check(attn.attn_bwd_preprocess(a["o"], a["do"], bb.dpsum, bb.dq_accum, B, H, N, d,
+                                                stream))
+            attn.check(attn.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"],
+                                     bb.dq_accum, bb.dk, bb.dv, B, H, H_kv, N, d, w.scale,
+                                     w.causal, w.softcap, bb.dpsum, stream))
+            attn.check(attn.attn_bwd_finalize(bb.dq_accum, bb.dq, w.scale, B, H, N, d, stream))
+            computed[i] = ev()
+            computed[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(computed[i])
+                h_out["dq"].copy_(bb.dq, non_blocking=True)
+                h_out["dk"].copy_(bb.dk, non_blocking=True)
+                h_out["dv"].copy_(bb.dv, non_blocking=True)
+                out_done[i] = ev()
+                out_done[i].record(s_out)
 
-    e2e_step()
+    run_e2e(2)
     torch.cuda.synchronize(dev)
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_in)
+    s_in.wait_stream(stream)
+    run_e2e(e2e_steps)
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(stream)
+    e1.record(s_out)
     torch.cuda.synchronize(dev)
     barrier(world)
+    rc, status = attn.attn_device_status(clear=True, stream=stream)
+    if rc != 0 or status != 0:
+        raise RuntimeError("device status %d after the end-to-end steps" % status)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / e2e_steps
     e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
 
@@ -296,12 +331,14 @@ def run_ours(args, w):
         "clocks": clock_info,
         "gpu_launches": 3 * args.steps,
         "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "streaming": "two device buffer sets; step i+1's host->device copy and step "
+                             "i-1's device->host copy overlap step i's kernels"},
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     if world == 1 and not args.no_all_configs:
-        del q, k, v, do, o, lse, bufs, pin, h_o, h_lse, h_out
+        del q, k, v, do, o, lse, bufs, pin, h_out, dins, dbufs
         torch.cuda.empty_cache()
         line["all_configs"] = all_configs(dev, peaks["bf16_tflops"])
     return line
