@@ -1,12 +1,13 @@
 // attn_bwd: attention backward on sm_103a, N-outer / Q-inner, recompute-P.
 //
 // Method ("反向传播算法详解" §2-§6; "解析 FlashAttention（3）" §3-§4):
-// one CTA owns a block of Bc = 128 keys of one KV head (block coordinate
-// (n_block, kv_head, batch), "反向传播算法详解" §3.3). It loads K_j, V_j once
-// (§4.5) and keeps the fp32 accumulators dK_j, dV_j in tensor memory while it
-// walks every query block i (Br = 128 rows) of every query head of the KV
-// head's group. Per (i, j) tile it runs the five GEMMs of §5.2 on the
-// tcgen05 tensor cores and the elementwise softmax backward in registers:
+// the unit of work is a block of Bc = 128 keys of one KV head (block
+// coordinate (n_block, kv_head, batch), "反向传播算法详解" §3.3). Its CTA
+// loads K_j, V_j once (§4.5) and keeps the fp32 accumulators dK_j, dV_j in
+// tensor memory while it walks every query block i (Br = 128 rows) of every
+// query head of the KV head's group. Per (i, j) tile it runs the five GEMMs
+// of §5.2 on the tcgen05 tensor cores and the elementwise softmax backward in
+// registers:
 //
 //   S^T  = K_j Q_i^T                (M = keys, N = queries, K = d)
 //   dP^T = V_j dO_i^T
@@ -14,31 +15,36 @@
 //   dS   = P o (dP - D)              [softcap: o (1 - tanh^2)]
 //   dV_j += P^T dO_i                 (P^T taken from tensor memory)
 //   dK_j += dS^T Q_i                 (dS^T from shared memory)
-//   dQ_i += dS K_j                   (dS from shared memory; fp32 atomics)
+//   dQ_i += dS K_j                   (dS from shared memory; fp32 TMA
+//                                     reductions into dq_accum)
 //
 // Because S^T is computed with keys on the tensor-memory lanes, P^T already
 // sits in the layout the dV GEMM wants as its A operand and never passes
 // through shared memory (the analogue of feeding P from registers to the dV
-// GEMM, "反向传播算法详解" §8.2). dK/dV are summed over
-// the GQA group on chip (§8.5 sums them in fp32 HBM buffers instead), so they
-// need no atomics; only dQ is accumulated globally (§3.2, §6).
+// GEMM, "反向传播算法详解" §8.2). dK/dV are summed over the GQA group on chip
+// (§8.5 sums them in fp32 HBM buffers instead), so they need no atomics;
+// only dQ is accumulated globally (§3.2, §6).
 //
-// Warp roles (640 threads, five warpgroups; registers rebalanced with
+// The kernel is persistent: one CTA per SM walks units in snake order, with
+// the next unit's K and V loaded as soon as the last GEMMs that read the
+// current ones are done.
+//
+// Warp roles (640 threads, five warpgroups; registers 80 / 128 / 72 after
 // setmaxnreg):
-//   warp 0       TMA producer: K, V once; Q_i (+LSE_i, D_i), dO_i per tile,
-//                two-stage rings (the two pipelines of §4.3)
-//   warp 1       tcgen05 MMA issuer (one thread), tensor-memory owner
+//   warp 0       TMA producer: per tile Q_i (+LSE_i, D_i) and dO_i into rings
+//                (the two pipelines of §4.3); per unit K_j, V_j
+//   warp 1       tcgen05 MMA issuer (the whole warp runs the loop, one
+//                elected lane issues), tensor-memory owner
 //   warps 4-11   softmax backward: two warpgroups, one per half of the
-//                query columns; thread = key row (tensor-memory lane);
-//                afterwards the dK/dV epilogue
-//   warps 12-19  dQ drain: two warpgroups, each loads half of the dQ tile
-//                from tensor memory and frees it; for d = 128 it then stages
-//                the half in shared memory and adds it into dq_accum with
-//                TMA reductions, for d = 64 with fp32 vector atomics
+//                query columns; thread = key row (tensor-memory lane)
+//   warps 12-19  dQ drain: two warpgroups, each loads its share of the dQ
+//                tile from tensor memory and frees it, then stages it in
+//                shared memory and adds it into dq_accum with TMA tensor
+//                reductions; after a unit's last tile, its dK/dV epilogue
 //
 // MMA issue order per tile: dP_t, dV_t, S_{t+1}, dQ_t, dK_t. The P phase of
 // tile t+1 overlaps dQ_t/dK_t, dK_t overlaps the dQ drain, and only
-// dP -> dS -> dQ -> drain forms the per-tile dependency chain. The dQ atomic
+// dP -> dS -> dQ -> drain forms the per-tile dependency chain. The dQ
 // reduction (bounded by the L2 reduction rate, about 6 TB/s on GB300)
 // overlaps the next tile instead of stalling it.
 //
