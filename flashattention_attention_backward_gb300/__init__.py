@@ -14,7 +14,7 @@ import os
 from .build import LIB_PATH
 
 __all__ = [
-    "AttnError", "check", "library", "attn_fwd_ref", "attn_bwd_preprocess", "attn_bwd",
+    "AttnError", "check", "library", "attn_fwd", "attn_fwd_ref", "attn_bwd_preprocess", "attn_bwd",
     "attn_bwd_finalize", "attn_bwd_noalloc", "attn_device_status", "attn_strerror",
     "attn_selftest_wait_timeout",
     "ATTN_OK", "ATTN_ERR_NULL", "ATTN_ERR_SHAPE", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_ALIGN",
@@ -37,6 +37,7 @@ _F = ctypes.c_float
 
 _SIGNATURES = {
     "attn_fwd_ref": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _F, _P],
+    "attn_fwd": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _F, _P],
     "attn_bwd_preprocess": [_P, _P, _P, _P, _I, _I, _I, _I, _P],
     "attn_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _F, _P, _P],
     "attn_bwd_finalize": [_P, _P, _F, _I, _I, _I, _I, _P],
@@ -98,6 +99,11 @@ def check(rc):
 def attn_fwd_ref(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap, stream=None):
     return library().attn_fwd_ref(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, H_kv, N,
                                   d, scale, int(causal), softcap, _stream(stream))
+
+
+def attn_fwd(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap, stream=None):
+    return library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, H_kv, N, d,
+                              scale, int(causal), softcap, _stream(stream))
 
 
 def attn_bwd_preprocess(o, dO, dpsum, dq_accum, B, H, N, d, stream=None):

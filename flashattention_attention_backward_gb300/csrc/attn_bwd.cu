@@ -1057,12 +1057,14 @@ extern "C" int attn_device_status(int* status, int clear, void* stream) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_LAUNCH;
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, bwd::g_status, sizeof(int)) != cudaSuccess) return ATTN_ERR_LAUNCH;
-  *status = v;
   if (clear) {
     const int zero = 0;
     if (cudaMemcpyToSymbol(bwd::g_status, &zero, sizeof(int)) != cudaSuccess)
       return ATTN_ERR_LAUNCH;
   }
+  int vf = 0;  // the forward kernels keep their own word
+  if (fwd_status(&vf, clear != 0) != ATTN_OK) return ATTN_ERR_LAUNCH;
+  *status = v != 0 ? v : vf;
   return ATTN_OK;
 }
 

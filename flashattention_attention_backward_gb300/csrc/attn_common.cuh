@@ -106,4 +106,8 @@ inline bool encode_f32_3d(CUtensorMap* map, const void* base, int d, int rows, l
   return r == CUDA_SUCCESS;
 }
 
+// Device status word of the forward kernels (attn_fwd.cu): *status := its
+// value, cleared when `clear`. Returns ATTN_OK or ATTN_ERR_LAUNCH.
+int fwd_status(int* status, bool clear);
+
 }  // namespace attn

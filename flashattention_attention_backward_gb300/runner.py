@@ -4,7 +4,8 @@ finalize. No arithmetic happens here; torch provides memory and streams.
 """
 import torch
 
-from . import (attn_bwd, attn_bwd_finalize, attn_bwd_preprocess, attn_fwd_ref, check)
+from . import (attn_bwd, attn_bwd_finalize, attn_bwd_preprocess, attn_fwd, attn_fwd_ref,
+               check)
 
 
 def _dims(q, k):
@@ -17,13 +18,14 @@ def _stream(stream):
     return stream if stream is not None else torch.cuda.current_stream()
 
 
-def forward(q, k, v, scale, causal, softcap=0.0, stream=None):
-    """O [B,H,N,d] bf16 and LSE [B,H,N] fp32 from attn_fwd_ref."""
+def forward(q, k, v, scale, causal, softcap=0.0, stream=None, impl="tc"):
+    """O [B,H,N,d] bf16 and LSE [B,H,N] fp32: attn_fwd (tensor cores, impl
+    "tc") or attn_fwd_ref (plain fp32, impl "ref")."""
     B, H, H_kv, N, d = _dims(q, k)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    check(attn_fwd_ref(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap,
-                       _stream(stream)))
+    fn = {"tc": attn_fwd, "ref": attn_fwd_ref}[impl]
+    check(fn(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap, _stream(stream)))
     return o, lse
 
 

@@ -22,7 +22,7 @@
  *    [B, H, N, d]; K, V, dK, dV are [B, H_kv, N, d]; LSE and D are [B, H, N].
  *    bf16 tensors are passed as `void*` (IEEE bfloat16 bit patterns).
  *  * Query head h uses KV head h / (H / H_kv) (H must be a multiple of H_kv).
- *  * d must be 64 or 128 for attn_fwd_ref and attn_bwd; preprocess and
+ *  * d must be 64 or 128 for attn_fwd, attn_fwd_ref and attn_bwd; preprocess and
  *    finalize accept any d that is a multiple of 4.
  *  * Every pointer must be 16-byte aligned (the kernels use TMA and 16-byte
  *    vector accesses).
@@ -71,6 +71,17 @@ extern "C" {
  */
 int attn_fwd_ref(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int H_kv, int N, int d, float scale, int causal, float softcap, void* stream);
+
+/*
+ * attn_fwd: the same forward as attn_fwd_ref (same arguments, outputs and
+ * layouts) on the tcgen05 tensor cores: one CTA per 128 queries of a query
+ * head walks the visible key blocks twice, first for the exact row statistics
+ * (LSE), then for O = P V with P = exp(S - LSE) already normalised
+ * ([bwd-detail] §1.2; [FA-v1-bwd] §1.1 forward). S and O accumulate in fp32;
+ * P enters the PV GEMM as bf16. d must be 64 or 128.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int H_kv, int N, int d, float scale, int causal, float softcap, void* stream);
 
 /*
  * attn_bwd_preprocess: D = rowsum(dO o O) ([FA-v1-bwd] §2.4 eq. 6;

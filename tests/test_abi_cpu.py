@@ -30,7 +30,7 @@ def _declared():
 
 def test_header_declares_entry_points():
     names = _declared()
-    for want in ("attn_fwd_ref", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_finalize",
+    for want in ("attn_fwd", "attn_fwd_ref", "attn_bwd_preprocess", "attn_bwd", "attn_bwd_finalize",
                  "attn_device_status", "attn_strerror"):
         assert want in names
 
@@ -80,6 +80,12 @@ def test_bwd_argument_validation(lib):
 
 def test_other_entry_points_validation(lib):
     a = FAKE
+    for fwd in (lib.attn_fwd_ref, lib.attn_fwd):
+        assert fwd(0, a, a, a, a, 1, 1, 1, 64, 64, 0.1, 0, 0.0) == lib.ATTN_ERR_NULL
+        assert fwd(a, a, a, a, a, 1, 1, 1, 64, 80, 0.1, 0, 0.0) == lib.ATTN_ERR_UNSUPPORTED
+        assert fwd(a, a, a, a, a, 1, 4, 3, 64, 64, 0.1, 0, 0.0) == lib.ATTN_ERR_SHAPE
+        assert fwd(a, a, a, a + 4, a, 1, 1, 1, 64, 64, 0.1, 0, 0.0) == lib.ATTN_ERR_ALIGN
+        assert fwd(a, a, a, a, a, 1, 0, 1, 64, 64, 0.1, 0, 0.0) == lib.ATTN_OK
     assert lib.attn_fwd_ref(0, a, a, a, a, 1, 1, 1, 64, 64, 0.1, 0, 0.0) == lib.ATTN_ERR_NULL
     assert lib.attn_fwd_ref(a, a, a, a, a, 1, 1, 1, 64, 80, 0.1, 0, 0.0) == lib.ATTN_ERR_UNSUPPORTED
     assert lib.attn_fwd_ref(a, a, a, a, a, 1, 4, 3, 64, 64, 0.1, 0, 0.0) == lib.ATTN_ERR_SHAPE
