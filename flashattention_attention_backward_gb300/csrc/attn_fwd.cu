@@ -19,11 +19,12 @@
 // and P (bf16 pairs, keys along the columns) is the A operand of the PV GEMM
 // straight from tensor memory.
 //
-// Warp roles (256 threads):
-//   warp 0     TMA producer: Q once, K_j for every S GEMM, V_j in pass 2
-//              (two-stage rings)
-//   warp 1     tcgen05 MMA issuer (whole warp, one elected lane issues)
-//   warps 4-7  softmax and epilogue (O -> bf16 -> shared -> TMA store; LSE)
+// Warp roles (384 threads):
+//   warp 0      TMA producer: Q once, K_j for every S GEMM, V_j in pass 2
+//               (two-stage rings)
+//   warp 1      tcgen05 MMA issuer (whole warp, one elected lane issues)
+//   warps 4-11  softmax in two warpgroups, one per S buffer, then the
+//               epilogue (O -> bf16 -> shared -> TMA store; LSE)
 //
 // Tensor memory (512 columns): S buffers at [0,128) and [128,256) (P
 // overwrites the first half of its buffer), O accumulator at [256, 256 + d).
@@ -41,7 +42,7 @@ using namespace ptx;
 
 constexpr int kBm = 128;  // queries per CTA (tensor-memory lanes)
 constexpr int kBn = 128;  // keys per tile
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr long long kWaitLimitCycles = 2000000000LL;  // about one second
@@ -54,7 +55,8 @@ struct Layout {
   static constexpr int kK1 = kK0 + kTileBytes;
   static constexpr int kV0 = kK1 + kTileBytes;
   static constexpr int kV1 = kV0 + kTileBytes;
-  static constexpr int kBars = kV1 + kTileBytes;
+  static constexpr int kStats = kV1 + kTileBytes;  // 2 x 128 rows x (m, l) fp32
+  static constexpr int kBars = kStats + 2 * 128 * 8;
   static constexpr int kNumBars = 16;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
@@ -72,7 +74,7 @@ enum Bar {
   BAR_V_EMPTY = 7,   // + stage
   BAR_S_FULL = 9,    // + buffer
   BAR_S_FREE = 11,   // + buffer: the softmax (pass 1) or the PV GEMM (pass 2) is done with it
-  BAR_P_FULL = 13,   // + buffer
+  BAR_P_FULL = 13,   // + buffer (pass 2 only)
   BAR_O_DONE = 15,
 };
 
@@ -200,6 +202,12 @@ __device__ void producer_role(const Ctx& c, const Work& w, uint32_t sbase, const
   }
 }
 
+// P_FULL + w keeps one phase per pass-2 tile of buffer w.
+__device__ __forceinline__ uint32_t p_phase(int s, int nk) {
+  const int first = ((nk & 1) == (s & 1)) ? nk : nk + 1;  // first pass-2 tile of this buffer
+  return static_cast<uint32_t>(((s - first) >> 1) & 1);
+}
+
 // ------------------------------------------------------------------ MMA issuer
 // S GEMM s (s < nk: pass 1, else pass 2 over the same key blocks) goes to
 // buffer s & 1 once the previous use of that buffer has been released; in
@@ -239,7 +247,7 @@ __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t t
     if (s + 1 < total && !(ok = issue_s(s + 1))) break;
     if (s >= w.nk) {
       const int j = s - w.nk, b = s & 1, vs = j & 1;
-      if (!(ok = wait_warp(c, BAR_P_FULL + (j & 1), (j >> 1) & 1))) break;
+      if (!(ok = wait_warp(c, BAR_P_FULL + b, p_phase(s, w.nk)))) break;
       if (!(ok = wait_warp(c, BAR_V_FULL + vs, (j >> 1) & 1))) break;
       tc_fence_after();
       if (leader) {
@@ -261,38 +269,47 @@ __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t t
 }
 
 // ------------------------------------------------------------------ softmax
+// Two warpgroups; warpgroup w takes the S GEMMs s with s & 1 == w, i.e. S
+// buffer w, so each processes one tile while the other's S GEMM runs.
 // Thread = query row r (tensor-memory lane). Pass 1 keeps the running
-// maximum m and sum l of 2^x over the row, x = logit * log2e; pass 2 writes
+// maximum m and sum l of 2^x over the row (x = logit * log2e) for the
+// warpgroup's key blocks; the two partial statistics are combined through
+// shared memory into LSE2 at the pass boundary. Pass 2 writes
 // P = 2^(x - LSE2) as bf16 pairs over the first half of the S buffer, which
-// the PV GEMM reads as its A operand. Then the epilogue.
+// the PV GEMM reads as its A operand. Then each warpgroup stores half of the
+// columns of O.
 template <int D, bool CAUSAL, bool SOFTCAP>
-__device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint32_t sbase,
-                             uint32_t tmem, const CUtensorMap* to) {
+__device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8_t* smem,
+                             uint32_t sbase, uint32_t tmem, const CUtensorMap* to) {
   using L = Layout<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int wg = (warp - 4) >> 2;  // 0 or 1: the S buffer this warpgroup owns
   const int r = ((warp & 3) << 5) + lane;
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
   const int q = w.m_block * kBm + r;
+  const int bar_wg = 1 + wg;  // named barrier of this warpgroup (128 threads)
   const float c_log2 = p.scale * kLog2e;
   const float cap_in = SOFTCAP ? 2.f * kLog2e * p.scale / p.softcap : 0.f;  // 2 log2e tau/c
   const float cap_out = SOFTCAP ? p.softcap * kLog2e : 0.f;                 // c log2e
   float m = -INFINITY, l = 0.f, lse2 = 0.f;
   bool ok = true;
-  for (int s = 0; s < 2 * w.nk; ++s) {
+  const uint32_t tS = tmem + lane_base + wg * 128;
+  // Both warpgroups pass the same sequence of named-barrier-3 operations on
+  // every path (the votes below), so an abort can never strand one of them.
+  auto tile = [&](int s) -> bool {
     const bool pass2 = s >= w.nk;
     const int j = pass2 ? s - w.nk : s;
-    const int b = s & 1;
-    // the four warps meet at named barrier 1 below: one decision for all
-    ok = named_bar_and(1, 128, wait(c, BAR_S_FULL + b, (s >> 1) & 1));
-    if (!ok) break;
+    // the warpgroup meets at its named barrier below: one decision for all
+    ok = named_bar_and(bar_wg, 128, wait(c, BAR_S_FULL + wg, (s >> 1) & 1));
+    if (!ok) return false;
     tc_fence_after();
     const bool masked = (CAUSAL && j == w.m_block) || (j + 1) * kBn > p.N;
 #pragma unroll
     for (int ch = 0; ch < kBn / 32; ++ch) {
       uint32_t raw[32];
-      tmem_ld32(tmem + lane_base + b * 128 + ch * 32, raw);
-      float cm = -INFINITY;
+      tmem_ld32(tS + ch * 32, raw);
+      float cm0 = -INFINITY, cm1 = -INFINITY;
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const float sv = __uint_as_float(raw[e]);
@@ -309,16 +326,19 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint3
           if (!(key < p.N && (!CAUSAL || key <= q))) x = -INFINITY;
         }
         raw[e] = __float_as_uint(x);
-        cm = fmaxf(cm, x);
+        if (e & 1)
+          cm1 = fmaxf(cm1, x);
+        else
+          cm0 = fmaxf(cm0, x);
       }
       if (!pass2) {
-        // every row sees at least one key in its first chunk (key 0), so
-        // m is finite from there on and no -inf - -inf arises
-        const float mn = fmaxf(m, cm);
-        float sum = 0.f;
+        // a row's first chunk always holds a visible key (key 0, or the
+        // diagonal), so m is finite from there on and -inf - -inf never arises
+        const float mn = fmaxf(m, fmaxf(cm0, cm1));
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int e = 0; e < 32; ++e) sum += ex2_approx(__uint_as_float(raw[e]) - mn);
-        l = l * ex2_approx(m - mn) + sum;
+        for (int e = 0; e < 32; ++e) s4[e & 3] += ex2_approx(__uint_as_float(raw[e]) - mn);
+        l = l * ex2_approx(m - mn) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
         m = mn;
       } else {
         uint32_t packed[16];
@@ -328,51 +348,69 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint3
                                   ex2_approx(__uint_as_float(raw[2 * u + 1]) - lse2));
         // keys 32 ch .. 32 ch + 31 -> columns 16 ch .. 16 ch + 15, whose S
         // values were read in this or an earlier chunk
-        tmem_st16(tmem + lane_base + b * 128 + ch * 16, packed);
+        tmem_st16(tS + ch * 16, packed);
       }
     }
     if (!pass2) {
-      if (s == w.nk - 1) lse2 = m + __log2f(l);
       // the buffer is free for the next S GEMM once every row has read it
       tc_fence_before();
-      named_bar_sync(1, 128);
-      if (threadIdx.x == 128) mbar_arrive(bar_addr(c, BAR_S_FREE + b));
+      named_bar_sync(bar_wg, 128);
+      if (r == 0) mbar_arrive(bar_addr(c, BAR_S_FREE + wg));
     } else {
       tmem_wait_st();
       tc_fence_before();
-      named_bar_sync(1, 128);
-      if (threadIdx.x == 128) mbar_arrive(bar_addr(c, BAR_P_FULL + (j & 1)));
+      named_bar_sync(bar_wg, 128);
+      if (r == 0) mbar_arrive(bar_addr(c, BAR_P_FULL + wg));
     }
+    return true;
+  };
+  // pass 1 over this warpgroup's key blocks
+  for (int s = wg; ok && s < w.nk; s += 2) ok = tile(s);
+  // combine the two warpgroups' row statistics (one without pass-1 tiles
+  // has m = -inf, l = 0)
+  ok = named_bar_and(3, 256, ok);
+  if (ok) {
+    float* st = reinterpret_cast<float*>(smem + L::kStats);
+    st[(wg * 128 + r) * 2] = m;
+    st[(wg * 128 + r) * 2 + 1] = l;
+    named_bar_sync(3, 256);
+    const float mo = st[((1 - wg) * 128 + r) * 2], lo = st[((1 - wg) * 128 + r) * 2 + 1];
+    const float mx = fmaxf(m, mo);
+    lse2 = mx + __log2f(l * ex2_approx(m - mx) + lo * ex2_approx(mo - mx));
   }
+  // pass 2
+  for (int s = ((w.nk & 1) == wg) ? w.nk : w.nk + 1; ok && s < 2 * w.nk; s += 2) ok = tile(s);
   // ---- epilogue: O (already normalised) -> bf16 rows in the Q buffer (free
-  // once every GEMM is done) -> TMA tensor store; LSE in natural log
+  // once every GEMM is done) -> TMA tensor store; LSE in natural log.
+  // Warpgroup wg takes columns [wg * D/2, (wg + 1) * D/2) of every row.
   if (ok) ok = wait(c, BAR_O_DONE, 0);
-  if (!named_bar_and(1, 128, ok)) return;
+  if (!named_bar_and(3, 256, ok)) return;  // both warpgroups reach this vote on every path
   tc_fence_after();
 #pragma unroll
-  for (int c16 = 0; c16 < D / 16; ++c16) {
+  for (int c16 = 0; c16 < D / 32; ++c16) {
+    const int col = wg * (D / 2) + c16 * 16;
     uint32_t raw[16];
-    tmem_ld16(tmem + lane_base + 256 + c16 * 16, raw);
+    tmem_ld16(tmem + lane_base + 256 + col, raw);
     uint32_t packed[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u)
       packed[u] = pack_bf16x2(__uint_as_float(raw[2 * u]), __uint_as_float(raw[2 * u + 1]));
-    // columns 16 c16 .. : box c16 / 4, 16-byte chunks 2 (c16 % 4), + 1 of row r
-    const uint32_t row_addr = sbase + L::kQ + (c16 >> 2) * 16384 + r * 128;
-    const int c0 = (c16 & 3) * 2;
+    // columns col .. col + 15: box col / 64, 16-byte chunks (col % 64) / 8, + 1
+    const uint32_t row_addr = sbase + L::kQ + (col >> 6) * 16384 + r * 128;
+    const int c0 = (col & 63) >> 3;
     st_shared_v4(row_addr + ((c0 ^ (r & 7)) << 4), packed[0], packed[1], packed[2], packed[3]);
     st_shared_v4(row_addr + (((c0 + 1) ^ (r & 7)) << 4), packed[4], packed[5], packed[6],
                  packed[7]);
   }
   fence_proxy_async_smem();
-  named_bar_sync(1, 128);
-  if (threadIdx.x == 128) {
+  named_bar_sync(3, 256);
+  if (wg == 0 && r == 0) {
     for (int cb = 0; cb < D / 64; ++cb)
       tma_store_3d(to, sbase + L::kQ + cb * 16384, 64 * cb, w.m_block * kBm, w.bh);
     bulk_commit_group();
     bulk_wait_all();
   }
-  if (q < p.N) p.lse[static_cast<long long>(w.bh) * p.N + q] = lse2 * kLn2;
+  if (wg == 0 && q < p.N) p.lse[static_cast<long long>(w.bh) * p.N + q] = lse2 * kLn2;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -412,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     mma_role<D>(c, w, sbase, tmem);
   } else if (warp >= 4) {
-    softmax_role<D, CAUSAL, SOFTCAP>(c, p, w, sbase, tmem, &tm_o);
+    softmax_role<D, CAUSAL, SOFTCAP>(c, p, w, smem, sbase, tmem, &tm_o);
   }
   tc_fence_before();
   __syncthreads();
