@@ -346,7 +346,8 @@ def run_ours(args, w):
 
 def all_configs(dev, peak, iters=20, warmup=3):
     """attn_bwd alone on each named workload (CUDA events around each launch,
-    median of `iters`): ms, TFLOP/s and the fraction of the bf16 peak."""
+    median of `iters`): ms, TFLOP/s and the fraction of the bf16 peak; the
+    same for the tensor-core forward attn_fwd."""
     import flashattention_attention_backward_gb300 as attn
     from flashattention_attention_backward_gb300 import runner
     from flashattention_attention_backward_gb300.inputs import WORKLOADS, make_inputs
@@ -376,9 +377,24 @@ def all_configs(dev, peak, iters=20, warmup=3):
             raise RuntimeError("device status %d on %s" % (status, name))
         ms = sorted(a.elapsed_time(b) for a, b in times)[len(times) // 2]
         tf = w.flops() / (ms * 1e-3) / 1e12
+        # the tensor-core forward on the same inputs (2 GEMMs of 2 N^2 d per
+        # head, halved for causal)
+        fts = []
+        for i in range(warmup + iters):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            attn.check(attn.attn_fwd(q, k, v, o, lse, w.B, w.H, w.H_kv, w.N, w.d, w.scale,
+                                     w.causal, w.softcap, stream))
+            e1.record(stream)
+            if i >= warmup:
+                fts.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        fms = sorted(a.elapsed_time(b) for a, b in fts)[len(fts) // 2]
+        ftf = w.flops() * 2 / 5 / (fms * 1e-3) / 1e12
         out[name] = {"B": w.B, "H": w.H, "H_kv": w.H_kv, "N": w.N, "d": w.d,
                      "causal": w.causal, "softcap": w.softcap, "bwd_ms": ms,
-                     "tflops": tf, "frac_of_peak": tf / peak}
+                     "tflops": tf, "frac_of_peak": tf / peak,
+                     "fwd_ms": fms, "fwd_tflops": ftf, "fwd_frac_of_peak": ftf / peak}
         del x, q, k, v, do, o, lse, bufs
         torch.cuda.empty_cache()
     return out
