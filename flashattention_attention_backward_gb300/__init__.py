@@ -16,7 +16,8 @@ from .build import LIB_PATH
 __all__ = [
     "AttnError", "check", "library", "attn_fwd", "attn_fwd_ref", "attn_bwd_preprocess", "attn_bwd",
     "attn_bwd_finalize", "attn_bwd_noalloc", "attn_device_status", "attn_strerror",
-    "attn_selftest_wait_timeout",
+    "attn_selftest_wait_timeout", "attn_bwd_dq_partials_bytes", "attn_bwd_deterministic",
+    "attn_bwd_finalize_partials",
     "ATTN_OK", "ATTN_ERR_NULL", "ATTN_ERR_SHAPE", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_ALIGN",
     "ATTN_ERR_LAUNCH", "ATTN_ERR_DEVICE_TIMEOUT", "ATTN_ERR_DEVICE", "ATTN_ERR_TOO_LARGE",
 ]
@@ -43,6 +44,9 @@ _SIGNATURES = {
     "attn_bwd_finalize": [_P, _P, _F, _I, _I, _I, _I, _P],
     "attn_device_status": [ctypes.POINTER(ctypes.c_int), _I, _P],
     "attn_selftest_wait_timeout": [ctypes.POINTER(ctypes.c_int), _P],
+    "attn_bwd_deterministic": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _F,
+                               _P, _P],
+    "attn_bwd_finalize_partials": [_P, _P, _F, _I, _I, _I, _I, _I, _P],
     "attn_bwd_noalloc": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _F, _P],
 }
 
@@ -68,6 +72,8 @@ def library():
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = ctypes.c_int
+        lib.attn_bwd_dq_partials_bytes.argtypes = [_I, _I, _I, _I, _I]
+        lib.attn_bwd_dq_partials_bytes.restype = ctypes.c_longlong
         lib.attn_strerror.argtypes = [ctypes.c_int]
         lib.attn_strerror.restype = ctypes.c_char_p
         _lib = lib
@@ -128,6 +134,22 @@ def attn_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, B, H, H_kv, N, d, scale, c
     return library().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
                                       _ptr(dq), _ptr(dk), _ptr(dv), B, H, H_kv, N, d, scale,
                                       int(causal), softcap, _stream(stream))
+
+
+def attn_bwd_dq_partials_bytes(B, H, N, d, causal):
+    return library().attn_bwd_dq_partials_bytes(B, H, N, d, int(causal))
+
+
+def attn_bwd_deterministic(q, k, v, o, dO, lse, dq_partials, dk, dv, B, H, H_kv, N, d, scale,
+                           causal, softcap, dpsum, stream=None):
+    return library().attn_bwd_deterministic(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq_partials), _ptr(dk),
+        _ptr(dv), B, H, H_kv, N, d, scale, int(causal), softcap, _ptr(dpsum), _stream(stream))
+
+
+def attn_bwd_finalize_partials(dq_partials, dq, scale, B, H, N, d, causal, stream=None):
+    return library().attn_bwd_finalize_partials(_ptr(dq_partials), _ptr(dq), scale, B, H, N, d,
+                                                int(causal), _stream(stream))
 
 
 def attn_device_status(clear=True, stream=None):

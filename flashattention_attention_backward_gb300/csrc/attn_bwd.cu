@@ -132,6 +132,11 @@ struct Params {
   int B, H, H_kv, N;
   int n_blocks, m_blocks;
   int n_units;  // n_blocks * H_kv * B
+  // deterministic dQ (kernel template flag DET): tiles are stored into
+  // dq_accum viewed as partials [B*H*pairs, 128, d] (pair of query block m
+  // and key block n: causal m (m + 1) / 2 + n, else m * n_blocks + n)
+  // instead of being added
+  int pairs;    // pairs per query head
   float scale;
   float softcap;
 };
@@ -757,7 +762,7 @@ __device__ __forceinline__ bool dq_epilogue(const Ctx& c, const Params& p, int k
   return true;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool DET>
 __device__ void dq_role(const Ctx& c, const Params& p, uint8_t* smem, uint32_t sbase,
                         uint32_t tmem, const CUtensorMap* tm_dq, const CUtensorMap* tm_dk,
                         const CUtensorMap* tm_dv) {
@@ -829,9 +834,17 @@ __device__ void dq_role(const Ctx& c, const Params& p, uint8_t* smem, uint32_t s
           fence_proxy_async_smem();
           named_bar_sync(1 + part, 128);
           const int row = m0 + part * 64 + ch * 32;
-          if (leader && row < p.N) {
-            tma_reduce_add_3d(tm_dq, stage, 0, row, static_cast<int>(bh));
-            bulk_commit_group();
+          if (leader) {
+            if (DET) {
+              const int m = m0 >> 7, n = row0 >> 7;
+              const int pi = CAUSAL ? (m * (m + 1) >> 1) + n : m * p.n_blocks + n;
+              tma_store_3d(tm_dq, stage, 0, part * 64 + ch * 32,
+                           static_cast<int>(bh) * p.pairs + pi);
+              bulk_commit_group();
+            } else if (row < p.N) {
+              tma_reduce_add_3d(tm_dq, stage, 0, row, static_cast<int>(bh));
+              bulk_commit_group();
+            }
           }
         }
       } else {
@@ -854,7 +867,14 @@ __device__ void dq_role(const Ctx& c, const Params& p, uint8_t* smem, uint32_t s
         __syncwarp();
         if (lane == 0) {
           const int row = m0 + 32 * (warp & 3);
-          if (row < p.N) tma_reduce_add_3d(tm_dq, buf, 32 * part, row, static_cast<int>(bh));
+          if (DET) {
+            const int m = m0 >> 7, n = row0 >> 7;
+            const int pi = CAUSAL ? (m * (m + 1) >> 1) + n : m * p.n_blocks + n;
+            tma_store_3d(tm_dq, buf, 32 * part, 32 * (warp & 3),
+                         static_cast<int>(bh) * p.pairs + pi);
+          } else if (row < p.N) {
+            tma_reduce_add_3d(tm_dq, buf, 32 * part, row, static_cast<int>(bh));
+          }
           bulk_commit_group();  // one group per tile, empty or not
         }
       }
@@ -866,7 +886,7 @@ __device__ void dq_role(const Ctx& c, const Params& p, uint8_t* smem, uint32_t s
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool CAUSAL, bool SOFTCAP>
+template <int D, bool CAUSAL, bool SOFTCAP, bool DET>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -931,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     softmax_role<D, CAUSAL, SOFTCAP>(c, p, smem, sbase, tmem);
   } else {
     setmaxnreg_dec<kRegsDq>();
-    dq_role<D, CAUSAL>(c, p, smem, sbase, tmem, &tm_dq, &tm_dk, &tm_dv);
+    dq_role<D, CAUSAL, DET>(c, p, smem, sbase, tmem, &tm_dq, &tm_dk, &tm_dv);
   }
   tc_fence_before();
   __syncthreads();
@@ -972,9 +992,9 @@ struct Maps {
   CUtensorMap q, k, v, dO, dq, dk, dv;
 };
 
-template <int D, bool CAUSAL, bool SOFTCAP>
+template <int D, bool CAUSAL, bool SOFTCAP, bool DET>
 int launch(const Maps& m, const Params& p, cudaStream_t stream) {
-  auto kern = attn_bwd_kernel<D, CAUSAL, SOFTCAP>;
+  auto kern = attn_bwd_kernel<D, CAUSAL, SOFTCAP, DET>;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -995,60 +1015,92 @@ int launch(const Maps& m, const Params& p, cudaStream_t stream) {
 
 using namespace attn;
 
-extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                        const void* dO, const float* lse, float* dq_accum, void* dk, void* dv,
-                        int B, int H, int H_kv, int N, int d, float scale, int causal,
-                        float softcap, const float* dpsum, void* stream) {
-  (void)o;  // D = rowsum(dO o O) arrives precomputed in dpsum
-  if (!q || !k || !v || !dO || !lse || !dq_accum || !dk || !dv || !dpsum) return ATTN_ERR_NULL;
+namespace attn {
+namespace bwd {
+
+template <bool DET>
+int dispatch(const Maps& m, const Params& p, cudaStream_t s, int d, bool cs, bool cap) {
+  if (d == 128) {
+    if (cs)
+      return cap ? launch<128, true, true, DET>(m, p, s) : launch<128, true, false, DET>(m, p, s);
+    return cap ? launch<128, false, true, DET>(m, p, s) : launch<128, false, false, DET>(m, p, s);
+  }
+  if (cs) return cap ? launch<64, true, true, DET>(m, p, s) : launch<64, true, false, DET>(m, p, s);
+  return cap ? launch<64, false, true, DET>(m, p, s) : launch<64, false, false, DET>(m, p, s);
+}
+
+// Shared by attn_bwd (dQ added into dq_target) and attn_bwd_deterministic
+// (dQ tiles stored into the partials buffer dq_target).
+int run(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+        float* dq_target, void* dk, void* dv, int B, int H, int H_kv, int N, int d, float scale,
+        int causal, float softcap, const float* dpsum, void* stream, bool det) {
+  if (!q || !k || !v || !dO || !lse || !dq_target || !dk || !dv || !dpsum) return ATTN_ERR_NULL;
   int rc = check_shape(B, H, H_kv, N, d);
   if (rc != ATTN_OK) return rc;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || scale == 0.f || std::isnan(softcap)) return ATTN_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
-      !aligned16(dq_accum) || !aligned16(dk) || !aligned16(dv) || !aligned16(dpsum))
+      !aligned16(dq_target) || !aligned16(dk) || !aligned16(dv) || !aligned16(dpsum))
     return ATTN_ERR_ALIGN;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
 
-  bwd::Maps m;
-  const long long hq = static_cast<long long>(B) * H, hk = static_cast<long long>(B) * H_kv;
-  if (!encode_bf16_3d(&m.q, q, d, N, hq, bwd::kBr) ||
-      !encode_bf16_3d(&m.k, k, d, N, hk, bwd::kBc) ||
-      !encode_bf16_3d(&m.v, v, d, N, hk, bwd::kBc) ||
-      !encode_bf16_3d(&m.dO, dO, d, N, hq, bwd::kBr) ||
-      !encode_f32_3d(&m.dq, dq_accum, d, N, hq, 32, d == 128 ? d : 32) ||
-      !encode_bf16_3d(&m.dk, dk, d, N, hk, bwd::kBc) ||
-      !encode_bf16_3d(&m.dv, dv, d, N, hk, bwd::kBc))
-    return ATTN_ERR_LAUNCH;
-
-  bwd::Params p;
+  Params p;
   p.lse = lse;
   p.dpsum = dpsum;
-  p.dq_accum = dq_accum;
+  p.dq_accum = dq_target;
   p.B = B;
   p.H = H;
   p.H_kv = H_kv;
   p.N = N;
-  p.n_blocks = (N + bwd::kBc - 1) / bwd::kBc;
-  p.m_blocks = (N + bwd::kBr - 1) / bwd::kBr;
+  p.n_blocks = (N + kBc - 1) / kBc;
+  p.m_blocks = (N + kBr - 1) / kBr;
   const long long units = static_cast<long long>(p.n_blocks) * H_kv * B;
   if (units > 0x7fffffffLL) return ATTN_ERR_TOO_LARGE;
   p.n_units = static_cast<int>(units);
+  const long long pairs = causal ? static_cast<long long>(p.m_blocks) * (p.m_blocks + 1) / 2
+                                 : static_cast<long long>(p.m_blocks) * p.n_blocks;
+  if (det && static_cast<long long>(B) * H * pairs > 0x7fffffffLL) return ATTN_ERR_TOO_LARGE;
+  p.pairs = static_cast<int>(pairs);
   p.scale = scale;
   const bool cap = softcap > 0.f;
   p.softcap = cap ? softcap : 0.f;
+
+  Maps m;
+  const long long hq = static_cast<long long>(B) * H, hk = static_cast<long long>(B) * H_kv;
+  const bool dq_ok =
+      det ? encode_f32_3d(&m.dq, dq_target, d, kBr, hq * pairs, 32, d == 128 ? d : 32)
+          : encode_f32_3d(&m.dq, dq_target, d, N, hq, 32, d == 128 ? d : 32);
+  if (!encode_bf16_3d(&m.q, q, d, N, hq, kBr) || !encode_bf16_3d(&m.k, k, d, N, hk, kBc) ||
+      !encode_bf16_3d(&m.v, v, d, N, hk, kBc) || !encode_bf16_3d(&m.dO, dO, d, N, hq, kBr) ||
+      !dq_ok || !encode_bf16_3d(&m.dk, dk, d, N, hk, kBc) ||
+      !encode_bf16_3d(&m.dv, dv, d, N, hk, kBc))
+    return ATTN_ERR_LAUNCH;
+
   cudaStream_t s = as_stream(stream);
   const bool cs = causal != 0;
-  if (d == 128) {
-    if (cs) return cap ? bwd::launch<128, true, true>(m, p, s)
-                       : bwd::launch<128, true, false>(m, p, s);
-    return cap ? bwd::launch<128, false, true>(m, p, s)
-               : bwd::launch<128, false, false>(m, p, s);
-  }
-  if (cs) return cap ? bwd::launch<64, true, true>(m, p, s)
-                     : bwd::launch<64, true, false>(m, p, s);
-  return cap ? bwd::launch<64, false, true>(m, p, s)
-             : bwd::launch<64, false, false>(m, p, s);
+  return det ? dispatch<true>(m, p, s, d, cs, cap) : dispatch<false>(m, p, s, d, cs, cap);
+}
+
+}  // namespace bwd
+}  // namespace attn
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                        const void* dO, const float* lse, float* dq_accum, void* dk, void* dv,
+                        int B, int H, int H_kv, int N, int d, float scale, int causal,
+                        float softcap, const float* dpsum, void* stream) {
+  (void)o;  // D = rowsum(dO o O) arrives precomputed in dpsum
+  return bwd::run(q, k, v, dO, lse, dq_accum, dk, dv, B, H, H_kv, N, d, scale, causal, softcap,
+                  dpsum, stream, false);
+}
+
+extern "C" int attn_bwd_deterministic(const void* q, const void* k, const void* v,
+                                      const void* o, const void* dO, const float* lse,
+                                      float* dq_partials, void* dk, void* dv, int B, int H,
+                                      int H_kv, int N, int d, float scale, int causal,
+                                      float softcap, const float* dpsum, void* stream) {
+  (void)o;
+  return bwd::run(q, k, v, dO, lse, dq_partials, dk, dv, B, H, H_kv, N, d, scale, causal,
+                  softcap, dpsum, stream, true);
 }
 
 extern "C" int attn_device_status(int* status, int clear, void* stream) {

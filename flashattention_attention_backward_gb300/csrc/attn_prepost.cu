@@ -8,6 +8,10 @@
 //    and the matching fp32 dQ-accumulator row is cleared with 16-byte stores.
 //  * finalize: dq = bf16(tau * dq_accum) ("解析 FlashAttention（3）" eq. 7),
 //    16 bytes read / 8 bytes written per thread step.
+//  * finalize_partials (deterministic dQ): dq = bf16(tau * sum over key
+//    blocks n, in increasing n, of the stored partial tiles dS_mn K_n of
+//    query block m) ("反向传播算法详解" §6.4: a fixed order of the
+//    additions makes dQ reproducible bit for bit).
 // Both grids are a multiple of the SM count and grid-stride over the rows.
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -40,7 +44,7 @@ __global__ void __launch_bounds__(kThreads)
         acc = fmaf(__uint_as_float(wo[e] & 0xffff0000u), __uint_as_float(wd[e] & 0xffff0000u),
                    acc);
       }
-      *reinterpret_cast<float4*>(dq_accum + base + c) = zero;
+      if (dq_accum != nullptr) *reinterpret_cast<float4*>(dq_accum + base + c) = zero;
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -64,6 +68,53 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// Partial dQ tiles of the deterministic mode: per query head, one 128-row
+// tile per (query block m, key block n) pair the mask keeps, pair index
+// m (m + 1) / 2 + n (causal, n <= m) or m * n_blocks + n.
+__host__ __device__ inline long long pair_index(int m, int n, int n_blocks, bool causal) {
+  return causal ? static_cast<long long>(m) * (m + 1) / 2 + n
+                : static_cast<long long>(m) * n_blocks + n;
+}
+__host__ __device__ inline long long pairs_per_head(int blocks, bool causal) {
+  return causal ? static_cast<long long>(blocks) * (blocks + 1) / 2
+                : static_cast<long long>(blocks) * blocks;
+}
+
+// One thread per 4 consecutive dQ elements of a row: the partials of its
+// query block are added in increasing key-block order.
+__global__ void __launch_bounds__(kThreads)
+    finalize_partials_kernel(const float* __restrict__ part, __nv_bfloat16* __restrict__ dq,
+                             float scale, long long rows, int N, int d, int blocks, int causal) {
+  const long long n4 = rows * (d / 4);
+  const long long stride = static_cast<long long>(gridDim.x) * kThreads;
+  const long long P = pairs_per_head(blocks, causal != 0);
+  for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < n4;
+       i += stride) {
+    const long long row = i / (d / 4);
+    const int c4 = static_cast<int>(i - row * (d / 4));
+    const long long bh = row / N;
+    const int qrow = static_cast<int>(row - bh * N);
+    const int m = qrow >> 7, r = qrow & 127;
+    const int n_end = causal ? m + 1 : blocks;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int n = 0; n < n_end; ++n) {
+      const long long tile = bh * P + pair_index(m, n, blocks, causal != 0);
+      const float4 a =
+          __ldcs(reinterpret_cast<const float4*>(part + (tile * 128 + r) * d) + c4);
+      acc.x += a.x;
+      acc.y += a.y;
+      acc.z += a.z;
+      acc.w += a.w;
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * scale, acc.y * scale);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * scale, acc.w * scale);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    __stcs(reinterpret_cast<uint2*>(dq) + i, u);
+  }
+}
+
 inline unsigned grid_for(long long work_items, int items_per_block) {
   const long long want = (work_items + items_per_block - 1) / items_per_block;
   const int sms = sm_count();
@@ -78,11 +129,12 @@ using namespace attn;
 
 extern "C" int attn_bwd_preprocess(const void* o, const void* dO, float* dpsum, float* dq_accum,
                                    int B, int H, int N, int d, void* stream) {
-  if (!o || !dO || !dpsum || !dq_accum) return ATTN_ERR_NULL;
+  if (!o || !dO || !dpsum) return ATTN_ERR_NULL;  // dq_accum may be NULL: D only
   int rc = check_shape(B, H, H > 0 ? 1 : 0, N, d);
   if (rc != ATTN_OK) return rc;
   if (d % 4 != 0) return ATTN_ERR_UNSUPPORTED;
-  if (!aligned16(o) || !aligned16(dO) || !aligned16(dpsum) || !aligned16(dq_accum))
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(dpsum) ||
+      (dq_accum != nullptr && !aligned16(dq_accum)))
     return ATTN_ERR_ALIGN;
   const long long rows = static_cast<long long>(B) * H * N;
   if (rows == 0) return ATTN_OK;
@@ -106,5 +158,30 @@ extern "C" int attn_bwd_finalize(const float* dq_accum, void* dq, float scale, i
   const unsigned grid = prepost::grid_for(n4, prepost::kThreads);
   prepost::finalize_kernel<<<grid, prepost::kThreads, 0, as_stream(stream)>>>(
       dq_accum, static_cast<__nv_bfloat16*>(dq), scale, n4);
+  return launch_status();
+}
+
+extern "C" long long attn_bwd_dq_partials_bytes(int B, int H, int N, int d, int causal) {
+  int rc = check_shape(B, H, H > 0 ? 1 : 0, N, d);
+  if (rc != ATTN_OK) return rc;
+  const int blocks = (N + 127) / 128;
+  return static_cast<long long>(B) * H * prepost::pairs_per_head(blocks, causal != 0) * 128 * d *
+         static_cast<long long>(sizeof(float));
+}
+
+extern "C" int attn_bwd_finalize_partials(const float* dq_partials, void* dq, float scale, int B,
+                                          int H, int N, int d, int causal, void* stream) {
+  if (!dq_partials || !dq) return ATTN_ERR_NULL;
+  int rc = check_shape(B, H, H > 0 ? 1 : 0, N, d);
+  if (rc != ATTN_OK) return rc;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return ATTN_ERR_SHAPE;
+  if (!aligned16(dq_partials) || !aligned16(dq)) return ATTN_ERR_ALIGN;
+  const long long rows = static_cast<long long>(B) * H * N;
+  if (rows == 0) return ATTN_OK;
+  const unsigned grid = prepost::grid_for(rows * (d / 4), prepost::kThreads);
+  prepost::finalize_partials_kernel<<<grid, prepost::kThreads, 0, as_stream(stream)>>>(
+      dq_partials, static_cast<__nv_bfloat16*>(dq), scale, rows, N, d, (N + 127) / 128,
+      causal != 0 ? 1 : 0);
   return launch_status();
 }

@@ -4,8 +4,8 @@ finalize. No arithmetic happens here; torch provides memory and streams.
 """
 import torch
 
-from . import (attn_bwd, attn_bwd_finalize, attn_bwd_preprocess, attn_fwd, attn_fwd_ref,
-               check)
+from . import (attn_bwd, attn_bwd_deterministic, attn_bwd_dq_partials_bytes, attn_bwd_finalize,
+               attn_bwd_finalize_partials, attn_bwd_preprocess, attn_fwd, attn_fwd_ref, check)
 
 
 def _dims(q, k):
@@ -42,14 +42,28 @@ class BackwardBuffers:
         self.dpsum = torch.empty((B, H, N), dtype=torch.float32, device=dev)
 
 
-def backward(q, k, v, o, do, lse, scale, causal, softcap=0.0, stream=None, bufs=None):
-    """dQ, dK, dV (bf16) via preprocess -> attn_bwd -> finalize."""
+def backward(q, k, v, o, do, lse, scale, causal, softcap=0.0, stream=None, bufs=None,
+             deterministic=False):
+    """dQ, dK, dV (bf16) via preprocess -> attn_bwd -> finalize, or, with
+    deterministic=True, preprocess -> attn_bwd_deterministic ->
+    finalize_partials (dQ identical bit for bit from run to run)."""
     B, H, H_kv, N, d = _dims(q, k)
     s = _stream(stream)
     if bufs is None:
         bufs = BackwardBuffers(q, k)
-    check(attn_bwd_preprocess(o, do, bufs.dpsum, bufs.dq_accum, B, H, N, d, s))
-    check(attn_bwd(q, k, v, o, do, lse, bufs.dq_accum, bufs.dk, bufs.dv, B, H, H_kv, N, d,
-                   scale, causal, softcap, bufs.dpsum, s))
-    check(attn_bwd_finalize(bufs.dq_accum, bufs.dq, scale, B, H, N, d, s))
+    if not deterministic:
+        check(attn_bwd_preprocess(o, do, bufs.dpsum, bufs.dq_accum, B, H, N, d, s))
+        check(attn_bwd(q, k, v, o, do, lse, bufs.dq_accum, bufs.dk, bufs.dv, B, H, H_kv, N, d,
+                       scale, causal, softcap, bufs.dpsum, s))
+        check(attn_bwd_finalize(bufs.dq_accum, bufs.dq, scale, B, H, N, d, s))
+        return bufs.dq, bufs.dk, bufs.dv
+    nbytes = attn_bwd_dq_partials_bytes(B, H, N, d, causal)
+    if nbytes < 0:
+        check(int(nbytes))
+    if getattr(bufs, "dq_partials", None) is None or bufs.dq_partials.numel() * 4 < nbytes:
+        bufs.dq_partials = torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device=q.device)
+    check(attn_bwd_preprocess(o, do, bufs.dpsum, None, B, H, N, d, s))
+    check(attn_bwd_deterministic(q, k, v, o, do, lse, bufs.dq_partials, bufs.dk, bufs.dv, B, H,
+                                 H_kv, N, d, scale, causal, softcap, bufs.dpsum, s))
+    check(attn_bwd_finalize_partials(bufs.dq_partials, bufs.dq, scale, B, H, N, d, causal, s))
     return bufs.dq, bufs.dk, bufs.dv

@@ -88,7 +88,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  * [bwd-detail] §2.1(3), "dPsum", computed before the main kernel) and
  * dq_accum := 0.
  * In:  o, dO [B,H,N,d] bf16.
- * Out: dpsum [B,H,N] fp32 (overwritten); dq_accum [B,H,N,d] fp32 (zeroed).
+ * Out: dpsum [B,H,N] fp32 (overwritten); dq_accum [B,H,N,d] fp32 (zeroed;
+ *      may be NULL, then only D is computed).
  */
 int attn_bwd_preprocess(const void* o, const void* dO, float* dpsum, float* dq_accum, int B,
                         int H, int N, int d, void* stream);
@@ -115,6 +116,36 @@ int attn_bwd_preprocess(const void* o, const void* dO, float* dpsum, float* dq_a
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
              const float* lse, float* dq_accum, void* dk, void* dv, int B, int H, int H_kv, int N,
              int d, float scale, int causal, float softcap, const float* dpsum, void* stream);
+
+/*
+ * Deterministic dQ ([bwd-detail] §6.4: the fp32 atomics make dQ differ in the
+ * last bits between runs; a fixed order of the additions removes that).
+ *
+ * attn_bwd_dq_partials_bytes: size of the partials workspace, in bytes, or a
+ *   negative ATTN_ERR_* code: one fp32 tile of 128 rows x d per query head
+ *   and (query block m, key block n) pair the mask keeps,
+ *   B * H * P * 128 * d * 4 with P = M (M + 1) / 2 (causal) or M * M, and
+ *   M = ceil(N / 128).
+ * attn_bwd_deterministic: attn_bwd with the same arguments, except that each
+ *   dQ tile (without the factor tau) is STORED into dq_partials (laid out as
+ *   [B*H, P, 128, d], pair index m (m + 1) / 2 + n if causal, else m M + n)
+ *   instead of being added into an accumulator; nothing needs zeroing
+ *   (attn_bwd_preprocess may be called with dq_accum = NULL). dK, dV as in
+ *   attn_bwd (already reproducible).
+ * attn_bwd_finalize_partials: dq = bf16(scale * sum over n = 0, 1, ... of
+ *   the partial tiles of each query block), always in that order, so dQ is
+ *   identical bit for bit from run to run. `causal` must match the backward.
+ * Order on the stream: attn_bwd_preprocess, attn_bwd_deterministic,
+ * attn_bwd_finalize_partials. Costs one fp32 tile write and read per pair
+ * (2.2 GB each way for B=2, H=32, N=4096, d=128 causal).
+ */
+long long attn_bwd_dq_partials_bytes(int B, int H, int N, int d, int causal);
+int attn_bwd_deterministic(const void* q, const void* k, const void* v, const void* o,
+                           const void* dO, const float* lse, float* dq_partials, void* dk,
+                           void* dv, int B, int H, int H_kv, int N, int d, float scale,
+                           int causal, float softcap, const float* dpsum, void* stream);
+int attn_bwd_finalize_partials(const float* dq_partials, void* dq, float scale, int B, int H,
+                               int N, int d, int causal, void* stream);
 
 /*
  * attn_bwd_finalize: dq = bf16(scale * dq_accum) ([FA-v1-bwd] eq. 7: the

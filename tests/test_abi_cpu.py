@@ -24,7 +24,8 @@ def _declared():
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
         text = open(h).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, flags=re.M))
+        names |= set(re.findall(r"^\s*(?:const\s+)?(?:long\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text,
+                                flags=re.M))
     return sorted(names)
 
 
@@ -100,3 +101,18 @@ def test_other_entry_points_validation(lib):
     assert lib.attn_bwd_finalize(a, a, 0.1, 0, 1, 64, 64) == lib.ATTN_OK
     rc = lib.library().attn_device_status(None, 0, None)
     assert rc == lib.ATTN_ERR_NULL
+    # deterministic-dQ entry points
+    assert lib.attn_bwd_dq_partials_bytes(2, 32, 4096, 128, 1) == 2 * 32 * 528 * 128 * 128 * 4
+    assert lib.attn_bwd_dq_partials_bytes(1, 2, 256, 64, 0) == 1 * 2 * 4 * 128 * 64 * 4
+    assert lib.attn_bwd_dq_partials_bytes(1, 3, 256, 64, 0) == 3 * 4 * 128 * 64 * 4
+    assert lib.attn_bwd_dq_partials_bytes(-1, 2, 256, 64, 0) == lib.ATTN_ERR_SHAPE
+    assert lib.attn_bwd_finalize_partials(0, a, 0.1, 1, 1, 64, 64, 1) == lib.ATTN_ERR_NULL
+    assert lib.attn_bwd_finalize_partials(a, a, 0.1, 1, 1, 64, 96, 1) == lib.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_bwd_finalize_partials(a, a, 0.1, 0, 1, 64, 64, 1) == lib.ATTN_OK
+    ok = (a, a, a, a, a, a, a, a, a)
+    assert lib.attn_bwd_deterministic(0, *ok[1:], 1, 2, 2, 128, 128, 0.1, 1, 0.0, a) == \
+        lib.ATTN_ERR_NULL
+    assert lib.attn_bwd_deterministic(*ok, 1, 2, 2, 128, 96, 0.1, 1, 0.0, a) == \
+        lib.ATTN_ERR_UNSUPPORTED
+    # preprocess may skip the accumulator
+    assert lib.attn_bwd_preprocess(a, a, a, None, 1, 1, 0, 64) == lib.ATTN_OK

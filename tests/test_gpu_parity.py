@@ -79,3 +79,37 @@ def test_dk_dv_bitwise_repeatable():
     _, b = run_gpu(w, x)
     assert torch.equal(a["dk"], b["dk"]) and torch.equal(a["dv"], b["dv"])
     assert torch.allclose(a["dq"].float(), b["dq"].float(), rtol=1e-2, atol=1e-3)
+
+
+DET = [
+    _w("det_gqa_d128_causal", 1, 8, 2, 300, 128, True),
+    _w("det_d64_softcap", 2, 4, 4, 257, 64, False, softcap=5.0, sigma_qkv=2.0),
+    _w("det_many_units_d128", 16, 8, 4, 300, 128, True),
+]
+
+
+@pytest.mark.parametrize("w", DET, ids=lambda w: w.name)
+def test_deterministic_dq(w):
+    """Deterministic mode: parity with the oracle, dQ identical bit for bit
+    across runs, dK/dV identical to the default path."""
+    from flashattention_attention_backward_gb300 import runner
+    from flashattention_attention_backward_gb300.inputs import make_inputs
+    x = make_inputs(w)
+    dev = torch.device("cuda:0")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = runner.forward(q, k, v, w.scale, w.causal, w.softcap)
+    outs = []
+    for _ in range(2):
+        dq, dk, dv = runner.backward(q, k, v, o, do, lse, w.scale, w.causal, w.softcap,
+                                     deterministic=True)
+        outs.append((dq.clone(), dk.clone(), dv.clone()))
+    dq_d, dk_d, dv_d = runner.backward(q, k, v, o, do, lse, w.scale, w.causal, w.softcap)
+    torch.cuda.synchronize()
+    import flashattention_attention_backward_gb300 as attn
+    rc, status = attn.attn_device_status(clear=True)
+    assert rc == 0 and status == 0
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], dk_d) and torch.equal(outs[0][2], dv_d)
+    assert torch.allclose(outs[0][0].float(), dq_d.float(), rtol=1e-2, atol=1e-3)
+    compare_full(w, x, {"o": o.cpu(), "lse": lse.cpu(), "dq": outs[0][0].cpu(),
+                        "dk": outs[0][1].cpu(), "dv": outs[0][2].cpu()})
