@@ -10,6 +10,9 @@ Sources (web pages, cited by title and section):
     backward derivation), §1.1, §2.2-2.7 (eq. 1-8), §3.2 (eq. 9).
   * "反向传播算法详解" (Inference Cookbook, backward pass in detail),
     §1.2-1.3, §2.1 (1)-(5) including the softcap derivative, §8.5 (GQA).
+  * Dropout: "解析 FlashAttention（3）" §3.3 and Algorithm 4 of §4; the keep
+    mask comes from Philox4x32-10 (Salmon et al., SC 2011), written out in
+    ``oracle/philox.py`` from its published definition.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` (hand-derived
 N=2, d=2 example, finite differences against an independent scalar forward,
@@ -21,3 +24,4 @@ from .attention import (  # noqa: F401
     head_forward,
     head_backward,
 )
+from .philox import dropout_keep_mask, keep_threshold, philox4x32_10  # noqa: F401

@@ -24,6 +24,12 @@ materialised chain written out once, in the pages' order:
       dQ  = tau * dZ K                  (eq. 7)
       dK  = tau * dZ^T Q                (eq. 8)
 
+Dropout ("解析 FlashAttention（3）" §3.3, Algorithm 4 of §4), optional: with a
+keep mask Z (from oracle.philox, drop probability p),
+      P~  = P o Z / (1 - p)             O = P~ V; LSE is that of P
+      dV  = P~^T dO                     dP = (dO V^T) o Z / (1 - p)
+and the rest as above; D = rowsum(dO o O) still equals rowsum(P o dP).
+
 Grouped KV heads ("反向传播算法详解" §8.5): query head h reads KV head
 floor(h / G) with G = H / H_kv, and dK, dV of a KV head are the sums over the
 G query heads of its group.
@@ -35,17 +41,19 @@ no blocking or reordering beyond the definitions above.
 """
 import numpy as np
 
+from .philox import dropout_keep_mask
+
 
 def _f64(x):
     return np.asarray(x, dtype=np.float64)
 
 
-def head_forward(q, k, v, scale, causal=False, softcap=0.0):
+def head_forward(q, k, v, scale, causal=False, softcap=0.0, keep=None, p_drop=0.0):
     """Forward pass of one query head against its KV head.
 
     q: [Nq, d], k, v: [Nk, d] (Nq == Nk when causal). Returns a dict with
     Z (tau Q K^T), T (tanh(Z/c) or None), S (masked logits), LSE, P and O,
-    all float64.
+    all float64. With a boolean keep mask [Nq, Nk], O = (P o keep / (1 - p)) V.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     Z = scale * (q @ k.T)
@@ -68,11 +76,12 @@ def head_forward(q, k, v, scale, causal=False, softcap=0.0):
         LSE = np.where(finite, m_safe + np.log(ell), -np.inf)
     lse_safe = np.where(finite, LSE, 0.0)
     P = np.where(finite[:, None], np.exp(S - lse_safe[:, None]), 0.0)
-    O = P @ v
-    return {"Z": Z, "T": T, "S": S, "LSE": LSE, "P": P, "O": O}
+    Pd = P if keep is None else np.where(keep, P / (1.0 - p_drop), 0.0)
+    O = Pd @ v
+    return {"Z": Z, "T": T, "S": S, "LSE": LSE, "P": P, "Pd": Pd, "O": O}
 
 
-def head_backward(q, k, v, do, scale, causal=False, softcap=0.0, o=None):
+def head_backward(q, k, v, do, scale, causal=False, softcap=0.0, o=None, keep=None, p_drop=0.0):
     """Backward pass of one query head (materialised P, dP, dS).
 
     Returns a dict with dQ [Nq, d], dK and dV [Nk, d] (this head's share,
@@ -80,12 +89,14 @@ def head_backward(q, k, v, do, scale, causal=False, softcap=0.0, o=None):
     O and LSE. If ``o`` is given, D is formed from that O instead of the
     oracle's own (used to separate forward error from backward error).
     """
-    fw = head_forward(q, k, v, scale, causal, softcap)
+    fw = head_forward(q, k, v, scale, causal, softcap, keep, p_drop)
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     P = fw["P"]
     O = fw["O"] if o is None else _f64(o)
-    dV = P.T @ do                                   # eq. 1
+    dV = fw["Pd"].T @ do                            # eq. 1 (dropped P)
     dP = do @ v.T                                   # eq. 2
+    if keep is not None:
+        dP = np.where(keep, dP / (1.0 - p_drop), 0.0)  # through the dropout
     D = (do * O).sum(axis=1)                        # eq. 6
     dS = P * (dP - D[:, None])                      # eq. 5
     if softcap > 0.0:
@@ -106,8 +117,17 @@ def _check_shapes(Q, K):
     return B, H, H_kv, N, Nk, d
 
 
-def attention_forward(Q, K, V, scale, causal=False, softcap=0.0):
-    """O [B,H,N,d] and natural-log LSE [B,H,N] for the whole batch."""
+def _keep(dropout, b, h, H, nq, nk):
+    """Keep mask of head (b, h) for dropout = (p_drop, seed), or None."""
+    if dropout is None or dropout[0] <= 0.0:
+        return None, 0.0
+    p_drop, seed = dropout
+    return dropout_keep_mask(seed, b * H + h, nq, nk, p_drop), float(p_drop)
+
+
+def attention_forward(Q, K, V, scale, causal=False, softcap=0.0, dropout=None):
+    """O [B,H,N,d] and natural-log LSE [B,H,N] for the whole batch.
+    dropout = (p_drop, seed) applies the Philox keep mask of oracle.philox."""
     B, H, H_kv, N, Nk, d = _check_shapes(Q, K)
     G = H // H_kv
     O = np.empty((B, H, N, d), dtype=np.float64)
@@ -115,21 +135,23 @@ def attention_forward(Q, K, V, scale, causal=False, softcap=0.0):
     for b in range(B):
         for h in range(H):
             g = h // G
-            fw = head_forward(Q[b, h], K[b, g], V[b, g], scale, causal, softcap)
+            keep, pd = _keep(dropout, b, h, H, N, Nk)
+            fw = head_forward(Q[b, h], K[b, g], V[b, g], scale, causal, softcap, keep, pd)
             O[b, h] = fw["O"]
             LSE[b, h] = fw["LSE"]
     return O, LSE
 
 
 def attention_backward(Q, K, V, dO, scale, causal=False, softcap=0.0,
-                       slices=None, O=None):
+                       slices=None, O=None, dropout=None):
     """dQ, dK, dV for the batch, or for selected (batch, kv_head) slices.
 
     With ``slices=None`` returns arrays dQ [B,H,N,d], dK, dV [B,H_kv,N,d].
     With ``slices=[(b, g), ...]`` returns a dict mapping (b, g) to a dict
     {"dQ": [G,N,d], "dK": [N,d], "dV": [N,d], "heads": [h...]} where dK and
     dV are summed over the G query heads of KV head g. ``O`` optionally
-    supplies the forward output used for D (same shape as Q).
+    supplies the forward output used for D (same shape as Q). dropout =
+    (p_drop, seed) applies the Philox keep mask of oracle.philox.
     """
     B, H, H_kv, N, Nk, d = _check_shapes(Q, K)
     G = H // H_kv
@@ -140,9 +162,10 @@ def attention_backward(Q, K, V, dO, scale, causal=False, softcap=0.0,
         dK = np.zeros((Nk, d), dtype=np.float64)
         dV = np.zeros((Nk, d), dtype=np.float64)
         for r, h in enumerate(heads):
+            keep, pd = _keep(dropout, b, h, H, N, Nk)
             res = head_backward(Q[b, h], K[b, g], V[b, g], dO[b, h], scale,
                                 causal, softcap,
-                                None if O is None else O[b, h])
+                                None if O is None else O[b, h], keep, pd)
             dQ[r] = res["dQ"]
             dK += res["dK"]                         # GQA group sum
             dV += res["dV"]

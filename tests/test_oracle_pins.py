@@ -89,8 +89,10 @@ def test_element_formulas_n2_d2():
 # --------------------------------------------------------------------------
 # independent brute-force scalar forward
 # --------------------------------------------------------------------------
-def brute_forward(Q, K, V, scale, causal, softcap):
-    """Pure-Python loops: O and LSE for [B,H,N,d] / [B,H_kv,N,d] nested lists."""
+def brute_forward(Q, K, V, scale, causal, softcap, keep=None, p_drop=0.0):
+    """Pure-Python loops: O and LSE for [B,H,N,d] / [B,H_kv,N,d] nested lists.
+    keep[b][h][i][j] (optional) drops P_ij where false and scales the rest by
+    1 / (1 - p_drop)."""
     B, H, N, d = len(Q), len(Q[0]), len(Q[0][0]), len(Q[0][0][0])
     H_kv = len(K[0])
     G = H // H_kv
@@ -117,6 +119,8 @@ def brute_forward(Q, K, V, scale, causal, softcap):
                 LSE[b][h][i] = lse
                 for j, x in logits:
                     pij = math.exp(x - lse)
+                    if keep is not None:
+                        pij = pij / (1.0 - p_drop) if keep[b][h][i][j] else 0.0
                     for c in range(d):
                         O[b][h][i][c] += pij * V[b][g][j][c]
     return O, LSE
@@ -340,3 +344,116 @@ def test_saturated_softcap_kills_gradient():
     do = np.ones((N, d))
     r = head_backward(q, k, v, do, 1.0, False, 1.0)
     assert np.abs(r["dZ"]).max() < 1e-60 or np.abs(r["dQ"]).max() < 1e-12
+
+
+# --------------------------------------------------------------------------
+# dropout: the Philox generator and the dropped forward/backward
+# --------------------------------------------------------------------------
+from oracle import dropout_keep_mask, keep_threshold, philox4x32_10  # noqa: E402
+
+# Known-answer vectors of Philox4x32-10 (counter, key -> output) published
+# with the Random123 library of Salmon et al.
+PHILOX_KAT = [
+    ((0, 0, 0, 0), (0, 0), (0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8)),
+    ((0xFFFFFFFF,) * 4, (0xFFFFFFFF, 0xFFFFFFFF), (0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD)),
+    ((0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344), (0xA4093822, 0x299F31D0),
+     (0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1)),
+]
+
+
+@pytest.mark.parametrize("ctr,key,out", PHILOX_KAT)
+def test_philox_known_answers(ctr, key, out):
+    got = philox4x32_10(*ctr, *key)
+    assert tuple(int(x) for x in got) == out
+
+
+def test_keep_mask_rate_and_layout():
+    p = 0.3
+    keep = dropout_keep_mask(12345, 3, 256, 256, p)
+    assert abs(keep.mean() - (1 - p)) < 0.01
+    # word i % 4 of the counter (i // 4, j, bh, 0)
+    w = philox4x32_10(5, 7, 3, 0, 12345, 0)
+    for i in range(20, 24):
+        assert keep[i, 7] == (int(w[i - 20]) >= keep_threshold(p))
+    assert dropout_keep_mask(1, 0, 8, 8, 0.0).all()
+
+
+DROP_CASES = [
+    # B, H, H_kv, N, d, causal, softcap, p_drop
+    (1, 1, 1, 5, 2, False, 0.0, 0.4),
+    (1, 2, 1, 5, 3, True, 0.0, 0.25),
+    (1, 2, 2, 4, 2, True, 2.0, 0.5),
+]
+
+
+def _drop_case(case, seed=9):
+    B, H, H_kv, N, d, causal, cap, p = case
+    rng = np.random.default_rng(seed)
+    Q, K, V = _rand(rng, (B, H, N, d)), _rand(rng, (B, H_kv, N, d)), _rand(rng, (B, H_kv, N, d))
+    dO = _rand(rng, (B, H, N, d))
+    keep = [[dropout_keep_mask(77, b * H + h, N, N, p).tolist() for h in range(H)]
+            for b in range(B)]
+    return Q, K, V, dO, 1.0 / math.sqrt(d), causal, cap, p, keep
+
+
+@pytest.mark.parametrize("case", DROP_CASES)
+def test_dropout_forward_matches_brute_force(case):
+    Q, K, V, dO, scale, causal, cap, p, keep = _drop_case(case)
+    O, LSE = attention_forward(Q, K, V, scale, causal, cap, dropout=(p, 77))
+    Ob, LSEb = brute_forward(Q.tolist(), K.tolist(), V.tolist(), scale, causal, cap, keep, p)
+    np.testing.assert_allclose(O, np.array(Ob), atol=1e-12, rtol=0)
+    np.testing.assert_allclose(LSE, np.array(LSEb), atol=1e-12, rtol=0)
+
+
+def _fd_dropout(Q, K, V, dO, scale, causal, cap, keep, p, h=1e-6):
+    def loss(Qx, Kx, Vx):
+        O, _ = brute_forward(Qx.tolist(), Kx.tolist(), Vx.tolist(), scale, causal, cap, keep, p)
+        return float((np.array(O) * dO).sum())
+
+    grads = []
+    for which in range(3):
+        base = [Q, K, V][which]
+        g = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            args_p = [Q.copy(), K.copy(), V.copy()]
+            args_m = [Q.copy(), K.copy(), V.copy()]
+            args_p[which][idx] += h
+            args_m[which][idx] -= h
+            g[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        grads.append(g)
+    return grads
+
+
+@pytest.mark.parametrize("case", DROP_CASES)
+def test_dropout_backward_matches_finite_differences(case):
+    Q, K, V, dO, scale, causal, cap, p, keep = _drop_case(case)
+    dQ, dK, dV = attention_backward(Q, K, V, dO, scale, causal, cap, dropout=(p, 77))
+    fQ, fK, fV = _fd_dropout(Q, K, V, dO, scale, causal, cap, keep, p)
+    assert _rel(dQ, fQ) < 1e-7
+    assert _rel(dK, fK) < 1e-7
+    assert _rel(dV, fV) < 1e-7
+
+
+def test_dropout_zero_is_plain_and_d_identity():
+    Q, K, V, dO, scale, causal, cap, p, keep = _drop_case(DROP_CASES[1])
+    a = attention_backward(Q, K, V, dO, scale, causal, cap)
+    b = attention_backward(Q, K, V, dO, scale, causal, cap, dropout=(0.0, 77))
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    # D = rowsum(dO o O) = rowsum(P o dP) with dP taken through the dropout
+    km = np.array(keep[0][1])
+    r = head_backward(Q[0, 1], K[0, 0], V[0, 0], dO[0, 1], scale, causal, cap, None, km, p)
+    np.testing.assert_allclose(r["D"], (r["P"] * r["dP"]).sum(axis=1), atol=1e-12)
+
+
+def test_dropout_missing_rescale_fails_fd():
+    """A backward that forgets the 1 / (1 - p) on dP is caught."""
+    Q, K, V, dO, scale, causal, cap, p, keep = _drop_case(DROP_CASES[0])
+    km = np.array(keep[0][0])
+    fw = head_forward(Q[0, 0], K[0, 0], V[0, 0], scale, causal, cap, km, p)
+    dP = np.where(km, dO[0, 0] @ V[0, 0].T, 0.0)  # mistake: no 1 / (1 - p)
+    D = (dO[0, 0] * fw["O"]).sum(axis=1)
+    dS = fw["P"] * (dP - D[:, None])
+    dQ = scale * dS @ K[0, 0]
+    fQ, _, _ = _fd_dropout(Q, K, V, dO, scale, causal, cap, keep, p)
+    assert _rel(dQ[None, None], fQ) > 1e-3
