@@ -106,6 +106,15 @@ inline bool encode_f32_3d(CUtensorMap* map, const void* base, int d, int rows, l
   return r == CUDA_SUCCESS;
 }
 
+// Dropout threshold and scale for drop probability p in (0, 1): a 32-bit
+// word keeps its element iff word >= round(p * 2^32).
+inline uint32_t dropout_threshold(float p) {
+  const double t = static_cast<double>(p) * 4294967296.0 + 0.5;  // round half up
+  if (t <= 0.0) return 0u;
+  if (t >= 4294967295.0) return 0xFFFFFFFFu;
+  return static_cast<uint32_t>(t);
+}
+
 // Device status word of the forward kernels (attn_fwd.cu): *status := its
 // value, cleared when `clear`. Returns ATTN_OK or ATTN_ERR_LAUNCH.
 int fwd_status(int* status, bool clear);

@@ -15,6 +15,8 @@ of query head bh is kept iff the 32-bit word (i mod 4) of
 Philox(counter = (floor(i / 4), j, bh, 0), key = (seed mod 2^32, seed >> 32))
 is >= round(p * 2^32); a kept element is scaled by 1 / (1 - p).
 """
+import math
+
 import numpy as np
 
 _M0 = np.uint64(0xD2511F53)
@@ -43,8 +45,11 @@ def philox4x32_10(c0, c1, c2, c3, k0, k1):
 
 
 def keep_threshold(p_drop):
-    """32-bit threshold: a word u keeps its element iff u >= threshold."""
-    return int(min(max(round(float(p_drop) * 4294967296.0), 0), 4294967295))
+    """32-bit threshold: a word u keeps its element iff u >= threshold, for
+    the float32 value of p_drop (what the library receives), rounded half
+    up."""
+    t = float(np.float32(p_drop)) * 4294967296.0
+    return int(min(max(math.floor(t + 0.5), 0), 4294967295))
 
 
 def dropout_keep_mask(seed, bh, n_q, n_k, p_drop):
