@@ -61,6 +61,7 @@
 #include <cuda_bf16.h>
 
 #include "attn_common.cuh"
+#include "philox.cuh"
 #include "sm103_ptx.cuh"
 
 namespace attn {
@@ -137,6 +138,7 @@ struct Params {
   // and key block n: causal m (m + 1) / 2 + n, else m * n_blocks + n)
   // instead of being added
   int pairs;    // pairs per query head
+  Dropout drop; // kernel template flag DROP: keep mask of philox.cuh
   float scale;
   float softcap;
 };
@@ -507,10 +509,15 @@ __device__ void mma_role(const Ctx& c, const Params& p, uint32_t sbase, uint32_t
 // ------------------------------------------------------------------ softmax
 // One tile, one half of its query columns. Thread = key row r (tensor-memory
 // lane r); columns [64*half, 64*half + 64).
-template <int D, bool SOFTCAP, bool CAUSAL, bool MASKED>
+// With dropout (DROP), P^T for dV is P o Z / (1 - p) and dP passes through the
+// same mask (dP o Z / (1 - p)) before dS = P o (dP - D); the keep bits of the
+// thread's 64 columns are drawn in the P phase (one Philox call per four
+// queries of its key) and kept in km[] for the dS phase.
+template <int D, bool SOFTCAP, bool CAUSAL, bool MASKED, bool DROP>
 __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint8_t* smem,
                                              uint32_t sbase, uint32_t tmem, int t, int half,
-                                             int r, int key, int m0, int dsbuf_parity) {
+                                             int r, int key, int m0, int dsbuf_parity,
+                                             uint32_t bh) {
   using L = Layout<D>;
   const int st = t & 1;
   const int lane = threadIdx.x & 31;
@@ -521,6 +528,7 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
   const float cap_in = SOFTCAP ? 2.f * kLog2e * p.scale / p.softcap : 0.f;  // 2 log2e tau/c
   const float cap_out = SOFTCAP ? p.softcap * kLog2e : 0.f;                 // c log2e
   float pk[64];  // P, or P (1 - tanh^2) with softcap, for this thread's 64 columns
+  uint32_t km[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};  // dropout keep bits of the 64 columns
 
   // ---- P = exp(S - LSE) -> bf16 P^T in tensor memory
   if (!wait(c, BAR_S_FULL, t & 1)) return false;
@@ -530,7 +538,7 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
   // leaves the registers for more of those chains in flight. P^T of a group
   // (bf16 pairs) lands in columns whose S values were read by this or an
   // earlier group.
-  constexpr int kPasses = SOFTCAP ? 2 : 1;
+  constexpr int kPasses = (SOFTCAP || DROP) ? 2 : 1;
   constexpr int kCols = 64 / kPasses;
 #pragma unroll
   for (int pass = 0; pass < kPasses; ++pass) {
@@ -545,6 +553,17 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
       const float4 l4 =
           *reinterpret_cast<const float4*>(s_lse + half * 64 + pass * kCols + 4 * j4);
       const float lse4[4] = {l4.x, l4.y, l4.z, l4.w};
+      uint32_t kb = 0xFu;
+      if (DROP) {
+        const int cc = pass * kCols + 4 * j4;  // first of the four columns
+        const PhiloxOut rr = philox4x32_10(
+            static_cast<uint32_t>((m0 + half * 64 + cc) >> 2), static_cast<uint32_t>(key), bh,
+            0u, p.drop.seed_lo, p.drop.seed_hi);
+        kb = 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) kb |= (rr.w[e] >= p.drop.threshold ? 1u : 0u) << e;
+        km[cc >> 5] = (km[cc >> 5] & ~(0xFu << (cc & 31))) | (kb << (cc & 31));
+      }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int j = 4 * j4 + e;
@@ -566,6 +585,7 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
           prob = ok ? prob : 0.f;
           keep = ok ? keep : 0.f;
         }
+        if (DROP) prob = (kb >> e) & 1u ? prob * p.drop.inv_keep : 0.f;
         raw[j] = __float_as_uint(prob);
         pk[pass * kCols + j] = keep;
       }
@@ -607,7 +627,9 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int j = 4 * j4 + e;
-        raw[j] = __float_as_uint(pk[hh * 32 + j] * (__uint_as_float(raw[j]) - dd[e]));
+        float dp = __uint_as_float(raw[j]);
+        if (DROP) dp = (km[hh] >> j) & 1u ? dp * p.drop.inv_keep : 0.f;
+        raw[j] = __float_as_uint(pk[hh * 32 + j] * (dp - dd[e]));
       }
     }
 #pragma unroll
@@ -633,7 +655,7 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
   return true;
 }
 
-template <int D, bool CAUSAL, bool SOFTCAP>
+template <int D, bool CAUSAL, bool SOFTCAP, bool DROP>
 __device__ void softmax_role(const Ctx& c, const Params& p, uint8_t* smem, uint32_t sbase,
                              uint32_t tmem) {
   const int warp = threadIdx.x >> 5;
@@ -657,12 +679,13 @@ __device__ void softmax_role(const Ctx& c, const Params& p, uint8_t* smem, uint3
       if (!(ok = wait(c, BAR_Q_FULL + (t & 1), (t >> 1) & 1))) break;
       const bool masked = (CAUSAL && m_block == w.n_block) || key_tail || (m0 + kBr > p.N);
       const int dsbuf = (tl == 0 && ur > 0) ? ((ur - 1) & 1) : -1;
+      const uint32_t bh = static_cast<uint32_t>(w.b * p.H + h);
       if (masked)
-        ok = softmax_tile<D, SOFTCAP, CAUSAL, true>(c, p, smem, sbase, tmem, t, half, r, key, m0,
-                                                    dsbuf);
+        ok = softmax_tile<D, SOFTCAP, CAUSAL, true, DROP>(c, p, smem, sbase, tmem, t, half, r,
+                                                          key, m0, dsbuf, bh);
       else
-        ok = softmax_tile<D, SOFTCAP, CAUSAL, false>(c, p, smem, sbase, tmem, t, half, r, key,
-                                                     m0, dsbuf);
+        ok = softmax_tile<D, SOFTCAP, CAUSAL, false, DROP>(c, p, smem, sbase, tmem, t, half, r,
+                                                           key, m0, dsbuf, bh);
     }
     tg += w.T;
   }
@@ -886,7 +909,7 @@ __device__ void dq_role(const Ctx& c, const Params& p, uint8_t* smem, uint32_t s
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool CAUSAL, bool SOFTCAP, bool DET>
+template <int D, bool CAUSAL, bool SOFTCAP, bool DET, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -948,7 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 12) {
     setmaxnreg_inc<kRegsSoftmax>();
-    softmax_role<D, CAUSAL, SOFTCAP>(c, p, smem, sbase, tmem);
+    softmax_role<D, CAUSAL, SOFTCAP, DROP>(c, p, smem, sbase, tmem);
   } else {
     setmaxnreg_dec<kRegsDq>();
     dq_role<D, CAUSAL, DET>(c, p, smem, sbase, tmem, &tm_dq, &tm_dk, &tm_dv);
@@ -992,9 +1015,9 @@ struct Maps {
   CUtensorMap q, k, v, dO, dq, dk, dv;
 };
 
-template <int D, bool CAUSAL, bool SOFTCAP, bool DET>
+template <int D, bool CAUSAL, bool SOFTCAP, bool DET, bool DROP>
 int launch(const Maps& m, const Params& p, cudaStream_t stream) {
-  auto kern = attn_bwd_kernel<D, CAUSAL, SOFTCAP, DET>;
+  auto kern = attn_bwd_kernel<D, CAUSAL, SOFTCAP, DET, DROP>;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1018,27 +1041,34 @@ using namespace attn;
 namespace attn {
 namespace bwd {
 
-template <bool DET>
+template <bool DET, bool DROP>
 int dispatch(const Maps& m, const Params& p, cudaStream_t s, int d, bool cs, bool cap) {
   if (d == 128) {
     if (cs)
-      return cap ? launch<128, true, true, DET>(m, p, s) : launch<128, true, false, DET>(m, p, s);
-    return cap ? launch<128, false, true, DET>(m, p, s) : launch<128, false, false, DET>(m, p, s);
+      return cap ? launch<128, true, true, DET, DROP>(m, p, s)
+                 : launch<128, true, false, DET, DROP>(m, p, s);
+    return cap ? launch<128, false, true, DET, DROP>(m, p, s)
+               : launch<128, false, false, DET, DROP>(m, p, s);
   }
-  if (cs) return cap ? launch<64, true, true, DET>(m, p, s) : launch<64, true, false, DET>(m, p, s);
-  return cap ? launch<64, false, true, DET>(m, p, s) : launch<64, false, false, DET>(m, p, s);
+  if (cs)
+    return cap ? launch<64, true, true, DET, DROP>(m, p, s)
+               : launch<64, true, false, DET, DROP>(m, p, s);
+  return cap ? launch<64, false, true, DET, DROP>(m, p, s)
+             : launch<64, false, false, DET, DROP>(m, p, s);
 }
 
 // Shared by attn_bwd (dQ added into dq_target) and attn_bwd_deterministic
 // (dQ tiles stored into the partials buffer dq_target).
 int run(const void* q, const void* k, const void* v, const void* dO, const float* lse,
         float* dq_target, void* dk, void* dv, int B, int H, int H_kv, int N, int d, float scale,
-        int causal, float softcap, const float* dpsum, void* stream, bool det) {
+        int causal, float softcap, const float* dpsum, void* stream, bool det, float p_drop = 0.f,
+        unsigned long long seed = 0) {
   if (!q || !k || !v || !dO || !lse || !dq_target || !dk || !dv || !dpsum) return ATTN_ERR_NULL;
   int rc = check_shape(B, H, H_kv, N, d);
   if (rc != ATTN_OK) return rc;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || scale == 0.f || std::isnan(softcap)) return ATTN_ERR_SHAPE;
+  if (!(p_drop >= 0.f && p_drop < 1.f)) return ATTN_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
       !aligned16(dq_target) || !aligned16(dk) || !aligned16(dv) || !aligned16(dpsum))
     return ATTN_ERR_ALIGN;
@@ -1064,6 +1094,11 @@ int run(const void* q, const void* k, const void* v, const void* dO, const float
   p.scale = scale;
   const bool cap = softcap > 0.f;
   p.softcap = cap ? softcap : 0.f;
+  const bool drop = p_drop > 0.f;
+  p.drop.seed_lo = static_cast<uint32_t>(seed);
+  p.drop.seed_hi = static_cast<uint32_t>(seed >> 32);
+  p.drop.threshold = dropout_threshold(p_drop);
+  p.drop.inv_keep = 1.f / (1.f - p_drop);
 
   Maps m;
   const long long hq = static_cast<long long>(B) * H, hk = static_cast<long long>(B) * H_kv;
@@ -1078,7 +1113,8 @@ int run(const void* q, const void* k, const void* v, const void* dO, const float
 
   cudaStream_t s = as_stream(stream);
   const bool cs = causal != 0;
-  return det ? dispatch<true>(m, p, s, d, cs, cap) : dispatch<false>(m, p, s, d, cs, cap);
+  if (drop) return dispatch<false, true>(m, p, s, d, cs, cap);  // not combined with det
+  return det ? dispatch<true, false>(m, p, s, d, cs, cap) : dispatch<false, false>(m, p, s, d, cs, cap);
 }
 
 }  // namespace bwd
@@ -1091,6 +1127,16 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   (void)o;  // D = rowsum(dO o O) arrives precomputed in dpsum
   return bwd::run(q, k, v, dO, lse, dq_accum, dk, dv, B, H, H_kv, N, d, scale, causal, softcap,
                   dpsum, stream, false);
+}
+
+extern "C" int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* o,
+                                const void* dO, const float* lse, float* dq_accum, void* dk,
+                                void* dv, int B, int H, int H_kv, int N, int d, float scale,
+                                int causal, float softcap, const float* dpsum, float p_drop,
+                                unsigned long long seed, void* stream) {
+  (void)o;
+  return bwd::run(q, k, v, dO, lse, dq_accum, dk, dv, B, H, H_kv, N, d, scale, causal, softcap,
+                  dpsum, stream, false, p_drop, seed);
 }
 
 extern "C" int attn_bwd_deterministic(const void* q, const void* k, const void* v,

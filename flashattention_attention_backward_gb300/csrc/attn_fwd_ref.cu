@@ -14,6 +14,7 @@
 #include <math_constants.h>
 
 #include "attn_common.cuh"
+#include "philox.cuh"
 
 namespace attn {
 namespace fwd {
@@ -43,6 +44,8 @@ struct Params {
   float scale;
   float softcap;  // <= 0: disabled
   int causal;
+  int dropout;    // 0: off; else the keep mask of philox.cuh scales P in O = P V
+  Dropout drop;
 };
 
 __device__ __forceinline__ void load8(const __nv_bfloat16* src, bool ok, float (&f)[8]) {
@@ -140,6 +143,21 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_ref_kernel(const Params p) 
         for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
 
+    // dropout keep bits: bit i of keep[j] for rows m0 + 4 ty + i, key
+    // n0 + 4 tx + j (one Philox call covers the four rows of a key)
+    uint32_t keep[4] = {0xFu, 0xFu, 0xFu, 0xFu};
+    if (p.dropout) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const PhiloxOut r = philox4x32_10(static_cast<uint32_t>((m0 + ty * 4) >> 2),
+                                          static_cast<uint32_t>(n0 + tx * 4 + j),
+                                          static_cast<uint32_t>(bh), 0u, p.drop.seed_lo,
+                                          p.drop.seed_hi);
+        keep[j] = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) keep[j] |= (r.w[i] >= p.drop.threshold ? 1u : 0u) << i;
+      }
+    }
     float alpha[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -164,7 +182,9 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_ref_kernel(const Params p) 
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float pv = expf(z[j] - shift);
-        sP[(ty * 4 + i) * kPStride + tx * 4 + j] = pv;
+        // the row sum (hence LSE) is that of P; O takes the dropped P
+        sP[(ty * 4 + i) * kPStride + tx * 4 + j] =
+            p.dropout ? ((keep[j] >> i) & 1u ? pv * p.drop.inv_keep : 0.f) : pv;
         rs += pv;
       }
 #pragma unroll
@@ -236,18 +256,22 @@ int launch(const Params& p, cudaStream_t s) {
 
 using namespace attn;
 
-extern "C" int attn_fwd_ref(const void* q, const void* k, const void* v, void* o, float* lse,
-                            int B, int H, int H_kv, int N, int d, float scale, int causal,
-                            float softcap, void* stream) {
+namespace attn {
+namespace fwd {
+
+int run(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv,
+        int N, int d, float scale, int causal, float softcap, float p_drop,
+        unsigned long long seed, void* stream) {
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
   int rc = check_shape(B, H, H_kv, N, d);
   if (rc != ATTN_OK) return rc;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || scale == 0.f || std::isnan(softcap)) return ATTN_ERR_SHAPE;
+  if (!(p_drop >= 0.f && p_drop < 1.f)) return ATTN_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_ALIGN;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
-  fwd::Params p;
+  Params p;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);
   p.v = static_cast<const __nv_bfloat16*>(v);
@@ -257,10 +281,32 @@ extern "C" int attn_fwd_ref(const void* q, const void* k, const void* v, void* o
   p.H = H;
   p.H_kv = H_kv;
   p.N = N;
-  p.q_blocks = (N + fwd::kBM - 1) / fwd::kBM;
+  p.q_blocks = (N + kBM - 1) / kBM;
   p.scale = scale;
   p.softcap = softcap > 0.f ? softcap : 0.f;
   p.causal = causal != 0;
+  p.dropout = p_drop > 0.f ? 1 : 0;
+  p.drop.seed_lo = static_cast<uint32_t>(seed);
+  p.drop.seed_hi = static_cast<uint32_t>(seed >> 32);
+  p.drop.threshold = dropout_threshold(p_drop);
+  p.drop.inv_keep = 1.f / (1.f - p_drop);
   cudaStream_t s = as_stream(stream);
-  return d == 128 ? fwd::launch<128>(p, s) : fwd::launch<64>(p, s);
+  return d == 128 ? launch<128>(p, s) : launch<64>(p, s);
+}
+
+}  // namespace fwd
+}  // namespace attn
+
+extern "C" int attn_fwd_ref(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int H, int H_kv, int N, int d, float scale, int causal,
+                            float softcap, void* stream) {
+  return fwd::run(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap, 0.f, 0ull, stream);
+}
+
+extern "C" int attn_fwd_ref_dropout(const void* q, const void* k, const void* v, void* o,
+                                    float* lse, int B, int H, int H_kv, int N, int d, float scale,
+                                    int causal, float softcap, float p_drop,
+                                    unsigned long long seed, void* stream) {
+  return fwd::run(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap, p_drop, seed,
+                  stream);
 }

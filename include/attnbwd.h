@@ -73,6 +73,30 @@ int attn_fwd_ref(const void* q, const void* k, const void* v, void* o, float* ls
                  int H_kv, int N, int d, float scale, int causal, float softcap, void* stream);
 
 /*
+ * Dropout ([FA-v1-bwd] §3.3 and Algorithm 4 of §4), drop probability
+ * p_drop in [0, 1) (0 = none) and a 64-bit seed. Element (query i, key j) of
+ * query head bh = b * H + h is kept iff word (i mod 4) of
+ * Philox4x32-10(counter = (floor(i / 4), j, bh, 0), key = (seed mod 2^32,
+ * seed >> 32)) is >= round(p_drop * 2^32) (Philox4x32-10: Salmon et al.,
+ * "Parallel random numbers: as easy as 1, 2, 3", SC 2011); kept elements of
+ * P are scaled by 1 / (1 - p_drop). LSE is that of P before dropout.
+ *
+ * attn_fwd_ref_dropout: attn_fwd_ref with dropout: O = (P o Z / (1 - p)) V.
+ * attn_bwd_dropout: attn_bwd for that forward (same mask from the same
+ *   seed): dV = (P o Z / (1 - p))^T dO, dP = (dO V^T) o Z / (1 - p),
+ *   dS = P o (dP - D) with D = rowsum(dO o O) of the dropped O. Run it with
+ *   attn_bwd_preprocess and attn_bwd_finalize as attn_bwd.
+ * Both return ATTN_ERR_SHAPE for p_drop outside [0, 1).
+ */
+int attn_fwd_ref_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int H_kv, int N, int d, float scale, int causal,
+                         float softcap, float p_drop, unsigned long long seed, void* stream);
+int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                     const float* lse, float* dq_accum, void* dk, void* dv, int B, int H,
+                     int H_kv, int N, int d, float scale, int causal, float softcap,
+                     const float* dpsum, float p_drop, unsigned long long seed, void* stream);
+
+/*
  * attn_fwd: the same forward as attn_fwd_ref (same arguments, outputs and
  * layouts) on the tcgen05 tensor cores: one CTA per 128 queries of a query
  * head walks the visible key blocks twice, first for the exact row statistics
