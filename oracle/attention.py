@@ -24,6 +24,10 @@ materialised chain written out once, in the pages' order:
       dQ  = tau * dZ K                  (eq. 7)
       dK  = tau * dZ^T Q                (eq. 8)
 
+Local window ("反向传播算法详解" §3.4, the local-attention masking), optional:
+window = (left, right) hides key j from query i unless i - left <= j <= i + right
+(a negative bound is unbounded); it combines with the causal mask.
+
 Dropout ("解析 FlashAttention（3）" §3.3, Algorithm 4 of §4), optional: with a
 keep mask Z (from oracle.philox, drop probability p),
       P~  = P o Z / (1 - p)             O = P~ V; LSE is that of P
@@ -48,7 +52,8 @@ def _f64(x):
     return np.asarray(x, dtype=np.float64)
 
 
-def head_forward(q, k, v, scale, causal=False, softcap=0.0, keep=None, p_drop=0.0):
+def head_forward(q, k, v, scale, causal=False, softcap=0.0, keep=None, p_drop=0.0,
+                 window=None):
     """Forward pass of one query head against its KV head.
 
     q: [Nq, d], k, v: [Nk, d] (Nq == Nk when causal). Returns a dict with
@@ -63,11 +68,17 @@ def head_forward(q, k, v, scale, causal=False, softcap=0.0, keep=None, p_drop=0.
     else:
         T = None
         S = Z.copy()
+    nq, nk = S.shape
+    i = np.arange(nq)[:, None]
+    j = np.arange(nk)[None, :]
     if causal:
-        nq, nk = S.shape
-        i = np.arange(nq)[:, None]
-        j = np.arange(nk)[None, :]
         S = np.where(j > i, -np.inf, S)
+    if window is not None:
+        left, right = window
+        if left >= 0:
+            S = np.where(j < i - left, -np.inf, S)
+        if right >= 0:
+            S = np.where(j > i + right, -np.inf, S)
     m = S.max(axis=1)
     finite = np.isfinite(m)
     m_safe = np.where(finite, m, 0.0)
@@ -81,7 +92,8 @@ def head_forward(q, k, v, scale, causal=False, softcap=0.0, keep=None, p_drop=0.
     return {"Z": Z, "T": T, "S": S, "LSE": LSE, "P": P, "Pd": Pd, "O": O}
 
 
-def head_backward(q, k, v, do, scale, causal=False, softcap=0.0, o=None, keep=None, p_drop=0.0):
+def head_backward(q, k, v, do, scale, causal=False, softcap=0.0, o=None, keep=None, p_drop=0.0,
+                  window=None):
     """Backward pass of one query head (materialised P, dP, dS).
 
     Returns a dict with dQ [Nq, d], dK and dV [Nk, d] (this head's share,
@@ -89,7 +101,7 @@ def head_backward(q, k, v, do, scale, causal=False, softcap=0.0, o=None, keep=No
     O and LSE. If ``o`` is given, D is formed from that O instead of the
     oracle's own (used to separate forward error from backward error).
     """
-    fw = head_forward(q, k, v, scale, causal, softcap, keep, p_drop)
+    fw = head_forward(q, k, v, scale, causal, softcap, keep, p_drop, window)
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     P = fw["P"]
     O = fw["O"] if o is None else _f64(o)
@@ -125,9 +137,10 @@ def _keep(dropout, b, h, H, nq, nk):
     return dropout_keep_mask(seed, b * H + h, nq, nk, p_drop), float(p_drop)
 
 
-def attention_forward(Q, K, V, scale, causal=False, softcap=0.0, dropout=None):
+def attention_forward(Q, K, V, scale, causal=False, softcap=0.0, dropout=None, window=None):
     """O [B,H,N,d] and natural-log LSE [B,H,N] for the whole batch.
-    dropout = (p_drop, seed) applies the Philox keep mask of oracle.philox."""
+    dropout = (p_drop, seed) applies the Philox keep mask of oracle.philox;
+    window = (left, right) the local-attention mask."""
     B, H, H_kv, N, Nk, d = _check_shapes(Q, K)
     G = H // H_kv
     O = np.empty((B, H, N, d), dtype=np.float64)
@@ -136,14 +149,15 @@ def attention_forward(Q, K, V, scale, causal=False, softcap=0.0, dropout=None):
         for h in range(H):
             g = h // G
             keep, pd = _keep(dropout, b, h, H, N, Nk)
-            fw = head_forward(Q[b, h], K[b, g], V[b, g], scale, causal, softcap, keep, pd)
+            fw = head_forward(Q[b, h], K[b, g], V[b, g], scale, causal, softcap, keep, pd,
+                              window)
             O[b, h] = fw["O"]
             LSE[b, h] = fw["LSE"]
     return O, LSE
 
 
 def attention_backward(Q, K, V, dO, scale, causal=False, softcap=0.0,
-                       slices=None, O=None, dropout=None):
+                       slices=None, O=None, dropout=None, window=None):
     """dQ, dK, dV for the batch, or for selected (batch, kv_head) slices.
 
     With ``slices=None`` returns arrays dQ [B,H,N,d], dK, dV [B,H_kv,N,d].
@@ -151,7 +165,8 @@ def attention_backward(Q, K, V, dO, scale, causal=False, softcap=0.0,
     {"dQ": [G,N,d], "dK": [N,d], "dV": [N,d], "heads": [h...]} where dK and
     dV are summed over the G query heads of KV head g. ``O`` optionally
     supplies the forward output used for D (same shape as Q). dropout =
-    (p_drop, seed) applies the Philox keep mask of oracle.philox.
+    (p_drop, seed) applies the Philox keep mask of oracle.philox; window =
+    (left, right) the local-attention mask.
     """
     B, H, H_kv, N, Nk, d = _check_shapes(Q, K)
     G = H // H_kv
@@ -165,7 +180,7 @@ def attention_backward(Q, K, V, dO, scale, causal=False, softcap=0.0,
             keep, pd = _keep(dropout, b, h, H, N, Nk)
             res = head_backward(Q[b, h], K[b, g], V[b, g], dO[b, h], scale,
                                 causal, softcap,
-                                None if O is None else O[b, h], keep, pd)
+                                None if O is None else O[b, h], keep, pd, window)
             dQ[r] = res["dQ"]
             dK += res["dK"]                         # GQA group sum
             dV += res["dV"]

@@ -89,7 +89,7 @@ def test_element_formulas_n2_d2():
 # --------------------------------------------------------------------------
 # independent brute-force scalar forward
 # --------------------------------------------------------------------------
-def brute_forward(Q, K, V, scale, causal, softcap, keep=None, p_drop=0.0):
+def brute_forward(Q, K, V, scale, causal, softcap, keep=None, p_drop=0.0, window=None):
     """Pure-Python loops: O and LSE for [B,H,N,d] / [B,H_kv,N,d] nested lists.
     keep[b][h][i][j] (optional) drops P_ij where false and scales the rest by
     1 / (1 - p_drop)."""
@@ -105,6 +105,9 @@ def brute_forward(Q, K, V, scale, causal, softcap, keep=None, p_drop=0.0):
                 logits = []
                 for j in range(N):
                     if causal and j > i:
+                        continue
+                    if window is not None and ((window[0] >= 0 and j < i - window[0]) or
+                                               (window[1] >= 0 and j > i + window[1])):
                         continue
                     raw = 0.0
                     for c in range(d):
@@ -457,3 +460,74 @@ def test_dropout_missing_rescale_fails_fd():
     dQ = scale * dS @ K[0, 0]
     fQ, _, _ = _fd_dropout(Q, K, V, dO, scale, causal, cap, keep, p)
     assert _rel(dQ[None, None], fQ) > 1e-3
+
+
+# --------------------------------------------------------------------------
+# local window
+# --------------------------------------------------------------------------
+WIN_CASES = [
+    # B, H, H_kv, N, d, causal, softcap, (left, right)
+    (1, 1, 1, 6, 2, False, 0.0, (1, 2)),
+    (1, 2, 1, 6, 3, True, 0.0, (2, -1)),
+    (1, 2, 2, 5, 2, False, 2.0, (0, 0)),
+    (1, 1, 1, 7, 2, False, 0.0, (-1, 1)),
+]
+
+
+def _win_case(case, seed=13):
+    B, H, H_kv, N, d, causal, cap, win = case
+    rng = np.random.default_rng(seed)
+    Q, K, V = _rand(rng, (B, H, N, d)), _rand(rng, (B, H_kv, N, d)), _rand(rng, (B, H_kv, N, d))
+    dO = _rand(rng, (B, H, N, d))
+    return Q, K, V, dO, 1.0 / math.sqrt(d), causal, cap, win
+
+
+@pytest.mark.parametrize("case", WIN_CASES)
+def test_window_forward_matches_brute_force(case):
+    Q, K, V, dO, scale, causal, cap, win = _win_case(case)
+    O, LSE = attention_forward(Q, K, V, scale, causal, cap, window=win)
+    Ob, LSEb = brute_forward(Q.tolist(), K.tolist(), V.tolist(), scale, causal, cap, window=win)
+    np.testing.assert_allclose(O, np.array(Ob), atol=1e-12, rtol=0)
+    np.testing.assert_allclose(LSE, np.array(LSEb), atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("case", WIN_CASES)
+def test_window_backward_matches_finite_differences(case):
+    Q, K, V, dO, scale, causal, cap, win = _win_case(case)
+    dQ, dK, dV = attention_backward(Q, K, V, dO, scale, causal, cap, window=win)
+
+    def loss(Qx, Kx, Vx):
+        O, _ = brute_forward(Qx.tolist(), Kx.tolist(), Vx.tolist(), scale, causal, cap,
+                             window=win)
+        return float((np.array(O) * dO).sum())
+
+    h = 1e-6
+    for which, got in enumerate((dQ, dK, dV)):
+        base = [Q, K, V][which]
+        g = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            ap = [Q.copy(), K.copy(), V.copy()]
+            am = [Q.copy(), K.copy(), V.copy()]
+            ap[which][idx] += h
+            am[which][idx] -= h
+            g[idx] = (loss(*ap) - loss(*am)) / (2 * h)
+        # relative to the gradient's size, or absolute where it vanishes
+        # (window (0, 0) leaves dQ = dK = 0 exactly)
+        assert np.abs(got - g).max() <= 1e-7 * max(np.abs(g).max(), 1.0)
+
+
+def test_window_special_cases():
+    Q, K, V, dO, scale, causal, cap, win = _win_case((1, 2, 1, 6, 2, False, 0.0, (0, 0)))
+    # an unbounded or wider-than-N window is no window; (-1, 0) is causal
+    plain = attention_backward(Q, K, V, dO, scale, False, 0.0)
+    for w in ((-1, -1), (10, 10), (6, 6)):
+        for x, y in zip(plain, attention_backward(Q, K, V, dO, scale, False, 0.0, window=w)):
+            np.testing.assert_array_equal(x, y)
+    causal_ = attention_backward(Q, K, V, dO, scale, True, 0.0)
+    for x, y in zip(causal_, attention_backward(Q, K, V, dO, scale, False, 0.0, window=(-1, 0))):
+        np.testing.assert_array_equal(x, y)
+    # window (0, 0): every query sees only its own key, P = 1, dS = 0
+    dQ, dK, dV = attention_backward(Q, K, V, dO, scale, False, 0.0, window=(0, 0))
+    np.testing.assert_allclose(dQ, 0.0, atol=1e-15)
+    np.testing.assert_allclose(dK, 0.0, atol=1e-15)
+    np.testing.assert_allclose(dV[0, 0], dO[0, 0] + dO[0, 1], atol=1e-14)
