@@ -10,6 +10,9 @@ L2, so no explicit flush is done between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle, timed on the host
+  python bench.py --kernel-only attn_fwd --workload causal_gqa --steps 3 --warmup 3
+      # W + K launches of one kernel alone (for ncu captures); prints its
+      # median time
 
 Under torchrun every rank runs its own copy of the workload on its own GPU
 (weak scaling, no data-path collective); rank 0 prints one JSON line with the
@@ -305,7 +308,7 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded i.i.d. normal bf16 Q/K/V/dO; O and LSE from attn_fwd_ref)",
+        "data": "synthetic (seeded i.i.d. normal bf16 Q/K/V/dO; O and LSE from attn_fwd)",
         "config": {
             "workload": "%s B=%d H=%d H_kv=%d N=%d d=%d %s%s" % (
                 w.name, w.B, w.H, w.H_kv, w.N, w.d, "causal" if w.causal else "non-causal",
@@ -397,7 +400,70 @@ def all_configs(dev, peak, iters=20, warmup=3):
                      "fwd_ms": fms, "fwd_tflops": ftf, "fwd_frac_of_peak": ftf / peak}
         del x, q, k, v, do, o, lse, bufs
         torch.cuda.empty_cache()
+    out["causal_gqa_window1024"] = local_window_timing(dev, peak, iters, warmup)
     return out
+
+
+def visible_pairs(N, causal, left, right):
+    """(query, key) pairs of one head inside the band i - left <= j <= i + right
+    (negative = unbounded) and, if causal, j <= i."""
+    total = 0
+    for i in range(N):
+        lo = 0 if left < 0 else max(0, i - left)
+        hi = N - 1 if right < 0 else min(N - 1, i + right)
+        if causal:
+            hi = min(hi, i)
+        total += max(0, hi - lo + 1)
+    return total
+
+
+def local_window_timing(dev, peak, iters, warmup, left=1023):
+    """attn_bwd_local and attn_fwd_local on the causal GQA shape under a
+    causal sliding window of left + 1 keys; FLOPs counted over the visible
+    pairs (5 GEMMs of 2 d per pair backward, 2 forward)."""
+    import flashattention_attention_backward_gb300 as attn
+    from flashattention_attention_backward_gb300 import runner
+    from flashattention_attention_backward_gb300.inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS["causal_gqa"]
+    win = (left, -1)
+    stream = torch.cuda.current_stream(dev)
+    x = make_inputs(w)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = runner.forward(q, k, v, w.scale, True, window=win)
+    bufs = runner.BackwardBuffers(q, k)
+    bt, ft = [], []
+    for i in range(warmup + iters):
+        attn.check(attn.attn_bwd_preprocess(o, do, bufs.dpsum, bufs.dq_accum, w.B, w.H, w.N, w.d,
+                                            stream))
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(stream)
+        attn.check(attn.attn_bwd_local(q, k, v, o, do, lse, bufs.dq_accum, bufs.dk, bufs.dv, w.B,
+                                       w.H, w.H_kv, w.N, w.d, w.scale, True, 0.0, bufs.dpsum,
+                                       win[0], win[1], stream))
+        e[1].record(stream)
+        e[2].record(stream)
+        attn.check(attn.attn_fwd_local(q, k, v, o, lse, w.B, w.H, w.H_kv, w.N, w.d, w.scale,
+                                       True, 0.0, win[0], win[1], stream))
+        e[3].record(stream)
+        if i >= warmup:
+            bt.append((e[0], e[1]))
+            ft.append((e[2], e[3]))
+    torch.cuda.synchronize(dev)
+    rc, status = attn.attn_device_status(clear=True, stream=stream)
+    if rc != 0 or status != 0:
+        raise RuntimeError("device status %d on the local-window timing" % status)
+    pairs = w.B * w.H * visible_pairs(w.N, True, left, -1)
+    bms = sorted(a.elapsed_time(b) for a, b in bt)[len(bt) // 2]
+    fms = sorted(a.elapsed_time(b) for a, b in ft)[len(ft) // 2]
+    btf = 10.0 * w.d * pairs / (bms * 1e-3) / 1e12
+    ftf = 4.0 * w.d * pairs / (fms * 1e-3) / 1e12
+    del x, q, k, v, do, o, lse, bufs
+    torch.cuda.empty_cache()
+    return {"B": w.B, "H": w.H, "H_kv": w.H_kv, "N": w.N, "d": w.d, "causal": True,
+            "window": list(win), "visible_pairs": pairs, "bwd_ms": bms, "tflops": btf,
+            "frac_of_peak": btf / peak, "fwd_ms": fms, "fwd_tflops": ftf,
+            "fwd_frac_of_peak": ftf / peak}
 
 
 # ---------------------------------------------------------------- the oracle on the host
@@ -474,6 +540,56 @@ def run_reference(args, w):
     }
 
 
+def kernel_only(args, w):
+    """W + K launches of one kernel of the path on workload `w`, nothing else
+    between them (inputs prepared first); returns a short JSON-able record."""
+    import flashattention_attention_backward_gb300 as attn
+    from flashattention_attention_backward_gb300 import runner
+    from flashattention_attention_backward_gb300.inputs import make_inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    x = make_inputs(w)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    win = (args.window_left, -1) if args.kernel_only.endswith("_local") else None
+    o, lse = runner.forward(q, k, v, w.scale, w.causal, w.softcap, window=win)
+    bufs = runner.BackwardBuffers(q, k)
+    B, H, H_kv, N, d = w.B, w.H, w.H_kv, w.N, w.d
+    attn.check(attn.attn_bwd_preprocess(o, do, bufs.dpsum, bufs.dq_accum, B, H, N, d, stream))
+
+    def launch():
+        name = args.kernel_only
+        if name == "attn_fwd":
+            return attn.attn_fwd(q, k, v, o, lse, B, H, H_kv, N, d, w.scale, w.causal, w.softcap,
+                                 stream)
+        if name == "attn_fwd_local":
+            return attn.attn_fwd_local(q, k, v, o, lse, B, H, H_kv, N, d, w.scale, w.causal,
+                                       w.softcap, win[0], win[1], stream)
+        if name == "attn_bwd_local":
+            return attn.attn_bwd_local(q, k, v, o, do, lse, bufs.dq_accum, bufs.dk, bufs.dv, B, H,
+                                       H_kv, N, d, w.scale, w.causal, w.softcap, bufs.dpsum,
+                                       win[0], win[1], stream)
+        return attn.attn_bwd(q, k, v, o, do, lse, bufs.dq_accum, bufs.dk, bufs.dv, B, H, H_kv, N,
+                             d, w.scale, w.causal, w.softcap, bufs.dpsum, stream)
+
+    times = []
+    for i in range(args.warmup + args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        attn.check(launch())
+        e1.record(stream)
+        if i >= args.warmup:
+            times.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    rc, status = attn.attn_device_status(clear=True, stream=stream)
+    if rc != 0 or status != 0:
+        raise RuntimeError("device status %d" % status)
+    ms = sorted(a.elapsed_time(b) for a, b in times)[len(times) // 2]
+    return {"kernel": args.kernel_only, "workload": w.name, "window": win,
+            "launches": args.warmup + args.steps, "median_ms": ms}
+
+
 def main(argv=None):
     from flashattention_attention_backward_gb300.inputs import WORKLOADS
 
@@ -488,10 +604,18 @@ def main(argv=None):
                     help="skip the per-workload attn_bwd timings added to the line")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=120.0)
+    ap.add_argument("--kernel-only", default=None,
+                    choices=["attn_bwd", "attn_fwd", "attn_bwd_local", "attn_fwd_local"],
+                    help="launch only this kernel W + K times (profiling); no bench line")
+    ap.add_argument("--window-left", type=int, default=1023,
+                    help="left bound of the causal sliding window of the *_local kernels")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     w = WORKLOADS[args.workload]
+    if args.kernel_only:
+        print(json.dumps(kernel_only(args, w)), flush=True)
+        return
     line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
     if line is not None:
         print(json.dumps(line), flush=True)

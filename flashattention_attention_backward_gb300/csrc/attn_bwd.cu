@@ -141,6 +141,10 @@ struct Params {
   Dropout drop; // kernel template flag DROP: keep mask of philox.cuh
   float scale;
   float softcap;
+  // visibility band: key j is visible to query i iff
+  // i - win_left <= j <= i + win_right (the causal mask is win_right = 0;
+  // an unbounded side holds N)
+  int win_left, win_right;
 };
 
 // One unit of work: a block of 128 keys of one KV head of one batch entry,
@@ -161,7 +165,9 @@ __device__ __forceinline__ int unit_of(int r, int n_units) {
   return u < n_units ? u : -1;
 }
 
-template <bool CAUSAL>
+// The query blocks a key block meets are those holding a query of its
+// visibility band: queries n0 - win_right .. n0 + 127 + win_left. The band
+// always holds the diagonal, so every unit has at least one tile per head.
 __device__ __forceinline__ void unit_work(const Params& p, int u, Work& w) {
   const int per_nb = p.H_kv * p.B;
   w.n_block = u / per_nb;
@@ -169,9 +175,18 @@ __device__ __forceinline__ void unit_work(const Params& p, int u, Work& w) {
   w.b = rem / p.H_kv;
   w.g = rem - w.b * p.H_kv;
   w.G = p.H / p.H_kv;
-  w.m_start = CAUSAL ? w.n_block : 0;
-  w.per_head = p.m_blocks - w.m_start;
+  const int n0 = w.n_block * kBc;
+  w.m_start = max(0, n0 - p.win_right) / kBr;
+  const int m_end = min(p.m_blocks - 1, (n0 + kBc - 1 + p.win_left) / kBr);
+  w.per_head = m_end - w.m_start + 1;
   w.T = w.G * w.per_head;
+}
+
+// A tile needs the elementwise mask unless every (query, key) pair in it is
+// inside the band and inside the sequence.
+__device__ __forceinline__ bool tile_masked(const Params& p, int m0, int n0) {
+  return n0 + kBc - 1 - m0 > p.win_right || m0 + kBr - 1 - n0 > p.win_left || n0 + kBc > p.N ||
+         m0 + kBr > p.N;
 }
 
 struct Ctx {
@@ -258,7 +273,7 @@ __device__ void producer_role(const Ctx& c, const Params& p, uint8_t* smem, uint
     const int u = unit_of(r, p.n_units);
     if (u < 0) break;
     Work w;
-    unit_work<CAUSAL>(p, u, w);
+    unit_work(p, u, w);
     for (int tl = 0; tl < w.T; ++tl) {
       const int t = tg + tl;
       const int st = t & 1;
@@ -437,7 +452,7 @@ __device__ void mma_role(const Ctx& c, const Params& p, uint32_t sbase, uint32_t
     const int u = unit_of(r, p.n_units);
     if (u < 0) break;
     Work w;
-    unit_work<CAUSAL>(p, u, w);
+    unit_work(p, u, w);
     // unit prologue: dP of the first tile, then S
     {
       const int ost = tg % L::kDOStages;
@@ -581,7 +596,8 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
         }
         if (MASKED) {
           const int q = m0 + half * 64 + pass * kCols + j;
-          const bool ok = key < p.N && q < p.N && (!CAUSAL || key <= q);
+          const bool ok =
+              key < p.N && q < p.N && key - q <= p.win_right && q - key <= p.win_left;
           prob = ok ? prob : 0.f;
           keep = ok ? keep : 0.f;
         }
@@ -667,17 +683,16 @@ __device__ void softmax_role(const Ctx& c, const Params& p, uint8_t* smem, uint3
     const int u = unit_of(ur, p.n_units);
     if (u < 0) break;
     Work w;
-    unit_work<CAUSAL>(p, u, w);
+    unit_work(p, u, w);
     const int n0 = w.n_block * kBc;
     const int key = n0 + r;
-    const bool key_tail = n0 + kBc > p.N;
     for (int tl = 0; tl < w.T && ok; ++tl) {
       const int t = tg + tl;
       int h, m_block;
       tile_coord(w, tl, h, m_block);
       const int m0 = m_block * kBr;
       if (!(ok = wait(c, BAR_Q_FULL + (t & 1), (t >> 1) & 1))) break;
-      const bool masked = (CAUSAL && m_block == w.n_block) || key_tail || (m0 + kBr > p.N);
+      const bool masked = tile_masked(p, m0, n0);
       const int dsbuf = (tl == 0 && ur > 0) ? ((ur - 1) & 1) : -1;
       const uint32_t bh = static_cast<uint32_t>(w.b * p.H + h);
       if (masked)
@@ -813,13 +828,13 @@ __device__ void dq_role(const Ctx& c, const Params& p, uint8_t* smem, uint32_t s
       const int u = unit_of(ur++, p.n_units);
       if (u < 0) break;
       Work w;
-      unit_work<CAUSAL>(p, u, w);
+      unit_work(p, u, w);
       kvh = w.b * p.H_kv + w.g;
       row0 = w.n_block * kBc;
       T = w.T;
       head0 = w.b * p.H + w.g * G;
       hh = 0;
-      m_block = p.m_blocks - 1;
+      m_block = w.m_start + w.per_head - 1;
     }
     {
       const int t = tg + tl;
@@ -1062,7 +1077,7 @@ int dispatch(const Maps& m, const Params& p, cudaStream_t s, int d, bool cs, boo
 int run(const void* q, const void* k, const void* v, const void* dO, const float* lse,
         float* dq_target, void* dk, void* dv, int B, int H, int H_kv, int N, int d, float scale,
         int causal, float softcap, const float* dpsum, void* stream, bool det, float p_drop = 0.f,
-        unsigned long long seed = 0) {
+        unsigned long long seed = 0, int window_left = -1, int window_right = -1) {
   if (!q || !k || !v || !dO || !lse || !dq_target || !dk || !dv || !dpsum) return ATTN_ERR_NULL;
   int rc = check_shape(B, H, H_kv, N, d);
   if (rc != ATTN_OK) return rc;
@@ -1094,6 +1109,10 @@ int run(const void* q, const void* k, const void* v, const void* dO, const float
   p.scale = scale;
   const bool cap = softcap > 0.f;
   p.softcap = cap ? softcap : 0.f;
+  // a negative or wider-than-N side of the window is unbounded (N); the
+  // causal mask bounds the right side at 0
+  p.win_left = (window_left < 0 || window_left > N) ? N : window_left;
+  p.win_right = causal ? 0 : ((window_right < 0 || window_right > N) ? N : window_right);
   const bool drop = p_drop > 0.f;
   p.drop.seed_lo = static_cast<uint32_t>(seed);
   p.drop.seed_hi = static_cast<uint32_t>(seed >> 32);
@@ -1137,6 +1156,16 @@ extern "C" int attn_bwd_dropout(const void* q, const void* k, const void* v, con
   (void)o;
   return bwd::run(q, k, v, dO, lse, dq_accum, dk, dv, B, H, H_kv, N, d, scale, causal, softcap,
                   dpsum, stream, false, p_drop, seed);
+}
+
+extern "C" int attn_bwd_local(const void* q, const void* k, const void* v, const void* o,
+                              const void* dO, const float* lse, float* dq_accum, void* dk,
+                              void* dv, int B, int H, int H_kv, int N, int d, float scale,
+                              int causal, float softcap, const float* dpsum, int window_left,
+                              int window_right, void* stream) {
+  (void)o;
+  return bwd::run(q, k, v, dO, lse, dq_accum, dk, dv, B, H, H_kv, N, d, scale, causal, softcap,
+                  dpsum, stream, false, 0.f, 0, window_left, window_right);
 }
 
 extern "C" int attn_bwd_deterministic(const void* q, const void* k, const void* v,

@@ -84,6 +84,10 @@ struct Params {
   int m_blocks;
   float scale;
   float softcap;
+  // visibility band: key j is visible to query i iff
+  // i - win_left <= j <= i + win_right (the causal mask is win_right = 0;
+  // an unbounded side holds N)
+  int win_left, win_right;
 };
 
 struct Ctx {
@@ -126,22 +130,26 @@ __device__ __forceinline__ void wait_drain(const Ctx& c, int bar, uint32_t parit
   }
 }
 
-// Work of one CTA: query block m_block of head bh (= b * H + h).
+// Work of one CTA: query block m_block of head bh (= b * H + h), against
+// key blocks j0 .. j0 + nk - 1 (those holding a key of the rows' bands).
 struct Work {
-  int bh, kvh, m_block, nk;  // nk: key blocks visited (per pass)
+  int bh, kvh, m_block, j0, nk;  // nk: key blocks visited (per pass)
 };
 
-template <bool CAUSAL>
 __device__ __forceinline__ Work work_of(const Params& p) {
   Work w;
   const int heads = p.B * p.H;
   const int idx = static_cast<int>(blockIdx.x);
-  // heaviest query blocks first for a causal mask
+  // heaviest query blocks first for a causal mask (the last ones see the
+  // most keys)
   w.m_block = p.m_blocks - 1 - idx / heads;
   w.bh = idx - (idx / heads) * heads;
   const int b = w.bh / p.H, h = w.bh - b * p.H;
   w.kvh = b * p.H_kv + h / (p.H / p.H_kv);
-  w.nk = CAUSAL ? w.m_block + 1 : (p.N + kBn - 1) / kBn;
+  const int m0 = w.m_block * kBm;
+  w.j0 = max(0, m0 - p.win_left) / kBn;
+  const int j_end = min((p.N + kBn - 1) / kBn - 1, (m0 + kBm - 1 + p.win_right) / kBn);
+  w.nk = j_end - w.j0 + 1;
   return w;
 }
 
@@ -174,8 +182,8 @@ __device__ void producer_role(const Ctx& c, const Work& w, uint32_t sbase, const
       mbar_arrive_expect_tx(bar_addr(c, BAR_K_FULL + ks), kTileBytes);
       const uint32_t dst = sbase + (ks ? L::kK1 : L::kK0);
       for (int cb = 0; cb < kBoxes; ++cb)
-        tma_load_3d_hint(dst + cb * 16384, tk, bar_addr(c, BAR_K_FULL + ks), 64 * cb, j * kBn,
-                         w.kvh, keep);
+        tma_load_3d_hint(dst + cb * 16384, tk, bar_addr(c, BAR_K_FULL + ks), 64 * cb,
+                         (w.j0 + j) * kBn, w.kvh, keep);
     }
     issued_k = s + 1;
     if (pass2) {
@@ -185,8 +193,8 @@ __device__ void producer_role(const Ctx& c, const Work& w, uint32_t sbase, const
         mbar_arrive_expect_tx(bar_addr(c, BAR_V_FULL + vs), kTileBytes);
         const uint32_t dst = sbase + (vs ? L::kV1 : L::kV0);
         for (int cb = 0; cb < kBoxes; ++cb)
-          tma_load_3d_hint(dst + cb * 16384, tv, bar_addr(c, BAR_V_FULL + vs), 64 * cb, j * kBn,
-                           w.kvh, keep);
+          tma_load_3d_hint(dst + cb * 16384, tv, bar_addr(c, BAR_V_FULL + vs), 64 * cb,
+                           (w.j0 + j) * kBn, w.kvh, keep);
       }
       issued_v = j + 1;
     }
@@ -269,6 +277,67 @@ __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t t
 }
 
 // ------------------------------------------------------------------ softmax
+// One S tile of one query row (this thread's tensor-memory lane), in four
+// 32-key chunks. Pass 1 (PASS2 false) folds the chunk into the running
+// maximum m and sum l of 2^x; pass 2 writes P = 2^(x - lse2) as bf16 pairs
+// over the first half of the S buffer. MASKED tiles (the band's edges, the
+// sequence's end) hide invisible keys with -inf; the others skip the test.
+template <bool SOFTCAP, bool MASKED, bool PASS2>
+__device__ __forceinline__ void tile_rows(const Params& p, uint32_t tS, int n0, int q,
+                                          float c_log2, float cap_in, float cap_out, float& m,
+                                          float& l, float lse2) {
+#pragma unroll
+  for (int ch = 0; ch < kBn / 32; ++ch) {
+    uint32_t raw[32];
+    tmem_ld32(tS + ch * 32, raw);
+    float cm0 = -INFINITY, cm1 = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const float sv = __uint_as_float(raw[e]);
+      float x;
+      if (SOFTCAP) {
+        // tanh(u) = 1 - 2 / (exp(2u) + 1) with u = tau s / c
+        const float ex = ex2_approx(sv * cap_in);
+        x = (1.f - 2.f * rcp_approx(ex + 1.f)) * cap_out;
+      } else {
+        x = sv * c_log2;
+      }
+      if (MASKED) {
+        const int key = n0 + ch * 32 + e;
+        if (!(key < p.N && key - q <= p.win_right && q - key <= p.win_left)) x = -INFINITY;
+      }
+      raw[e] = __float_as_uint(x);
+      if (!PASS2) {
+        if (e & 1)
+          cm1 = fmaxf(cm1, x);
+        else
+          cm0 = fmaxf(cm0, x);
+      }
+    }
+    if (!PASS2) {
+      const float mn = fmaxf(m, fmaxf(cm0, cm1));
+      // only a masked chunk (a window's edge, a padding row) can hold no
+      // visible key; the shift then stays finite so that -inf - -inf never
+      // arises (the exponentials of -inf are 0)
+      const float sh = (MASKED && mn == -INFINITY) ? 0.f : mn;
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int e = 0; e < 32; ++e) s4[e & 3] += ex2_approx(__uint_as_float(raw[e]) - sh);
+      l = l * ex2_approx(m - sh) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+      m = mn;
+    } else {
+      uint32_t packed[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        packed[u] = pack_bf16x2(ex2_approx(__uint_as_float(raw[2 * u]) - lse2),
+                                ex2_approx(__uint_as_float(raw[2 * u + 1]) - lse2));
+      // keys 32 ch .. 32 ch + 31 -> columns 16 ch .. 16 ch + 15, whose S
+      // values were read in this or an earlier chunk
+      tmem_st16(tS + ch * 16, packed);
+    }
+  }
+}
+
 // Two warpgroups; warpgroup w takes the S GEMMs s with s & 1 == w, i.e. S
 // buffer w, so each processes one tile while the other's S GEMM runs.
 // Thread = query row r (tensor-memory lane). Pass 1 keeps the running
@@ -278,7 +347,7 @@ __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t t
 // P = 2^(x - LSE2) as bf16 pairs over the first half of the S buffer, which
 // the PV GEMM reads as its A operand. Then each warpgroup stores half of the
 // columns of O.
-template <int D, bool CAUSAL, bool SOFTCAP>
+template <int D, bool SOFTCAP>
 __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8_t* smem,
                              uint32_t sbase, uint32_t tmem, const CUtensorMap* to) {
   using L = Layout<D>;
@@ -304,52 +373,20 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8
     ok = named_bar_and(bar_wg, 128, wait(c, BAR_S_FULL + wg, (s >> 1) & 1));
     if (!ok) return false;
     tc_fence_after();
-    const bool masked = (CAUSAL && j == w.m_block) || (j + 1) * kBn > p.N;
-#pragma unroll
-    for (int ch = 0; ch < kBn / 32; ++ch) {
-      uint32_t raw[32];
-      tmem_ld32(tS + ch * 32, raw);
-      float cm0 = -INFINITY, cm1 = -INFINITY;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float sv = __uint_as_float(raw[e]);
-        float x;
-        if (SOFTCAP) {
-          // tanh(u) = 1 - 2 / (exp(2u) + 1) with u = tau s / c
-          const float ex = ex2_approx(sv * cap_in);
-          x = (1.f - 2.f * rcp_approx(ex + 1.f)) * cap_out;
-        } else {
-          x = sv * c_log2;
-        }
-        if (masked) {
-          const int key = j * kBn + ch * 32 + e;
-          if (!(key < p.N && (!CAUSAL || key <= q))) x = -INFINITY;
-        }
-        raw[e] = __float_as_uint(x);
-        if (e & 1)
-          cm1 = fmaxf(cm1, x);
-        else
-          cm0 = fmaxf(cm0, x);
-      }
-      if (!pass2) {
-        // a row's first chunk always holds a visible key (key 0, or the
-        // diagonal), so m is finite from there on and -inf - -inf never arises
-        const float mn = fmaxf(m, fmaxf(cm0, cm1));
-        float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int e = 0; e < 32; ++e) s4[e & 3] += ex2_approx(__uint_as_float(raw[e]) - mn);
-        l = l * ex2_approx(m - mn) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
-        m = mn;
-      } else {
-        uint32_t packed[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-          packed[u] = pack_bf16x2(ex2_approx(__uint_as_float(raw[2 * u]) - lse2),
-                                  ex2_approx(__uint_as_float(raw[2 * u + 1]) - lse2));
-        // keys 32 ch .. 32 ch + 31 -> columns 16 ch .. 16 ch + 15, whose S
-        // values were read in this or an earlier chunk
-        tmem_st16(tS + ch * 16, packed);
-      }
+    const int n0 = (w.j0 + j) * kBn;
+    const int m0 = w.m_block * kBm;
+    const bool masked = n0 + kBn - 1 - m0 > p.win_right || m0 + kBm - 1 - n0 > p.win_left ||
+                        n0 + kBn > p.N;
+    if (pass2) {
+      if (masked)
+        tile_rows<SOFTCAP, true, true>(p, tS, n0, q, c_log2, cap_in, cap_out, m, l, lse2);
+      else
+        tile_rows<SOFTCAP, false, true>(p, tS, n0, q, c_log2, cap_in, cap_out, m, l, lse2);
+    } else {
+      if (masked)
+        tile_rows<SOFTCAP, true, false>(p, tS, n0, q, c_log2, cap_in, cap_out, m, l, lse2);
+      else
+        tile_rows<SOFTCAP, false, false>(p, tS, n0, q, c_log2, cap_in, cap_out, m, l, lse2);
     }
     if (!pass2) {
       // the buffer is free for the next S GEMM once every row has read it
@@ -376,7 +413,10 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8
     named_bar_sync(3, 256);
     const float mo = st[((1 - wg) * 128 + r) * 2], lo = st[((1 - wg) * 128 + r) * 2 + 1];
     const float mx = fmaxf(m, mo);
-    lse2 = mx + __log2f(l * ex2_approx(m - mx) + lo * ex2_approx(mo - mx));
+    const float sh = mx == -INFINITY ? 0.f : mx;
+    lse2 = sh + __log2f(l * ex2_approx(m - sh) + lo * ex2_approx(mo - sh));
+    // a padding row past N may see no key at all: its P must be 0, not NaN
+    if (!(lse2 < INFINITY && lse2 > -INFINITY)) lse2 = INFINITY;
   }
   // pass 2
   for (int s = ((w.nk & 1) == wg) ? w.nk : w.nk + 1; ok && s < 2 * w.nk; s += 2) ok = tile(s);
@@ -414,7 +454,7 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool CAUSAL, bool SOFTCAP>
+template <int D, bool SOFTCAP>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -444,13 +484,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
-  const Work w = work_of<CAUSAL>(p);
+  const Work w = work_of(p);
   if (warp == 0) {
     producer_role<D>(c, w, sbase, &tm_q, &tm_k, &tm_v);
   } else if (warp == 1) {
     mma_role<D>(c, w, sbase, tmem);
   } else if (warp >= 4) {
-    softmax_role<D, CAUSAL, SOFTCAP>(c, p, w, smem, sbase, tmem, &tm_o);
+    softmax_role<D, SOFTCAP>(c, p, w, smem, sbase, tmem, &tm_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -460,10 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool SOFTCAP>
+template <int D, bool SOFTCAP>
 int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
            const CUtensorMap& to, const Params& p, cudaStream_t stream) {
-  auto kern = attn_fwd_kernel<D, CAUSAL, SOFTCAP>;
+  auto kern = attn_fwd_kernel<D, SOFTCAP>;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -497,9 +537,12 @@ int fwd_status(int* status, bool clear) {
 
 using namespace attn;
 
-extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                        int H, int H_kv, int N, int d, float scale, int causal, float softcap,
-                        void* stream) {
+namespace attn {
+namespace fwdtc {
+
+int run(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv,
+        int N, int d, float scale, int causal, float softcap, int window_left, int window_right,
+        void* stream) {
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
   int rc = check_shape(B, H, H_kv, N, d);
   if (rc != ATTN_OK) return rc;
@@ -510,31 +553,41 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
   CUtensorMap tq, tk, tv, to;
   const long long hq = static_cast<long long>(B) * H, hk = static_cast<long long>(B) * H_kv;
-  if (!encode_bf16_3d(&tq, q, d, N, hq, fwdtc::kBm) ||
-      !encode_bf16_3d(&tk, k, d, N, hk, fwdtc::kBn) ||
-      !encode_bf16_3d(&tv, v, d, N, hk, fwdtc::kBn) ||
-      !encode_bf16_3d(&to, o, d, N, hq, fwdtc::kBm))
+  if (!encode_bf16_3d(&tq, q, d, N, hq, kBm) || !encode_bf16_3d(&tk, k, d, N, hk, kBn) ||
+      !encode_bf16_3d(&tv, v, d, N, hk, kBn) || !encode_bf16_3d(&to, o, d, N, hq, kBm))
     return ATTN_ERR_LAUNCH;
-  fwdtc::Params p;
+  Params p;
   p.lse = lse;
   p.B = B;
   p.H = H;
   p.H_kv = H_kv;
   p.N = N;
-  p.m_blocks = (N + fwdtc::kBm - 1) / fwdtc::kBm;
+  p.m_blocks = (N + kBm - 1) / kBm;
   p.scale = scale;
   const bool cap = softcap > 0.f;
   p.softcap = cap ? softcap : 0.f;
+  // a negative or wider-than-N side of the window is unbounded (N); the
+  // causal mask bounds the right side at 0
+  p.win_left = (window_left < 0 || window_left > N) ? N : window_left;
+  p.win_right = causal ? 0 : ((window_right < 0 || window_right > N) ? N : window_right);
   cudaStream_t s = as_stream(stream);
-  const bool cs = causal != 0;
-  if (d == 128) {
-    if (cs) return cap ? fwdtc::launch<128, true, true>(tq, tk, tv, to, p, s)
-                       : fwdtc::launch<128, true, false>(tq, tk, tv, to, p, s);
-    return cap ? fwdtc::launch<128, false, true>(tq, tk, tv, to, p, s)
-               : fwdtc::launch<128, false, false>(tq, tk, tv, to, p, s);
-  }
-  if (cs) return cap ? fwdtc::launch<64, true, true>(tq, tk, tv, to, p, s)
-                     : fwdtc::launch<64, true, false>(tq, tk, tv, to, p, s);
-  return cap ? fwdtc::launch<64, false, true>(tq, tk, tv, to, p, s)
-             : fwdtc::launch<64, false, false>(tq, tk, tv, to, p, s);
+  if (d == 128)
+    return cap ? launch<128, true>(tq, tk, tv, to, p, s) : launch<128, false>(tq, tk, tv, to, p, s);
+  return cap ? launch<64, true>(tq, tk, tv, to, p, s) : launch<64, false>(tq, tk, tv, to, p, s);
+}
+
+}  // namespace fwdtc
+}  // namespace attn
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int H_kv, int N, int d, float scale, int causal, float softcap,
+                        void* stream) {
+  return fwdtc::run(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap, -1, -1, stream);
+}
+
+extern "C" int attn_fwd_local(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H, int H_kv, int N, int d, float scale, int causal,
+                              float softcap, int window_left, int window_right, void* stream) {
+  return fwdtc::run(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap, window_left,
+                    window_right, stream);
 }

@@ -43,7 +43,10 @@ struct Params {
   int q_blocks;
   float scale;
   float softcap;  // <= 0: disabled
-  int causal;
+  // visibility band: key j is visible to query i iff
+  // i - win_left <= j <= i + win_right (causal: win_right = 0; an unbounded
+  // side holds N)
+  int win_left, win_right;
   int dropout;    // 0: off; else the keep mask of philox.cuh scales P in O = P V
   Dropout drop;
 };
@@ -105,8 +108,9 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_ref_kernel(const Params p) 
   }
 
   const int n_tiles = (p.N + kBN - 1) / kBN;
-  const int last_tile = p.causal ? min(n_tiles - 1, (m0 + kBM - 1) / kBN) : n_tiles - 1;
-  for (int kt = 0; kt <= last_tile; ++kt) {
+  const int first_tile = max(0, m0 - p.win_left) / kBN;
+  const int last_tile = min(n_tiles - 1, (m0 + kBM - 1 + p.win_right) / kBN);
+  for (int kt = first_tile; kt <= last_tile; ++kt) {
     const int n0 = kt * kBN;
     __syncthreads();  // previous tile's sKt / sV / sP reads are done
     for (int idx = tid; idx < kBN * (D / 8); idx += kThreads) {
@@ -169,7 +173,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_ref_kernel(const Params p) 
         const int key = n0 + tx * 4 + j;
         float s = acc[i][j] * p.scale;
         if (p.softcap > 0.f) s = p.softcap * tanhf(s / p.softcap);
-        const bool ok = key < p.N && (!p.causal || key <= qrow);
+        const bool ok = key < p.N && key - qrow <= p.win_right && qrow - key <= p.win_left;
         z[j] = ok ? s : -CUDART_INF_F;
         mx = fmaxf(mx, z[j]);
       }
@@ -261,7 +265,7 @@ namespace fwd {
 
 int run(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv,
         int N, int d, float scale, int causal, float softcap, float p_drop,
-        unsigned long long seed, void* stream) {
+        unsigned long long seed, void* stream, int window_left = -1, int window_right = -1) {
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
   int rc = check_shape(B, H, H_kv, N, d);
   if (rc != ATTN_OK) return rc;
@@ -284,7 +288,9 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
   p.q_blocks = (N + kBM - 1) / kBM;
   p.scale = scale;
   p.softcap = softcap > 0.f ? softcap : 0.f;
-  p.causal = causal != 0;
+  // a negative or wider-than-N side of the window is unbounded (N)
+  p.win_left = (window_left < 0 || window_left > N) ? N : window_left;
+  p.win_right = causal ? 0 : ((window_right < 0 || window_right > N) ? N : window_right);
   p.dropout = p_drop > 0.f ? 1 : 0;
   p.drop.seed_lo = static_cast<uint32_t>(seed);
   p.drop.seed_hi = static_cast<uint32_t>(seed >> 32);
@@ -309,4 +315,12 @@ extern "C" int attn_fwd_ref_dropout(const void* q, const void* k, const void* v,
                                     unsigned long long seed, void* stream) {
   return fwd::run(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap, p_drop, seed,
                   stream);
+}
+
+extern "C" int attn_fwd_ref_local(const void* q, const void* k, const void* v, void* o,
+                                  float* lse, int B, int H, int H_kv, int N, int d, float scale,
+                                  int causal, float softcap, int window_left, int window_right,
+                                  void* stream) {
+  return fwd::run(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap, 0.f, 0ull, stream,
+                  window_left, window_right);
 }

@@ -5,8 +5,9 @@ finalize. No arithmetic happens here; torch provides memory and streams.
 import torch
 
 from . import (attn_bwd, attn_bwd_deterministic, attn_bwd_dq_partials_bytes, attn_bwd_dropout,
-               attn_bwd_finalize, attn_bwd_finalize_partials, attn_bwd_preprocess, attn_fwd,
-               attn_fwd_ref, attn_fwd_ref_dropout, check)
+               attn_bwd_finalize, attn_bwd_finalize_partials, attn_bwd_local, attn_bwd_preprocess,
+               attn_fwd, attn_fwd_local, attn_fwd_ref, attn_fwd_ref_dropout, attn_fwd_ref_local,
+               check)
 
 
 def _dims(q, k):
@@ -19,16 +20,23 @@ def _stream(stream):
     return stream if stream is not None else torch.cuda.current_stream()
 
 
-def forward(q, k, v, scale, causal, softcap=0.0, stream=None, impl="tc", dropout=None):
+def forward(q, k, v, scale, causal, softcap=0.0, stream=None, impl="tc", dropout=None,
+            window=None):
     """O [B,H,N,d] bf16 and LSE [B,H,N] fp32: attn_fwd (tensor cores, impl
     "tc") or attn_fwd_ref (plain fp32, impl "ref"). dropout = (p_drop, seed)
-    runs attn_fwd_ref_dropout."""
+    runs attn_fwd_ref_dropout; window = (left, right) runs attn_fwd_local or
+    attn_fwd_ref_local."""
     B, H, H_kv, N, d = _dims(q, k)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if dropout is not None:
         check(attn_fwd_ref_dropout(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap,
                                    dropout[0], dropout[1], _stream(stream)))
+        return o, lse
+    if window is not None:
+        fn = {"tc": attn_fwd_local, "ref": attn_fwd_ref_local}[impl]
+        check(fn(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap, window[0], window[1],
+                 _stream(stream)))
         return o, lse
     fn = {"tc": attn_fwd, "ref": attn_fwd_ref}[impl]
     check(fn(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap, _stream(stream)))
@@ -49,10 +57,11 @@ class BackwardBuffers:
 
 
 def backward(q, k, v, o, do, lse, scale, causal, softcap=0.0, stream=None, bufs=None,
-             deterministic=False, dropout=None):
+             deterministic=False, dropout=None, window=None):
     """dQ, dK, dV (bf16) via preprocess -> attn_bwd -> finalize, or, with
     deterministic=True, preprocess -> attn_bwd_deterministic ->
-    finalize_partials (dQ identical bit for bit from run to run)."""
+    finalize_partials (dQ identical bit for bit from run to run). window =
+    (left, right) runs attn_bwd_local in place of attn_bwd."""
     B, H, H_kv, N, d = _dims(q, k)
     s = _stream(stream)
     if bufs is None:
@@ -62,6 +71,14 @@ def backward(q, k, v, o, do, lse, scale, causal, softcap=0.0, stream=None, bufs=
         check(attn_bwd_dropout(q, k, v, o, do, lse, bufs.dq_accum, bufs.dk, bufs.dv, B, H, H_kv,
                                N, d, scale, causal, softcap, bufs.dpsum, dropout[0], dropout[1],
                                s))
+        check(attn_bwd_finalize(bufs.dq_accum, bufs.dq, scale, B, H, N, d, s))
+        return bufs.dq, bufs.dk, bufs.dv
+    if window is not None:
+        if deterministic:
+            raise ValueError("the local window has no deterministic variant")
+        check(attn_bwd_preprocess(o, do, bufs.dpsum, bufs.dq_accum, B, H, N, d, s))
+        check(attn_bwd_local(q, k, v, o, do, lse, bufs.dq_accum, bufs.dk, bufs.dv, B, H, H_kv, N,
+                             d, scale, causal, softcap, bufs.dpsum, window[0], window[1], s))
         check(attn_bwd_finalize(bufs.dq_accum, bufs.dq, scale, B, H, N, d, s))
         return bufs.dq, bufs.dk, bufs.dv
     if not deterministic:

@@ -108,6 +108,35 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              int H_kv, int N, int d, float scale, int causal, float softcap, void* stream);
 
 /*
+ * Local (sliding-window) attention ([bwd-detail] §3.4, the third masking
+ * phase of the Q-inner loop: query blocks at the window's edge are masked
+ * elementwise, those inside it run unmasked, those outside it are skipped).
+ * Key j is visible to query i iff
+ *     i - window_left <= j <= i + window_right,
+ * and, if causal != 0, also j <= i. A negative bound (or one of N or more)
+ * leaves that side unbounded, so (-1, -1) is the plain call, and (-1, 0)
+ * without causal equals the causal mask. Every row keeps its own key (the
+ * diagonal), so LSE is always finite.
+ *
+ * attn_fwd_local, attn_fwd_ref_local: attn_fwd / attn_fwd_ref under that
+ *   mask (same outputs and layouts).
+ * attn_bwd_local: attn_bwd under that mask; a CTA visits only the query
+ *   blocks of its key block's band. Run it with attn_bwd_preprocess and
+ *   attn_bwd_finalize as attn_bwd.
+ * Arguments, errors and stream order as for the calls they extend.
+ */
+int attn_fwd_local(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int H_kv, int N, int d, float scale, int causal, float softcap,
+                   int window_left, int window_right, void* stream);
+int attn_fwd_ref_local(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int H_kv, int N, int d, float scale, int causal, float softcap,
+                       int window_left, int window_right, void* stream);
+int attn_bwd_local(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                   const float* lse, float* dq_accum, void* dk, void* dv, int B, int H, int H_kv,
+                   int N, int d, float scale, int causal, float softcap, const float* dpsum,
+                   int window_left, int window_right, void* stream);
+
+/*
  * attn_bwd_preprocess: D = rowsum(dO o O) ([FA-v1-bwd] §2.4 eq. 6;
  * [bwd-detail] §2.1(3), "dPsum", computed before the main kernel) and
  * dq_accum := 0.
