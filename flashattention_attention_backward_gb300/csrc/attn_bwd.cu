@@ -96,7 +96,7 @@ struct Layout {
   static constexpr int kDS = kDO0 + kDOStages * kTileBytes;  // dS^T, [key][query], 32 KB
   static constexpr int kDQS = kDS + kBc * kBr * 2;            // dQ staging
   static constexpr int kDQSBytes = D == 128 ? 2 * 16384 : 8 * 2 * 4096;
-  static constexpr int kLSE = kDQS + kDQSBytes;  // 2 stages x 128 fp32 (LSE*log2e)
+  static constexpr int kLSE = kDQS + kDQSBytes;  // 2 stages x 128 fp32 (-LSE*log2e)
   static constexpr int kDsum = kLSE + 2 * kBr * 4;  // 2 stages x 128 fp32 (D)
   static constexpr int kBars = kDsum + 2 * kBr * 4;
   static constexpr int kNumBars = 21;
@@ -302,7 +302,7 @@ __device__ void producer_role(const Ctx& c, const Params& p, uint8_t* smem, uint
             lv = __ldg(p.lse + row0 + i);
             dv = __ldg(p.dpsum + row0 + i);
           }
-          s_lse[i] = lv * kLog2e;
+          s_lse[i] = -lv * kLog2e;
           s_d[i] = dv;
         }
         mbar_arrive(bar_addr(c, BAR_Q_FULL + st));
@@ -542,7 +542,15 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
   const float c_log2 = p.scale * kLog2e;                                  // tau*log2e
   const float cap_in = SOFTCAP ? 2.f * kLog2e * p.scale / p.softcap : 0.f;  // 2 log2e tau/c
   const float cap_out = SOFTCAP ? p.softcap * kLog2e : 0.f;                 // c log2e
-  float pk[64];  // P, or P (1 - tanh^2) with softcap, for this thread's 64 columns
+  // pairs of columns go through the f32x2 arithmetic (same roundings as the
+  // scalar forms, half the instructions)
+  const uint64_t c2 = f2_make(SOFTCAP ? cap_in : c_log2, SOFTCAP ? cap_in : c_log2);
+  const uint64_t out2 = f2_make(cap_out, cap_out);
+  const uint64_t one2 = f2_make(1.f, 1.f), mone2 = f2_make(-1.f, -1.f),
+                 mtwo2 = f2_make(-2.f, -2.f);
+  // P, or with a softcap -P (1 - tanh^2) (the sign is undone in the dS
+  // phase), for this thread's 64 columns as 32 pairs
+  uint64_t pk[32];
   uint32_t km[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};  // dropout keep bits of the 64 columns
 
   // ---- P = exp(S - LSE) -> bf16 P^T in tensor memory
@@ -565,9 +573,10 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
       tmem_ld32(src, raw);
 #pragma unroll
     for (int j4 = 0; j4 < kCols / 4; ++j4) {
+      // -LSE*log2e of the four query columns
       const float4 l4 =
           *reinterpret_cast<const float4*>(s_lse + half * 64 + pass * kCols + 4 * j4);
-      const float lse4[4] = {l4.x, l4.y, l4.z, l4.w};
+      const uint64_t nl2[2] = {f2_make(l4.x, l4.y), f2_make(l4.z, l4.w)};
       uint32_t kb = 0xFu;
       if (DROP) {
         const int cc = pass * kCols + 4 * j4;  // first of the four columns
@@ -580,30 +589,41 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
         km[cc >> 5] = (km[cc >> 5] & ~(0xFu << (cc & 31))) | (kb << (cc & 31));
       }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = 4 * j4 + e;
-        const float s = __uint_as_float(raw[j]);
-        float prob, keep;
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int j = 4 * j4 + 2 * e2;  // columns j, j + 1 of this group
+        const uint64_t s2 = f2_make(raw[j], raw[j + 1]);
+        float pr[2], kp[2];
         if (SOFTCAP) {
           // tanh(u) = 1 - 2 / (exp(2u) + 1) with u = tau s / c
-          const float ex = ex2_approx(s * cap_in);
-          const float th = 1.f - 2.f * rcp_approx(ex + 1.f);
-          prob = ex2_approx(th * cap_out - lse4[e]);
-          keep = prob * (1.f - th * th);
+          const uint64_t u2 = f2_mul(s2, c2);
+          const uint64_t e1 = f2_add(f2_make(ex2_approx(f2_lo(u2)), ex2_approx(f2_hi(u2))), one2);
+          const uint64_t th2 =
+              f2_fma(f2_make(rcp_approx(f2_lo(e1)), rcp_approx(f2_hi(e1))), mtwo2, one2);
+          const uint64_t y2 = f2_fma(th2, out2, nl2[e2]);
+          pr[0] = ex2_approx(f2_lo(y2));
+          pr[1] = ex2_approx(f2_hi(y2));
+          // -P (1 - tanh^2) = P (tanh^2 - 1)
+          const uint64_t k2 = f2_mul(f2_make(pr[0], pr[1]), f2_fma(th2, th2, mone2));
+          kp[0] = f2_lo(k2);
+          kp[1] = f2_hi(k2);
         } else {
-          prob = ex2_approx(s * c_log2 - lse4[e]);
-          keep = prob;
+          const uint64_t y2 = f2_fma(s2, c2, nl2[e2]);
+          pr[0] = kp[0] = ex2_approx(f2_lo(y2));
+          pr[1] = kp[1] = ex2_approx(f2_hi(y2));
         }
-        if (MASKED) {
-          const int q = m0 + half * 64 + pass * kCols + j;
-          const bool ok =
-              key < p.N && q < p.N && key - q <= p.win_right && q - key <= p.win_left;
-          prob = ok ? prob : 0.f;
-          keep = ok ? keep : 0.f;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          if (MASKED) {
+            const int q = m0 + half * 64 + pass * kCols + j + h2;
+            const bool ok =
+                key < p.N && q < p.N && key - q <= p.win_right && q - key <= p.win_left;
+            pr[h2] = ok ? pr[h2] : 0.f;
+            kp[h2] = ok ? kp[h2] : 0.f;
+          }
+          if (DROP) pr[h2] = (kb >> (2 * e2 + h2)) & 1u ? pr[h2] * p.drop.inv_keep : 0.f;
+          raw[j + h2] = __float_as_uint(pr[h2]);
         }
-        if (DROP) prob = (kb >> e) & 1u ? prob * p.drop.inv_keep : 0.f;
-        raw[j] = __float_as_uint(prob);
-        pk[pass * kCols + j] = keep;
+        pk[(pass * kCols + j) >> 1] = f2_make(kp[0], kp[1]);
       }
     }
 #pragma unroll
@@ -639,13 +659,22 @@ __device__ __forceinline__ bool softmax_tile(const Ctx& c, const Params& p, uint
 #pragma unroll
     for (int j4 = 0; j4 < 8; ++j4) {
       const float4 d4 = *reinterpret_cast<const float4*>(s_d + col0 + 4 * j4);
-      const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+      const uint64_t dd2[2] = {f2_make(d4.x, d4.y), f2_make(d4.z, d4.w)};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = 4 * j4 + e;
-        float dp = __uint_as_float(raw[j]);
-        if (DROP) dp = (km[hh] >> j) & 1u ? dp * p.drop.inv_keep : 0.f;
-        raw[j] = __float_as_uint(pk[hh * 32 + j] * (dp - dd[e]));
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int j = 4 * j4 + 2 * e2;
+        uint32_t dp0 = raw[j], dp1 = raw[j + 1];
+        if (DROP) {
+          dp0 = (km[hh] >> j) & 1u ? __float_as_uint(__uint_as_float(dp0) * p.drop.inv_keep) : 0u;
+          dp1 = (km[hh] >> (j + 1)) & 1u ? __float_as_uint(__uint_as_float(dp1) * p.drop.inv_keep)
+                                         : 0u;
+        }
+        const uint64_t dp2 = f2_make(dp0, dp1);
+        // dS = P (dP - D); with a softcap (-P (1 - tanh^2)) (D - dP)
+        const uint64_t r2 =
+            f2_mul(pk[(hh * 32 + j) >> 1], SOFTCAP ? f2_sub(dd2[e2], dp2) : f2_sub(dp2, dd2[e2]));
+        raw[j] = static_cast<uint32_t>(r2);
+        raw[j + 1] = static_cast<uint32_t>(r2 >> 32);
       }
     }
 #pragma unroll
