@@ -1,33 +1,39 @@
 // attn_fwd: attention forward on sm_103a producing O and the natural-log
 // LSE the backward needs ("反向传播算法详解" §1.2-§1.3 saved tensors;
-// "解析 FlashAttention（3）" §1.1 forward).
+// "解析 FlashAttention（3）" §1.1 forward and §3.2 eq. 9-12, the running
+// (max, sum) statistics of the online softmax).
 //
-// One CTA owns a block of Bm = 128 queries of one query head and walks the
-// key blocks (Bn = 128 keys) its mask lets it see, in two passes:
-//   pass 1  S_j = Q K_j^T on the tensor cores; the softmax warps keep the
-//           running row maximum m and sum l of exp2 over S_j, which gives
-//           LSE exactly (in base 2: LSE2 = m + log2 l);
-//   pass 2  S_j again; P_j = exp2(S_j * tau*log2e - LSE2) is already
-//           normalised, goes to tensor memory as bf16 and O += P_j V_j
-//           accumulates there with no rescaling.
-// This spends one extra S GEMM per tile (three GEMMs instead of two) to keep
-// the O accumulator free of the running-max corrections of a one-pass
-// online softmax.
+// One CTA owns two blocks of 128 queries (tiles 0 and 1) of one query head
+// and walks, once, the key blocks (128 keys) their masks let them see. Per
+// key block j and tile q:
+//   S_q(j)  = Q_q K_j^T                          (tensor cores, fp32 in TMEM)
+//   m       = running row maximum of x = logit * log2e; the shift m_used is
+//             moved only when the maximum grows by more than kRescale (in
+//             log2 units), and then O_q and l are multiplied by
+//             2^(m_used_old - m_used_new)
+//   P_q(j)  = 2^(x - m_used) as bf16 pairs over the S buffer, l += sum P
+//   O_q    += P_q(j) V_j                         (P read from TMEM)
+// and at the end O = O_q / l, LSE = (m_used + log2 l) ln 2. The values of P
+// stay below 2^kRescale, so neither the bf16 P nor the fp32 O can overflow.
 //
-// Queries sit on the tensor-memory lanes: thread r of the softmax warpgroup
-// owns query row r, so row maxima and sums need no cross-thread reduction,
-// and P (bf16 pairs, keys along the columns) is the A operand of the PV GEMM
-// straight from tensor memory.
+// The two tiles ping-pong on the tensor cores: while the softmax of tile 0
+// works on S_0(j), the tensor cores run P_1(j-1) V and S_1(j), and the other
+// way round. K_j and V_j serve both tiles.
+//
+// Queries sit on the tensor-memory lanes: thread r of softmax warpgroup q
+// owns row r of tile q, so row maxima and sums need no cross-thread
+// reduction.
 //
 // Warp roles (384 threads):
-//   warp 0      TMA producer: Q once, K_j for every S GEMM, V_j in pass 2
-//               (two-stage rings)
+//   warp 0      TMA producer: Q_0, Q_1 once; K_j, V_j in two-stage rings
 //   warp 1      tcgen05 MMA issuer (whole warp, one elected lane issues)
-//   warps 4-11  softmax in two warpgroups, one per S buffer, then the
-//               epilogue (O -> bf16 -> shared -> TMA store; LSE)
+//   warps 4-7   softmax of tile 0, then its epilogue (O / l -> bf16 ->
+//               shared -> TMA store; LSE)
+//   warps 8-11  the same for tile 1
 //
-// Tensor memory (512 columns): S buffers at [0,128) and [128,256) (P
-// overwrites the first half of its buffer), O accumulator at [256, 256 + d).
+// Tensor memory (512 columns for d = 128): S buffers of tiles 0 and 1 at
+// [0,128) and [128,256) (P overwrites the first half of its buffer), O_0 at
+// [256, 256 + d), O_1 at [256 + d, 256 + 2d).
 // Every mbarrier wait is bounded, as in attn_bwd.
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -40,48 +46,50 @@ namespace fwdtc {
 
 using namespace ptx;
 
-constexpr int kBm = 128;  // queries per CTA (tensor-memory lanes)
-constexpr int kBn = 128;  // keys per tile
+constexpr int kBm = 128;  // queries per tile (tensor-memory lanes)
+constexpr int kBn = 128;  // keys per block
 constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescale = 8.f;  // move the shift only when the maximum grows by more
 constexpr long long kWaitLimitCycles = 2000000000LL;  // about one second
 
 template <int D>
 struct Layout {
   static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kQ = 0;  // also the O staging buffer at the end
-  static constexpr int kK0 = kQ + kTileBytes;
+  static constexpr int kQ0 = 0;  // Q of tile 0; its O staging buffer at the end
+  static constexpr int kQ1 = kQ0 + kTileBytes;
+  static constexpr int kK0 = kQ1 + kTileBytes;
   static constexpr int kK1 = kK0 + kTileBytes;
   static constexpr int kV0 = kK1 + kTileBytes;
   static constexpr int kV1 = kV0 + kTileBytes;
-  static constexpr int kStats = kV1 + kTileBytes;  // 2 x 128 rows x (m, l) fp32
-  static constexpr int kBars = kStats + 2 * 128 * 8;
-  static constexpr int kNumBars = 16;
+  static constexpr int kBars = kV1 + kTileBytes;
+  static constexpr int kNumBars = 17;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
-  // d = 64 needs 80 KB; it asks for more than half of the SM's shared memory
+  // d = 64 needs 96 KB; it asks for more than half of the SM's shared memory
   // so that a second CTA never waits on the first one's tensor memory
   static constexpr int kUsed = kAbort + 12;
   static constexpr int kBytes = kUsed > 120 * 1024 ? kUsed : 120 * 1024;
 };
+static_assert(Layout<128>::kBytes <= 232448, "shared memory budget");
 
 enum Bar {
-  BAR_Q_FULL = 0,
-  BAR_K_FULL = 1,    // + stage
-  BAR_K_EMPTY = 3,   // + stage
-  BAR_V_FULL = 5,    // + stage
-  BAR_V_EMPTY = 7,   // + stage
-  BAR_S_FULL = 9,    // + buffer
-  BAR_S_FREE = 11,   // + buffer: the softmax (pass 1) or the PV GEMM (pass 2) is done with it
-  BAR_P_FULL = 13,   // + buffer (pass 2 only)
-  BAR_O_DONE = 15,
+  BAR_Q_FULL = 0,    // + tile
+  BAR_K_FULL = 2,    // + stage
+  BAR_K_EMPTY = 4,   // + stage
+  BAR_V_FULL = 6,    // + stage
+  BAR_V_EMPTY = 8,   // + stage
+  BAR_S_FULL = 10,   // + tile: S_q(j) in its buffer
+  BAR_P_FULL = 12,   // + tile: P_q(j) written (and O_q rescaled if needed)
+  BAR_O_DONE = 14,   // + tile: P_q(j) V_j completed (one phase per key block of the tile)
+  BAR_DRAIN = 16,    // abort path only: completion of everything issued
 };
 
 struct Params {
   float* lse;
   int B, H, H_kv, N;
-  int m_blocks;
+  int pairs;  // CTAs per query head: ceil(query blocks / 2)
   float scale;
   float softcap;
   // visibility band: key j is visible to query i iff
@@ -130,10 +138,19 @@ __device__ __forceinline__ void wait_drain(const Ctx& c, int bar, uint32_t parit
   }
 }
 
-// Work of one CTA: query block m_block of head bh (= b * H + h), against
-// key blocks j0 .. j0 + nk - 1 (those holding a key of the rows' bands).
+// Work of one CTA: query tiles m0[0] = 256 * pair and m0[1] = m0[0] + 128
+// of head bh (= b * H + h). Tile q sees key blocks j0[q] .. j0[q] + nt[q] - 1
+// (nt[q] = 0: the tile lies past N); together they span jlo .. jhi.
 struct Work {
-  int bh, kvh, m_block, j0, nk;  // nk: key blocks visited (per pass)
+  int bh, kvh;
+  int m0[2], j0[2], nt[2];
+  int jlo, jhi;
+  __device__ __forceinline__ bool has(int q, int j) const {
+    return j >= j0[q] && j < j0[q] + nt[q];
+  }
+  __device__ __forceinline__ int uses(int j) const {
+    return (has(0, j) ? 1 : 0) + (has(1, j) ? 1 : 0);
+  }
 };
 
 __device__ __forceinline__ Work work_of(const Params& p) {
@@ -142,14 +159,26 @@ __device__ __forceinline__ Work work_of(const Params& p) {
   const int idx = static_cast<int>(blockIdx.x);
   // heaviest query blocks first for a causal mask (the last ones see the
   // most keys)
-  w.m_block = p.m_blocks - 1 - idx / heads;
+  const int pair = p.pairs - 1 - idx / heads;
   w.bh = idx - (idx / heads) * heads;
   const int b = w.bh / p.H, h = w.bh - b * p.H;
   w.kvh = b * p.H_kv + h / (p.H / p.H_kv);
-  const int m0 = w.m_block * kBm;
-  w.j0 = max(0, m0 - p.win_left) / kBn;
-  const int j_end = min((p.N + kBn - 1) / kBn - 1, (m0 + kBm - 1 + p.win_right) / kBn);
-  w.nk = j_end - w.j0 + 1;
+  const int last_block = (p.N + kBn - 1) / kBn - 1;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    w.m0[q] = pair * 2 * kBm + q * kBm;
+    if (w.m0[q] >= p.N) {
+      w.j0[q] = 0;
+      w.nt[q] = 0;
+      continue;
+    }
+    w.j0[q] = max(0, w.m0[q] - p.win_left) / kBn;
+    const int j_end = min(last_block, (w.m0[q] + kBm - 1 + p.win_right) / kBn);
+    w.nt[q] = j_end - w.j0[q] + 1;  // >= 1: the band holds the diagonal
+  }
+  // tile 1 starts and ends no earlier than tile 0, and their ranges touch
+  w.jlo = w.j0[0];
+  w.jhi = w.nt[1] > 0 ? w.j0[1] + w.nt[1] - 1 : w.j0[0] + w.nt[0] - 1;
   return w;
 }
 
@@ -165,292 +194,332 @@ __device__ void producer_role(const Ctx& c, const Work& w, uint32_t sbase, const
     prefetch_tmap(tq);
     prefetch_tmap(tk);
     prefetch_tmap(tv);
-    mbar_arrive_expect_tx(bar_addr(c, BAR_Q_FULL), kTileBytes);
-    for (int cb = 0; cb < kBoxes; ++cb)
-      tma_load_3d(sbase + L::kQ + cb * 16384, tq, bar_addr(c, BAR_Q_FULL), 64 * cb,
-                  w.m_block * kBm, w.bh);
+    for (int q = 0; q < 2; ++q) {
+      if (w.nt[q] == 0) continue;
+      mbar_arrive_expect_tx(bar_addr(c, BAR_Q_FULL + q), kTileBytes);
+      for (int cb = 0; cb < kBoxes; ++cb)
+        tma_load_3d(sbase + (q ? L::kQ1 : L::kQ0) + cb * 16384, tq, bar_addr(c, BAR_Q_FULL + q),
+                    64 * cb, w.m0[q], w.bh);
+    }
   }
   const uint64_t keep = policy_evict_last();  // K, V are read by every query block of the head
-  int issued_k = 0, issued_v = 0;
+  int issued = 0;
   bool ok = true;
-  for (int s = 0; s < 2 * w.nk; ++s) {
-    const bool pass2 = s >= w.nk;
-    const int j = pass2 ? s - w.nk : s;
-    const int ks = s & 1;
-    if (s >= 2 && !(ok = wait_warp(c, BAR_K_EMPTY + ks, ((s >> 1) - 1) & 1))) break;
+  for (int j = w.jlo; j <= w.jhi; ++j) {
+    const int kb = j - w.jlo, st = kb & 1;
+    const uint32_t ph = ((kb >> 1) - 1) & 1;
+    if (kb >= 2 && !(ok = wait_warp(c, BAR_K_EMPTY + st, ph))) break;
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar_addr(c, BAR_K_FULL + ks), kTileBytes);
-      const uint32_t dst = sbase + (ks ? L::kK1 : L::kK0);
+      mbar_arrive_expect_tx(bar_addr(c, BAR_K_FULL + st), kTileBytes);
       for (int cb = 0; cb < kBoxes; ++cb)
-        tma_load_3d_hint(dst + cb * 16384, tk, bar_addr(c, BAR_K_FULL + ks), 64 * cb,
-                         (w.j0 + j) * kBn, w.kvh, keep);
+        tma_load_3d_hint(sbase + (st ? L::kK1 : L::kK0) + cb * 16384, tk,
+                         bar_addr(c, BAR_K_FULL + st), 64 * cb, j * kBn, w.kvh, keep);
     }
-    issued_k = s + 1;
-    if (pass2) {
-      const int vs = j & 1;
-      if (j >= 2 && !(ok = wait_warp(c, BAR_V_EMPTY + vs, ((j >> 1) - 1) & 1))) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar_addr(c, BAR_V_FULL + vs), kTileBytes);
-        const uint32_t dst = sbase + (vs ? L::kV1 : L::kV0);
-        for (int cb = 0; cb < kBoxes; ++cb)
-          tma_load_3d_hint(dst + cb * 16384, tv, bar_addr(c, BAR_V_FULL + vs), 64 * cb,
-                           (w.j0 + j) * kBn, w.kvh, keep);
-      }
-      issued_v = j + 1;
+    if (kb >= 2 && !(ok = wait_warp(c, BAR_V_EMPTY + st, ph))) {
+      issued = 2 * kb + 1;
+      break;
     }
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_addr(c, BAR_V_FULL + st), kTileBytes);
+      for (int cb = 0; cb < kBoxes; ++cb)
+        tma_load_3d_hint(sbase + (st ? L::kV1 : L::kV0) + cb * 16384, tv,
+                         bar_addr(c, BAR_V_FULL + st), 64 * cb, j * kBn, w.kvh, keep);
+    }
+    issued = 2 * kb + 2;
     __syncwarp();
   }
   // When aborting, the copies in flight must land before the CTA exits.
   if (!ok || *c.abort) {
-    wait_drain(c, BAR_Q_FULL, 0);
-    for (int s = issued_k - 2 < 0 ? 0 : issued_k - 2; s < issued_k; ++s)
-      wait_drain(c, BAR_K_FULL + (s & 1), (s >> 1) & 1);
-    for (int j = issued_v - 2 < 0 ? 0 : issued_v - 2; j < issued_v; ++j)
-      wait_drain(c, BAR_V_FULL + (j & 1), (j >> 1) & 1);
+    for (int q = 0; q < 2; ++q)
+      if (w.nt[q] > 0) wait_drain(c, BAR_Q_FULL + q, 0);
+    // issued counts K and V loads in order K_0, V_0, K_1, V_1, ...
+    const int first = issued - 4 < 0 ? 0 : issued - 4;
+    for (int i = first; i < issued; ++i) {
+      const int kb = i >> 1;
+      wait_drain(c, ((i & 1) ? BAR_V_FULL : BAR_K_FULL) + (kb & 1), (kb >> 1) & 1);
+    }
   }
 }
 
-// P_FULL + w keeps one phase per pass-2 tile of buffer w.
-__device__ __forceinline__ uint32_t p_phase(int s, int nk) {
-  const int first = ((nk & 1) == (s & 1)) ? nk : nk + 1;  // first pass-2 tile of this buffer
-  return static_cast<uint32_t>(((s - first) >> 1) & 1);
-}
-
 // ------------------------------------------------------------------ MMA issuer
-// S GEMM s (s < nk: pass 1, else pass 2 over the same key blocks) goes to
-// buffer s & 1 once the previous use of that buffer has been released; in
-// pass 2, O += P V follows each P. Every barrier keeps one phase per use.
+// Issue order: S_0(first), S_1(first), then for every key block j and tile q
+// that sees it: P_q(j) V_j, then S_q(j + 1). S_q(j + 1) overwrites the S
+// buffer holding P_q(j) only after P_q(j) V_j, which reads it (tcgen05 MMAs of
+// one thread run in issue order). K_j and V_j stages are released after their
+// last use by either tile.
 template <int D>
 __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t tmem) {
   using L = Layout<D>;
   const bool leader = elect_one_sync() != 0;
   constexpr uint32_t kIdS = make_idesc_bf16(kBm, kBn, false, false);  // S = Q K^T
   constexpr uint32_t kIdO = make_idesc_bf16(kBm, D, false, true);     // O += P V
-  const uint32_t q_lo = sdesc_lo(sbase + L::kQ, 16);
-  const uint32_t k_lo0 = sdesc_lo(sbase + L::kK0, 16), k_lo1 = sdesc_lo(sbase + L::kK1, 16);
-  const uint32_t v_mn0 = sdesc_lo(sbase + L::kV0, 16384), v_mn1 = sdesc_lo(sbase + L::kV1, 16384);
-  const uint32_t tO = tmem + 256;
+  const uint32_t q_lo[2] = {sdesc_lo(sbase + L::kQ0, 16), sdesc_lo(sbase + L::kQ1, 16)};
+  const uint32_t k_lo[2] = {sdesc_lo(sbase + L::kK0, 16), sdesc_lo(sbase + L::kK1, 16)};
+  const uint32_t v_mn[2] = {sdesc_lo(sbase + L::kV0, 16384), sdesc_lo(sbase + L::kV1, 16384)};
   auto kmaj = [](int k) { return static_cast<uint32_t>(((k >> 2) * 16384 + (k & 3) * 32) >> 4); };
   auto mnmaj = [](int k) { return static_cast<uint32_t>((2048 * k) >> 4); };
-  const int total = 2 * w.nk;
-  bool ok = wait_warp(c, BAR_Q_FULL, 0);
-  auto issue_s = [&](int s) -> bool {
-    const int b = s & 1;
-    if (!wait_warp(c, BAR_K_FULL + b, (s >> 1) & 1)) return false;
-    if (s >= 2 && !wait_warp(c, BAR_S_FREE + b, ((s >> 1) - 1) & 1)) return false;
+  // uses of the K / V block each stage holds that are still to be issued
+  int k_left[2] = {0, 0}, v_left[2] = {0, 0}, k_blk[2] = {-1, -1}, v_blk[2] = {-1, -1};
+  bool ok = true;
+
+  auto issue_s = [&](int q, int j) -> bool {
+    const int kb = j - w.jlo, st = kb & 1;
+    if (!wait_warp(c, BAR_K_FULL + st, (kb >> 1) & 1)) return false;
+    if (k_blk[st] != j) {
+      k_blk[st] = j;
+      k_left[st] = w.uses(j);
+    }
     tc_fence_after();
     if (leader) {
-      const uint32_t kb = b ? k_lo1 : k_lo0;
 #pragma unroll
       for (int k = 0; k < D / 16; ++k)
-        mma_ss(tmem + b * 128, sdesc_from_lo(q_lo + kmaj(k)), sdesc_from_lo(kb + kmaj(k)), kIdS,
-               k > 0);
-      mma_commit(bar_addr(c, BAR_S_FULL + b));
-      mma_commit(bar_addr(c, BAR_K_EMPTY + b));
+        mma_ss(tmem + q * 128, sdesc_from_lo(q_lo[q] + kmaj(k)), sdesc_from_lo(k_lo[st] + kmaj(k)),
+               kIdS, k > 0);
+      mma_commit(bar_addr(c, BAR_S_FULL + q));
+      if (k_left[st] == 1) mma_commit(bar_addr(c, BAR_K_EMPTY + st));
     }
+    --k_left[st];
     return true;
   };
-  if (ok) ok = issue_s(0);
-  for (int s = 0; ok && s < total; ++s) {
-    if (s + 1 < total && !(ok = issue_s(s + 1))) break;
-    if (s >= w.nk) {
-      const int j = s - w.nk, b = s & 1, vs = j & 1;
-      if (!(ok = wait_warp(c, BAR_P_FULL + b, p_phase(s, w.nk)))) break;
-      if (!(ok = wait_warp(c, BAR_V_FULL + vs, (j >> 1) & 1))) break;
+
+  for (int q = 0; q < 2 && ok; ++q) {
+    if (w.nt[q] == 0) continue;
+    if (!(ok = wait_warp(c, BAR_Q_FULL + q, 0))) break;
+    ok = issue_s(q, w.j0[q]);
+  }
+  for (int j = w.jlo; ok && j <= w.jhi; ++j) {
+    const int kb = j - w.jlo, st = kb & 1;
+    for (int q = 0; q < 2; ++q) {
+      if (!w.has(q, j)) continue;
+      const int t = j - w.j0[q];
+      if (!(ok = wait_warp(c, BAR_P_FULL + q, t & 1))) break;
+      if (!(ok = wait_warp(c, BAR_V_FULL + st, (kb >> 1) & 1))) break;
+      if (v_blk[st] != j) {
+        v_blk[st] = j;
+        v_left[st] = w.uses(j);
+      }
       tc_fence_after();
       if (leader) {
-        const uint32_t vb = vs ? v_mn1 : v_mn0;
-        // A = P (bf16 pairs, keys along columns 8k .. of buffer b)
+        // A = P (bf16 pairs, keys along columns 8k .. of the tile's S buffer)
 #pragma unroll
         for (int k = 0; k < kBn / 16; ++k)
-          mma_ts(tO, tmem + b * 128 + 8 * k, sdesc_from_lo(vb + mnmaj(k)), kIdO,
-                 (j > 0 || k > 0) ? 1u : 0u);
-        mma_commit(bar_addr(c, BAR_S_FREE + b));
-        mma_commit(bar_addr(c, BAR_V_EMPTY + vs));
+          mma_ts(tmem + 256 + q * D, tmem + q * 128 + 8 * k, sdesc_from_lo(v_mn[st] + mnmaj(k)),
+                 kIdO, (t > 0 || k > 0) ? 1u : 0u);
+        mma_commit(bar_addr(c, BAR_O_DONE + q));
+        if (v_left[st] == 1) mma_commit(bar_addr(c, BAR_V_EMPTY + st));
       }
+      --v_left[st];
+      if (w.has(q, j + 1) && !(ok = issue_s(q, j + 1))) break;
     }
   }
-  // O complete (or, when aborting, everything issued complete)
-  if (leader) mma_commit(bar_addr(c, BAR_O_DONE));
-  if (__any_sync(0xffffffffu, !ok || *c.abort != 0)) wait_drain(c, BAR_O_DONE, 0);
+  if (__any_sync(0xffffffffu, !ok || *c.abort != 0)) {
+    // completion of everything issued before tensor memory is released
+    if (leader) mma_commit(bar_addr(c, BAR_DRAIN));
+    wait_drain(c, BAR_DRAIN, 0);
+  }
   __syncwarp();
 }
 
 // ------------------------------------------------------------------ softmax
-// One S tile of one query row (this thread's tensor-memory lane), in four
-// 32-key chunks. Pass 1 (PASS2 false) folds the chunk into the running
-// maximum m and sum l of 2^x; pass 2 writes P = 2^(x - lse2) as bf16 pairs
-// over the first half of the S buffer. MASKED tiles (the band's edges, the
-// sequence's end) hide invisible keys with -inf; the others skip the test.
-template <bool SOFTCAP, bool MASKED, bool PASS2>
-__device__ __forceinline__ void tile_rows(const Params& p, uint32_t tS, int n0, int q,
-                                          float c_log2, float cap_in, float cap_out, float& m,
-                                          float& l, float lse2) {
+// Row maximum of one S tile (raw scores; with tau > 0 the logit grows with
+// the score, softcap included). MASKED tiles (a band's edge, the sequence's
+// end) leave invisible keys out.
+template <bool MASKED>
+__device__ __forceinline__ float tile_max(const Params& p, uint32_t tS, int n0, int qrow) {
+  float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
   for (int ch = 0; ch < kBn / 32; ++ch) {
     uint32_t raw[32];
     tmem_ld32(tS + ch * 32, raw);
-    float cm0 = -INFINITY, cm1 = -INFINITY;
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-      const float sv = __uint_as_float(raw[e]);
-      float x;
-      if (SOFTCAP) {
-        // tanh(u) = 1 - 2 / (exp(2u) + 1) with u = tau s / c
-        const float ex = ex2_approx(sv * cap_in);
-        x = (1.f - 2.f * rcp_approx(ex + 1.f)) * cap_out;
-      } else {
-        x = sv * c_log2;
-      }
+      float s = __uint_as_float(raw[e]);
       if (MASKED) {
         const int key = n0 + ch * 32 + e;
-        if (!(key < p.N && key - q <= p.win_right && q - key <= p.win_left)) x = -INFINITY;
+        if (!(key < p.N && key - qrow <= p.win_right && qrow - key <= p.win_left)) s = -INFINITY;
       }
-      raw[e] = __float_as_uint(x);
-      if (!PASS2) {
-        if (e & 1)
-          cm1 = fmaxf(cm1, x);
-        else
-          cm0 = fmaxf(cm0, x);
-      }
-    }
-    if (!PASS2) {
-      const float mn = fmaxf(m, fmaxf(cm0, cm1));
-      // only a masked chunk (a window's edge, a padding row) can hold no
-      // visible key; the shift then stays finite so that -inf - -inf never
-      // arises (the exponentials of -inf are 0)
-      const float sh = (MASKED && mn == -INFINITY) ? 0.f : mn;
-      float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int e = 0; e < 32; ++e) s4[e & 3] += ex2_approx(__uint_as_float(raw[e]) - sh);
-      l = l * ex2_approx(m - sh) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
-      m = mn;
-    } else {
-      uint32_t packed[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u)
-        packed[u] = pack_bf16x2(ex2_approx(__uint_as_float(raw[2 * u]) - lse2),
-                                ex2_approx(__uint_as_float(raw[2 * u + 1]) - lse2));
-      // keys 32 ch .. 32 ch + 31 -> columns 16 ch .. 16 ch + 15, whose S
-      // values were read in this or an earlier chunk
-      tmem_st16(tS + ch * 16, packed);
+      if (e & 1)
+        m1 = fmaxf(m1, s);
+      else
+        m0 = fmaxf(m0, s);
     }
   }
+  return fmaxf(m0, m1);
 }
 
-// Two warpgroups; warpgroup w takes the S GEMMs s with s & 1 == w, i.e. S
-// buffer w, so each processes one tile while the other's S GEMM runs.
-// Thread = query row r (tensor-memory lane). Pass 1 keeps the running
-// maximum m and sum l of 2^x over the row (x = logit * log2e) for the
-// warpgroup's key blocks; the two partial statistics are combined through
-// shared memory into LSE2 at the pass boundary. Pass 2 writes
-// P = 2^(x - LSE2) as bf16 pairs over the first half of the S buffer, which
-// the PV GEMM reads as its A operand. Then each warpgroup stores half of the
-// columns of O.
+// P = 2^(x - shift) of one S tile as bf16 pairs over the first half of the
+// buffer; returns the row sum of P (fp32, before rounding). Keys
+// 32 ch .. 32 ch + 31 land in columns 16 ch .. 16 ch + 15, whose S values
+// were read in this or an earlier chunk.
+template <bool SOFTCAP, bool MASKED>
+__device__ __forceinline__ float tile_p(const Params& p, uint32_t tS, int n0, int qrow,
+                                        float c_log2, float cap_in, float cap_out, float shift) {
+  const uint64_t c2 = f2_make(SOFTCAP ? cap_in : c_log2, SOFTCAP ? cap_in : c_log2);
+  const uint64_t out2 = f2_make(cap_out, cap_out);
+  const uint64_t one2 = f2_make(1.f, 1.f), mtwo2 = f2_make(-2.f, -2.f);
+  const uint64_t nsh2 = f2_make(-shift, -shift);
+  uint64_t sum2 = f2_make(0.f, 0.f);
+#pragma unroll
+  for (int ch = 0; ch < kBn / 32; ++ch) {
+    uint32_t raw[32];
+    tmem_ld32(tS + ch * 32, raw);
+    uint32_t packed[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const uint64_t s2 = f2_make(raw[2 * u], raw[2 * u + 1]);
+      uint64_t y2;
+      if (SOFTCAP) {
+        // tanh(v) = 1 - 2 / (exp(2v) + 1) with v = tau s / c
+        const uint64_t v2 = f2_mul(s2, c2);
+        const uint64_t e1 = f2_add(f2_make(ex2_approx(f2_lo(v2)), ex2_approx(f2_hi(v2))), one2);
+        const uint64_t th2 =
+            f2_fma(f2_make(rcp_approx(f2_lo(e1)), rcp_approx(f2_hi(e1))), mtwo2, one2);
+        y2 = f2_fma(th2, out2, nsh2);
+      } else {
+        y2 = f2_fma(s2, c2, nsh2);
+      }
+      float y0 = f2_lo(y2), y1 = f2_hi(y2);
+      if (MASKED) {
+        const int key = n0 + ch * 32 + 2 * u;
+        if (!(key < p.N && key - qrow <= p.win_right && qrow - key <= p.win_left)) y0 = -INFINITY;
+        if (!(key + 1 < p.N && key + 1 - qrow <= p.win_right && qrow - key - 1 <= p.win_left))
+          y1 = -INFINITY;
+      }
+      const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+      sum2 = f2_add(sum2, f2_make(p0, p1));
+      packed[u] = pack_bf16x2(p0, p1);
+    }
+    tmem_st16(tS + ch * 16, packed);
+  }
+  return f2_lo(sum2) + f2_hi(sum2);
+}
+
+// Softmax warpgroup q (thread = query row r of tile q): per key block, the
+// row maximum, the shift update (with the rescale of O_q and l when the shift
+// moves), and P; then the epilogue of the tile.
 template <int D, bool SOFTCAP>
-__device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8_t* smem,
-                             uint32_t sbase, uint32_t tmem, const CUtensorMap* to) {
+__device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint32_t sbase,
+                             uint32_t tmem, const CUtensorMap* to) {
   using L = Layout<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int wg = (warp - 4) >> 2;  // 0 or 1: the S buffer this warpgroup owns
+  const int q = (warp - 4) >> 2;  // the tile this warpgroup owns
   const int r = ((warp & 3) << 5) + lane;
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
-  const int q = w.m_block * kBm + r;
-  const int bar_wg = 1 + wg;  // named barrier of this warpgroup (128 threads)
+  const uint32_t tS = tmem + lane_base + q * 128;
+  const uint32_t tO = tmem + lane_base + 256 + q * D;
+  const int qrow = w.m0[q] + r;
+  const int bar_wg = 1 + q;  // named barrier of this warpgroup (128 threads)
   const float c_log2 = p.scale * kLog2e;
   const float cap_in = SOFTCAP ? 2.f * kLog2e * p.scale / p.softcap : 0.f;  // 2 log2e tau/c
   const float cap_out = SOFTCAP ? p.softcap * kLog2e : 0.f;                 // c log2e
-  float m = -INFINITY, l = 0.f, lse2 = 0.f;
+  const int nt = w.nt[q];
+  if (nt == 0) return;
+  float m_used = -INFINITY, l = 0.f;
   bool ok = true;
-  const uint32_t tS = tmem + lane_base + wg * 128;
-  // Both warpgroups pass the same sequence of named-barrier-3 operations on
-  // every path (the votes below), so an abort can never strand one of them.
-  auto tile = [&](int s) -> bool {
-    const bool pass2 = s >= w.nk;
-    const int j = pass2 ? s - w.nk : s;
+  for (int t = 0; t < nt; ++t) {
+    const int n0 = (w.j0[q] + t) * kBn;
+    const int m0 = w.m0[q];
     // the warpgroup meets at its named barrier below: one decision for all
-    ok = named_bar_and(bar_wg, 128, wait(c, BAR_S_FULL + wg, (s >> 1) & 1));
-    if (!ok) return false;
+    ok = named_bar_and(bar_wg, 128, wait(c, BAR_S_FULL + q, t & 1));
+    if (!ok) break;
     tc_fence_after();
-    const int n0 = (w.j0 + j) * kBn;
-    const int m0 = w.m_block * kBm;
-    const bool masked = n0 + kBn - 1 - m0 > p.win_right || m0 + kBm - 1 - n0 > p.win_left ||
-                        n0 + kBn > p.N;
-    if (pass2) {
-      if (masked)
-        tile_rows<SOFTCAP, true, true>(p, tS, n0, q, c_log2, cap_in, cap_out, m, l, lse2);
-      else
-        tile_rows<SOFTCAP, false, true>(p, tS, n0, q, c_log2, cap_in, cap_out, m, l, lse2);
-    } else {
-      if (masked)
-        tile_rows<SOFTCAP, true, false>(p, tS, n0, q, c_log2, cap_in, cap_out, m, l, lse2);
-      else
-        tile_rows<SOFTCAP, false, false>(p, tS, n0, q, c_log2, cap_in, cap_out, m, l, lse2);
+    const bool masked =
+        n0 + kBn - 1 - m0 > p.win_right || m0 + kBm - 1 - n0 > p.win_left || n0 + kBn > p.N;
+    const float smax = masked ? tile_max<true>(p, tS, n0, qrow) : tile_max<false>(p, tS, n0, qrow);
+    float m_tile = -INFINITY;  // row maximum of x = logit * log2e over this block
+    if (smax > -INFINITY) {
+      if (SOFTCAP) {
+        const float ex = ex2_approx(smax * cap_in);
+        m_tile = (1.f - 2.f * rcp_approx(ex + 1.f)) * cap_out;
+      } else {
+        m_tile = smax * c_log2;
+      }
     }
-    if (!pass2) {
-      // the buffer is free for the next S GEMM once every row has read it
-      tc_fence_before();
-      named_bar_sync(bar_wg, 128);
-      if (r == 0) mbar_arrive(bar_addr(c, BAR_S_FREE + wg));
-    } else {
-      tmem_wait_st();
-      tc_fence_before();
-      named_bar_sync(bar_wg, 128);
-      if (r == 0) mbar_arrive(bar_addr(c, BAR_P_FULL + wg));
-    }
-    return true;
-  };
-  // pass 1 over this warpgroup's key blocks
-  for (int s = wg; ok && s < w.nk; s += 2) ok = tile(s);
-  // combine the two warpgroups' row statistics (one without pass-1 tiles
-  // has m = -inf, l = 0)
-  ok = named_bar_and(3, 256, ok);
-  if (ok) {
-    float* st = reinterpret_cast<float*>(smem + L::kStats);
-    st[(wg * 128 + r) * 2] = m;
-    st[(wg * 128 + r) * 2 + 1] = l;
-    named_bar_sync(3, 256);
-    const float mo = st[((1 - wg) * 128 + r) * 2], lo = st[((1 - wg) * 128 + r) * 2 + 1];
-    const float mx = fmaxf(m, mo);
-    const float sh = mx == -INFINITY ? 0.f : mx;
-    lse2 = sh + __log2f(l * ex2_approx(m - sh) + lo * ex2_approx(mo - sh));
-    // a padding row past N may see no key at all: its P must be 0, not NaN
-    if (!(lse2 < INFINITY && lse2 > -INFINITY)) lse2 = INFINITY;
-  }
-  // pass 2
-  for (int s = ((w.nk & 1) == wg) ? w.nk : w.nk + 1; ok && s < 2 * w.nk; s += 2) ok = tile(s);
-  // ---- epilogue: O (already normalised) -> bf16 rows in the Q buffer (free
-  // once every GEMM is done) -> TMA tensor store; LSE in natural log.
-  // Warpgroup wg takes columns [wg * D/2, (wg + 1) * D/2) of every row.
-  if (ok) ok = wait(c, BAR_O_DONE, 0);
-  if (!named_bar_and(3, 256, ok)) return;  // both warpgroups reach this vote on every path
-  tc_fence_after();
+    // move the shift when the maximum outgrows it by more than kRescale
+    const bool need = m_tile > m_used + kRescale;
+    if (__any_sync(0xffffffffu, need)) {
+      const float m_new = need ? m_tile : m_used;
+      const float f = need ? ex2_approx(m_used - m_new) : 1.f;  // 0 while m_used = -inf
+      // O_q holds a nonzero row only once the shift is finite; P_q(t - 1) V
+      // must have completed before the row is read
+      if (__any_sync(0xffffffffu, need && m_used > -INFINITY) && t > 0) {
+        if (!wait_warp(c, BAR_O_DONE + q, (t - 1) & 1)) ok = false;
+        if (ok) {
+          tc_fence_after();
+          const uint64_t f2 = f2_make(f, f);
 #pragma unroll
-  for (int c16 = 0; c16 < D / 32; ++c16) {
-    const int col = wg * (D / 2) + c16 * 16;
+          for (int c32 = 0; c32 < D / 32; ++c32) {
+            uint32_t o[32];
+            tmem_ld32(tO + c32 * 32, o);
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const uint64_t v = f2_mul(f2_make(o[2 * u], o[2 * u + 1]), f2);
+              o[2 * u] = static_cast<uint32_t>(v);
+              o[2 * u + 1] = static_cast<uint32_t>(v >> 32);
+            }
+            uint32_t lo[16], hi[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              lo[u] = o[u];
+              hi[u] = o[16 + u];
+            }
+            tmem_st16(tO + c32 * 32, lo);
+            tmem_st16(tO + c32 * 32 + 16, hi);
+          }
+        }
+      }
+      l *= f;
+      m_used = m_new;
+    }
+    ok = named_bar_and(bar_wg, 128, ok);
+    if (!ok) break;
+    const float shift = m_used > -INFINITY ? m_used : 0.f;
+    l += masked ? tile_p<SOFTCAP, true>(p, tS, n0, qrow, c_log2, cap_in, cap_out, shift)
+                : tile_p<SOFTCAP, false>(p, tS, n0, qrow, c_log2, cap_in, cap_out, shift);
+    tmem_wait_st();
+    tc_fence_before();
+    named_bar_sync(bar_wg, 128);
+    if (r == 0) mbar_arrive(bar_addr(c, BAR_P_FULL + q));
+  }
+  // ---- epilogue: O / l -> bf16 rows in the tile's Q buffer (free once its
+  // last S GEMM is done, which precedes the last P V) -> TMA tensor store;
+  // LSE in natural log
+  if (ok) ok = wait(c, BAR_O_DONE + q, (nt - 1) & 1);
+  if (!named_bar_and(bar_wg, 128, ok)) return;
+  tc_fence_after();
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const uint64_t inv2 = f2_make(inv, inv);
+  const uint32_t buf = sbase + (q ? L::kQ1 : L::kQ0);
+#pragma unroll
+  for (int c16 = 0; c16 < D / 16; ++c16) {
+    const int col = c16 * 16;
     uint32_t raw[16];
-    tmem_ld16(tmem + lane_base + 256 + col, raw);
+    tmem_ld16(tO + col, raw);
     uint32_t packed[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      packed[u] = pack_bf16x2(__uint_as_float(raw[2 * u]), __uint_as_float(raw[2 * u + 1]));
+    for (int u = 0; u < 8; ++u) {
+      const uint64_t v = f2_mul(f2_make(raw[2 * u], raw[2 * u + 1]), inv2);
+      packed[u] = pack_bf16x2(f2_lo(v), f2_hi(v));
+    }
     // columns col .. col + 15: box col / 64, 16-byte chunks (col % 64) / 8, + 1
-    const uint32_t row_addr = sbase + L::kQ + (col >> 6) * 16384 + r * 128;
+    const uint32_t row_addr = buf + (col >> 6) * 16384 + r * 128;
     const int c0 = (col & 63) >> 3;
     st_shared_v4(row_addr + ((c0 ^ (r & 7)) << 4), packed[0], packed[1], packed[2], packed[3]);
     st_shared_v4(row_addr + (((c0 + 1) ^ (r & 7)) << 4), packed[4], packed[5], packed[6],
                  packed[7]);
   }
   fence_proxy_async_smem();
-  named_bar_sync(3, 256);
-  if (wg == 0 && r == 0) {
+  named_bar_sync(bar_wg, 128);
+  if (r == 0) {
     for (int cb = 0; cb < D / 64; ++cb)
-      tma_store_3d(to, sbase + L::kQ + cb * 16384, 64 * cb, w.m_block * kBm, w.bh);
+      tma_store_3d(to, buf + cb * 16384, 64 * cb, w.m0[q], w.bh);
     bulk_commit_group();
     bulk_wait_all();
   }
-  if (wg == 0 && q < p.N) p.lse[static_cast<long long>(w.bh) * p.N + q] = lse2 * kLn2;
+  if (qrow < p.N)
+    p.lse[static_cast<long long>(w.bh) * p.N + qrow] =
+        l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -490,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     mma_role<D>(c, w, sbase, tmem);
   } else if (warp >= 4) {
-    softmax_role<D, SOFTCAP>(c, p, w, smem, sbase, tmem, &tm_o);
+    softmax_role<D, SOFTCAP>(c, p, w, sbase, tmem, &tm_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -511,7 +580,7 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
       return ATTN_ERR_LAUNCH;
     configured = true;
   }
-  const long long grid = static_cast<long long>(p.m_blocks) * p.B * p.H;
+  const long long grid = static_cast<long long>(p.pairs) * p.B * p.H;
   if (grid > 0x7fffffffLL) return ATTN_ERR_TOO_LARGE;
   kern<<<static_cast<unsigned>(grid), kThreads, Layout<D>::kBytes, stream>>>(tq, tk, tv, to, p);
   return launch_status();
@@ -547,7 +616,8 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
   int rc = check_shape(B, H, H_kv, N, d);
   if (rc != ATTN_OK) return rc;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-  if (!std::isfinite(scale) || scale == 0.f || std::isnan(softcap)) return ATTN_ERR_SHAPE;
+  // tau > 0: the kernel takes a row's largest logit at its largest score
+  if (!std::isfinite(scale) || !(scale > 0.f) || std::isnan(softcap)) return ATTN_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_ALIGN;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
@@ -562,7 +632,7 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
   p.H = H;
   p.H_kv = H_kv;
   p.N = N;
-  p.m_blocks = (N + kBm - 1) / kBm;
+  p.pairs = ((N + kBm - 1) / kBm + 1) / 2;
   p.scale = scale;
   const bool cap = softcap > 0.f;
   p.softcap = cap ? softcap : 0.f;

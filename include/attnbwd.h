@@ -98,11 +98,13 @@ int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* o,
 
 /*
  * attn_fwd: the same forward as attn_fwd_ref (same arguments, outputs and
- * layouts) on the tcgen05 tensor cores: one CTA per 128 queries of a query
- * head walks the visible key blocks twice, first for the exact row statistics
- * (LSE), then for O = P V with P = exp(S - LSE) already normalised
- * ([bwd-detail] §1.2; [FA-v1-bwd] §1.1 forward). S and O accumulate in fp32;
- * P enters the PV GEMM as bf16. d must be 64 or 128.
+ * layouts) on the tcgen05 tensor cores, in one pass with the online softmax
+ * ([bwd-detail] §1.2; [FA-v1-bwd] §1.1 forward, §3.2 eq. 9-12 running
+ * statistics): one CTA takes two blocks of 128 queries of a query head and
+ * walks the visible key blocks once; O accumulates un-normalised in fp32
+ * tensor memory, rescaled only when a row maximum grows by more than 2^8,
+ * and is divided by the row sum at the end. P enters the PV GEMM as bf16.
+ * d must be 64 or 128, and scale must be > 0 (ATTN_ERR_SHAPE otherwise).
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
              int H_kv, int N, int d, float scale, int causal, float softcap, void* stream);

@@ -87,6 +87,21 @@ def test_other_entry_points_validation(lib):
         assert fwd(a, a, a, a, a, 1, 4, 3, 64, 64, 0.1, 0, 0.0) == lib.ATTN_ERR_SHAPE
         assert fwd(a, a, a, a + 4, a, 1, 1, 1, 64, 64, 0.1, 0, 0.0) == lib.ATTN_ERR_ALIGN
         assert fwd(a, a, a, a, a, 1, 0, 1, 64, 64, 0.1, 0, 0.0) == lib.ATTN_OK
+    # the tensor-core forward takes tau > 0; the fp32 forward any finite nonzero tau
+    assert lib.attn_fwd(a, a, a, a, a, 1, 1, 1, 64, 64, -0.1, 0, 0.0) == lib.ATTN_ERR_SHAPE
+    assert lib.attn_fwd_local(a, a, a, a, a, 1, 1, 1, 64, 64, -0.1, 0, 0.0, 8, 8) == \
+        lib.ATTN_ERR_SHAPE
+    assert lib.attn_fwd_ref(a, a, a, a, a, 1, 0, 1, 64, 64, -0.1, 0, 0.0) == lib.ATTN_OK
+    for fn in (lib.attn_fwd_local, lib.attn_fwd_ref_local):
+        assert fn(0, a, a, a, a, 1, 1, 1, 64, 64, 0.1, 0, 0.0, 8, 8) == lib.ATTN_ERR_NULL
+        assert fn(a, a, a, a, a, 1, 1, 1, 64, 96, 0.1, 0, 0.0, 8, 8) == lib.ATTN_ERR_UNSUPPORTED
+        assert fn(a, a, a, a, a, 1, 0, 1, 64, 64, 0.1, 1, 0.0, 8, -1) == lib.ATTN_OK
+    ok9 = (a, a, a, a, a, a, a, a, a)
+    assert lib.attn_bwd_local(0, *ok9[1:], 1, 2, 2, 128, 128, 0.1, 1, 0.0, a, 64, -1) == \
+        lib.ATTN_ERR_NULL
+    assert lib.attn_bwd_local(*ok9, 1, 2, 2, 128, 96, 0.1, 1, 0.0, a, 64, -1) == \
+        lib.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_bwd_local(*ok9, 0, 2, 2, 128, 128, 0.1, 1, 0.0, a, 64, -1) == lib.ATTN_OK
     assert lib.attn_fwd_ref(0, a, a, a, a, 1, 1, 1, 64, 64, 0.1, 0, 0.0) == lib.ATTN_ERR_NULL
     assert lib.attn_fwd_ref(a, a, a, a, a, 1, 1, 1, 64, 80, 0.1, 0, 0.0) == lib.ATTN_ERR_UNSUPPORTED
     assert lib.attn_fwd_ref(a, a, a, a, a, 1, 4, 3, 64, 64, 0.1, 0, 0.0) == lib.ATTN_ERR_SHAPE
