@@ -12,10 +12,19 @@ from oracle import attention_backward, attention_forward
 GRAD_MAX_REL = 2e-2    # max |err| / max |ref| for dQ, dK, dV
 GRAD_FRO_REL = 5e-3    # ||err||_F / ||ref||_F for dQ, dK, dV
 O_MAX_REL = 2e-2       # forward O, max |err| / max |ref|
-LSE_ABS = 1e-5         # forward LSE, max |err|
+LSE_ABS = 1e-5         # forward LSE, max |err| (for |LSE| <= LSE_SCALE_FROM)
+# fp32 scores resolve a logit of size |x| only to a few ulps of |x|; beyond
+# |LSE| = 16 (the five workloads stay below it) the LSE bound keeps the same
+# number of ulps, i.e. grows with |LSE| / 16.
+LSE_SCALE_FROM = 16.0
 # Where the exact gradient vanishes (e.g. a single key: P = 1 so dS = 0), a
 # relative error is undefined; errors are then measured against this floor.
 REF_FLOOR = 1e-4
+
+
+def lse_tol(lse_ref):
+    """LSE_ABS, widened in proportion to |LSE| past LSE_SCALE_FROM."""
+    return LSE_ABS * max(1.0, float(np.abs(lse_ref).max()) / LSE_SCALE_FROM)
 
 
 def run_gpu(w, x=None):
