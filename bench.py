@@ -401,7 +401,75 @@ def all_configs(dev, peak, iters=20, warmup=3):
         del x, q, k, v, do, o, lse, bufs
         torch.cuda.empty_cache()
     out["causal_gqa_window1024"] = local_window_timing(dev, peak, iters, warmup)
+    out["causal_gqa_variants"] = variant_timing(dev, peak, iters, warmup)
     return out
+
+
+def variant_timing(dev, peak, iters, warmup, p_drop=0.1, seed=1234):
+    """The deterministic-dQ step (preprocess + attn_bwd_deterministic +
+    attn_bwd_finalize_partials) and attn_bwd_dropout on the causal GQA
+    workload, against the plain step; FLOPs as for the plain backward."""
+    import flashattention_attention_backward_gb300 as attn
+    from flashattention_attention_backward_gb300 import runner
+    from flashattention_attention_backward_gb300.inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS["causal_gqa"]
+    B, H, H_kv, N, d = w.B, w.H, w.H_kv, w.N, w.d
+    stream = torch.cuda.current_stream(dev)
+    x = make_inputs(w)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = runner.forward(q, k, v, w.scale, True)
+    bufs = runner.BackwardBuffers(q, k)
+    nbytes = attn.attn_bwd_dq_partials_bytes(B, H, N, d, True)
+    attn.check(int(nbytes) if nbytes < 0 else 0)
+    partials = torch.empty(nbytes // 4, dtype=torch.float32, device=dev)
+
+    def timed(fn):
+        ts = []
+        for i in range(warmup + iters):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            if i >= warmup:
+                ts.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        rc, status = attn.attn_device_status(clear=True, stream=stream)
+        if rc != 0 or status != 0:
+            raise RuntimeError("device status %d on the variant timing" % status)
+        return sorted(a.elapsed_time(b) for a, b in ts)[len(ts) // 2]
+
+    def plain_step():
+        attn.check(attn.attn_bwd_preprocess(o, do, bufs.dpsum, bufs.dq_accum, B, H, N, d, stream))
+        attn.check(attn.attn_bwd(q, k, v, o, do, lse, bufs.dq_accum, bufs.dk, bufs.dv, B, H,
+                                 H_kv, N, d, w.scale, True, 0.0, bufs.dpsum, stream))
+        attn.check(attn.attn_bwd_finalize(bufs.dq_accum, bufs.dq, w.scale, B, H, N, d, stream))
+
+    def det_step():
+        attn.check(attn.attn_bwd_preprocess(o, do, bufs.dpsum, None, B, H, N, d, stream))
+        attn.check(attn.attn_bwd_deterministic(q, k, v, o, do, lse, partials, bufs.dk, bufs.dv,
+                                               B, H, H_kv, N, d, w.scale, True, 0.0, bufs.dpsum,
+                                               stream))
+        attn.check(attn.attn_bwd_finalize_partials(partials, bufs.dq, w.scale, B, H, N, d, True,
+                                                   stream))
+
+    def drop_bwd():
+        attn.check(attn.attn_bwd_dropout(q, k, v, o, do, lse, bufs.dq_accum, bufs.dk, bufs.dv, B,
+                                         H, H_kv, N, d, w.scale, True, 0.0, bufs.dpsum, p_drop,
+                                         seed, stream))
+
+    res = {"plain_step_ms": timed(plain_step), "deterministic_step_ms": timed(det_step),
+           "dq_partials_bytes": int(nbytes)}
+    attn.check(attn.attn_bwd_preprocess(o, do, bufs.dpsum, bufs.dq_accum, B, H, N, d, stream))
+    res["dropout_bwd_ms"] = timed(drop_bwd)
+    res["dropout_p"] = p_drop
+    f = w.flops()
+    for key in ("plain_step_ms", "deterministic_step_ms", "dropout_bwd_ms"):
+        res[key.replace("_ms", "_tflops")] = f / (res[key] * 1e-3) / 1e12
+    res["dropout_bwd_frac_of_peak"] = res["dropout_bwd_tflops"] / peak
+    del x, q, k, v, do, o, lse, bufs, partials
+    torch.cuda.empty_cache()
+    return res
 
 
 def visible_pairs(N, causal, left, right):
