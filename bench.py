@@ -407,8 +407,9 @@ def all_configs(dev, peak, iters=20, warmup=3):
 
 def variant_timing(dev, peak, iters, warmup, p_drop=0.1, seed=1234):
     """The deterministic-dQ step (preprocess + attn_bwd_deterministic +
-    attn_bwd_finalize_partials) and attn_bwd_dropout on the causal GQA
-    workload, against the plain step; FLOPs as for the plain backward."""
+    attn_bwd_finalize_partials), attn_bwd_dropout and attn_fwd_dropout on the
+    causal GQA workload, against the plain step and attn_fwd; FLOPs as for
+    the plain kernels."""
     import flashattention_attention_backward_gb300 as attn
     from flashattention_attention_backward_gb300 import runner
     from flashattention_attention_backward_gb300.inputs import WORKLOADS, make_inputs
@@ -463,10 +464,16 @@ def variant_timing(dev, peak, iters, warmup, p_drop=0.1, seed=1234):
     attn.check(attn.attn_bwd_preprocess(o, do, bufs.dpsum, bufs.dq_accum, B, H, N, d, stream))
     res["dropout_bwd_ms"] = timed(drop_bwd)
     res["dropout_p"] = p_drop
+    res["dropout_fwd_ms"] = timed(lambda: attn.check(attn.attn_fwd_dropout(
+        q, k, v, o, lse, B, H, H_kv, N, d, w.scale, True, 0.0, p_drop, seed, stream)))
+    res["plain_fwd_ms"] = timed(lambda: attn.check(attn.attn_fwd(
+        q, k, v, o, lse, B, H, H_kv, N, d, w.scale, True, 0.0, stream)))
     f = w.flops()
     for key in ("plain_step_ms", "deterministic_step_ms", "dropout_bwd_ms"):
         res[key.replace("_ms", "_tflops")] = f / (res[key] * 1e-3) / 1e12
     res["dropout_bwd_frac_of_peak"] = res["dropout_bwd_tflops"] / peak
+    for key in ("dropout_fwd_ms", "plain_fwd_ms"):
+        res[key.replace("_ms", "_tflops")] = f * 2 / 5 / (res[key] * 1e-3) / 1e12
     del x, q, k, v, do, o, lse, bufs, partials
     torch.cuda.empty_cache()
     return res

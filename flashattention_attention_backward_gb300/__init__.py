@@ -18,7 +18,7 @@ __all__ = [
     "attn_bwd_finalize", "attn_bwd_noalloc", "attn_device_status", "attn_strerror",
     "attn_selftest_wait_timeout", "attn_bwd_dq_partials_bytes", "attn_bwd_deterministic",
     "attn_bwd_finalize_partials", "attn_fwd_ref_dropout", "attn_bwd_dropout", "attn_fwd_local",
-    "attn_fwd_ref_local", "attn_bwd_local",
+    "attn_fwd_ref_local", "attn_bwd_local", "attn_fwd_dropout",
     "ATTN_OK", "ATTN_ERR_NULL", "ATTN_ERR_SHAPE", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_ALIGN",
     "ATTN_ERR_LAUNCH", "ATTN_ERR_DEVICE_TIMEOUT", "ATTN_ERR_DEVICE", "ATTN_ERR_TOO_LARGE",
 ]
@@ -52,6 +52,8 @@ _SIGNATURES = {
                              ctypes.c_ulonglong, _P],
     "attn_bwd_dropout": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _F, _P,
                          _F, ctypes.c_ulonglong, _P],
+    "attn_fwd_dropout": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _F, _F,
+                         ctypes.c_ulonglong, _P],
     "attn_bwd_noalloc": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _F, _P],
     "attn_fwd_local": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _F, _I, _I, _P],
     "attn_fwd_ref_local": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _F, _I, _I, _P],
@@ -150,6 +152,13 @@ def attn_fwd_ref_dropout(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softc
     return library().attn_fwd_ref_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
                                           H_kv, N, d, scale, int(causal), softcap, p_drop,
                                           int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream))
+
+
+def attn_fwd_dropout(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap, p_drop, seed,
+                     stream=None):
+    return library().attn_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, H_kv,
+                                      N, d, scale, int(causal), softcap, p_drop,
+                                      int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream))
 
 
 def attn_bwd_dropout(q, k, v, o, dO, lse, dq_accum, dk, dv, B, H, H_kv, N, d, scale, causal,

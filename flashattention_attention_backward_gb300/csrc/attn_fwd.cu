@@ -39,6 +39,7 @@
 #include <cuda_bf16.h>
 
 #include "attn_common.cuh"
+#include "philox.cuh"
 #include "sm103_ptx.cuh"
 
 namespace attn {
@@ -96,6 +97,7 @@ struct Params {
   // i - win_left <= j <= i + win_right (the causal mask is win_right = 0;
   // an unbounded side holds N)
   int win_left, win_right;
+  Dropout drop;  // kernel template flag DROP: keep mask of philox.cuh
 };
 
 struct Ctx {
@@ -347,13 +349,42 @@ __device__ __forceinline__ float tile_max(const Params& p, uint32_t tS, int n0, 
   return fmaxf(m0, m1);
 }
 
+// Dropout keep bits of keys k0 .. k0 + 31 for this thread's query row.
+// One Philox call gives the words of four consecutive query rows of one key,
+// and those rows sit in the four lanes of a quad: lane t of the quad draws
+// the call of key k0 + 4 g + t, and a 4 x 4 transpose by shuffles hands
+// every lane its own row's word of each of the four keys (round k: a lane
+// offers word (t - k) mod 4 and reads from quad lane (t + k) mod 4).
+__device__ __forceinline__ uint32_t keep_bits32(const Params& p, int qrow, int k0, uint32_t bh) {
+  const int lane = threadIdx.x & 31;
+  const int t = lane & 3;
+  const uint32_t qgrp = static_cast<uint32_t>(qrow) >> 2;
+  uint32_t bits = 0;
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const PhiloxOut w = philox4x32_10(qgrp, static_cast<uint32_t>(k0 + 4 * g + t), bh, 0u,
+                                      p.drop.seed_lo, p.drop.seed_hi);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int off = (t - k) & 3;
+      const uint32_t give = off == 0 ? w.w[0] : off == 1 ? w.w[1] : off == 2 ? w.w[2] : w.w[3];
+      const uint32_t got =
+          k == 0 ? give : __shfl_sync(0xffffffffu, give, (lane & ~3) | ((t + k) & 3));
+      bits |= (got >= p.drop.threshold ? 1u : 0u) << (4 * g + ((t + k) & 3));
+    }
+  }
+  return bits;
+}
+
 // P = 2^(x - shift) of one S tile as bf16 pairs over the first half of the
-// buffer; returns the row sum of P (fp32, before rounding). Keys
-// 32 ch .. 32 ch + 31 land in columns 16 ch .. 16 ch + 15, whose S values
-// were read in this or an earlier chunk.
-template <bool SOFTCAP, bool MASKED>
+// buffer; returns the row sum of P (fp32, before rounding and before
+// dropout). With DROP the bf16 values are P o Z / (1 - p) (Z the keep mask);
+// the row sum stays that of P. Keys 32 ch .. 32 ch + 31 land in columns
+// 16 ch .. 16 ch + 15, whose S values were read in this or an earlier chunk.
+template <bool SOFTCAP, bool MASKED, bool DROP>
 __device__ __forceinline__ float tile_p(const Params& p, uint32_t tS, int n0, int qrow,
-                                        float c_log2, float cap_in, float cap_out, float shift) {
+                                        float c_log2, float cap_in, float cap_out, float shift,
+                                        uint32_t bh) {
   const uint64_t c2 = f2_make(SOFTCAP ? cap_in : c_log2, SOFTCAP ? cap_in : c_log2);
   const uint64_t out2 = f2_make(cap_out, cap_out);
   const uint64_t one2 = f2_make(1.f, 1.f), mtwo2 = f2_make(-2.f, -2.f);
@@ -363,6 +394,7 @@ __device__ __forceinline__ float tile_p(const Params& p, uint32_t tS, int n0, in
   for (int ch = 0; ch < kBn / 32; ++ch) {
     uint32_t raw[32];
     tmem_ld32(tS + ch * 32, raw);
+    const uint32_t kbits = DROP ? keep_bits32(p, qrow, n0 + ch * 32, bh) : 0xFFFFFFFFu;
     uint32_t packed[16];
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
@@ -387,7 +419,13 @@ __device__ __forceinline__ float tile_p(const Params& p, uint32_t tS, int n0, in
       }
       const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
       sum2 = f2_add(sum2, f2_make(p0, p1));
-      packed[u] = pack_bf16x2(p0, p1);
+      if (DROP) {
+        const float d0 = (kbits >> (2 * u)) & 1u ? p0 * p.drop.inv_keep : 0.f;
+        const float d1 = (kbits >> (2 * u + 1)) & 1u ? p1 * p.drop.inv_keep : 0.f;
+        packed[u] = pack_bf16x2(d0, d1);
+      } else {
+        packed[u] = pack_bf16x2(p0, p1);
+      }
     }
     tmem_st16(tS + ch * 16, packed);
   }
@@ -397,7 +435,7 @@ __device__ __forceinline__ float tile_p(const Params& p, uint32_t tS, int n0, in
 // Softmax warpgroup q (thread = query row r of tile q): per key block, the
 // row maximum, the shift update (with the rescale of O_q and l when the shift
 // moves), and P; then the epilogue of the tile.
-template <int D, bool SOFTCAP>
+template <int D, bool SOFTCAP, bool DROP>
 __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint32_t sbase,
                              uint32_t tmem, const CUtensorMap* to) {
   using L = Layout<D>;
@@ -475,8 +513,10 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint3
     ok = named_bar_and(bar_wg, 128, ok);
     if (!ok) break;
     const float shift = m_used > -INFINITY ? m_used : 0.f;
-    l += masked ? tile_p<SOFTCAP, true>(p, tS, n0, qrow, c_log2, cap_in, cap_out, shift)
-                : tile_p<SOFTCAP, false>(p, tS, n0, qrow, c_log2, cap_in, cap_out, shift);
+    const uint32_t bh = static_cast<uint32_t>(w.bh);
+    l += masked
+             ? tile_p<SOFTCAP, true, DROP>(p, tS, n0, qrow, c_log2, cap_in, cap_out, shift, bh)
+             : tile_p<SOFTCAP, false, DROP>(p, tS, n0, qrow, c_log2, cap_in, cap_out, shift, bh);
     tmem_wait_st();
     tc_fence_before();
     named_bar_sync(bar_wg, 128);
@@ -523,7 +563,7 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint3
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool SOFTCAP>
+template <int D, bool SOFTCAP, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -559,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     mma_role<D>(c, w, sbase, tmem);
   } else if (warp >= 4) {
-    softmax_role<D, SOFTCAP>(c, p, w, sbase, tmem, &tm_o);
+    softmax_role<D, SOFTCAP, DROP>(c, p, w, sbase, tmem, &tm_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -569,10 +609,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool SOFTCAP>
+template <int D, bool SOFTCAP, bool DROP>
 int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
            const CUtensorMap& to, const Params& p, cudaStream_t stream) {
-  auto kern = attn_fwd_kernel<D, SOFTCAP>;
+  auto kern = attn_fwd_kernel<D, SOFTCAP, DROP>;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -609,15 +649,26 @@ using namespace attn;
 namespace attn {
 namespace fwdtc {
 
+template <bool DROP>
+int dispatch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+             const CUtensorMap& to, const Params& p, cudaStream_t s, int d, bool cap) {
+  if (d == 128)
+    return cap ? launch<128, true, DROP>(tq, tk, tv, to, p, s)
+               : launch<128, false, DROP>(tq, tk, tv, to, p, s);
+  return cap ? launch<64, true, DROP>(tq, tk, tv, to, p, s)
+             : launch<64, false, DROP>(tq, tk, tv, to, p, s);
+}
+
 int run(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv,
         int N, int d, float scale, int causal, float softcap, int window_left, int window_right,
-        void* stream) {
+        void* stream, float p_drop = 0.f, unsigned long long seed = 0) {
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
   int rc = check_shape(B, H, H_kv, N, d);
   if (rc != ATTN_OK) return rc;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   // tau > 0: the kernel takes a row's largest logit at its largest score
   if (!std::isfinite(scale) || !(scale > 0.f) || std::isnan(softcap)) return ATTN_ERR_SHAPE;
+  if (!(p_drop >= 0.f && p_drop < 1.f)) return ATTN_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_ALIGN;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
@@ -640,10 +691,13 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
   // causal mask bounds the right side at 0
   p.win_left = (window_left < 0 || window_left > N) ? N : window_left;
   p.win_right = causal ? 0 : ((window_right < 0 || window_right > N) ? N : window_right);
+  p.drop.seed_lo = static_cast<uint32_t>(seed);
+  p.drop.seed_hi = static_cast<uint32_t>(seed >> 32);
+  p.drop.threshold = dropout_threshold(p_drop);
+  p.drop.inv_keep = 1.f / (1.f - p_drop);
   cudaStream_t s = as_stream(stream);
-  if (d == 128)
-    return cap ? launch<128, true>(tq, tk, tv, to, p, s) : launch<128, false>(tq, tk, tv, to, p, s);
-  return cap ? launch<64, true>(tq, tk, tv, to, p, s) : launch<64, false>(tq, tk, tv, to, p, s);
+  return p_drop > 0.f ? dispatch<true>(tq, tk, tv, to, p, s, d, cap)
+                      : dispatch<false>(tq, tk, tv, to, p, s, d, cap);
 }
 
 }  // namespace fwdtc
@@ -660,4 +714,12 @@ extern "C" int attn_fwd_local(const void* q, const void* k, const void* v, void*
                               float softcap, int window_left, int window_right, void* stream) {
   return fwdtc::run(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap, window_left,
                     window_right, stream);
+}
+
+extern "C" int attn_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int H, int H_kv, int N, int d, float scale, int causal,
+                                float softcap, float p_drop, unsigned long long seed,
+                                void* stream) {
+  return fwdtc::run(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap, -1, -1, stream,
+                    p_drop, seed);
 }

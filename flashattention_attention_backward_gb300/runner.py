@@ -6,8 +6,8 @@ import torch
 
 from . import (attn_bwd, attn_bwd_deterministic, attn_bwd_dq_partials_bytes, attn_bwd_dropout,
                attn_bwd_finalize, attn_bwd_finalize_partials, attn_bwd_local, attn_bwd_preprocess,
-               attn_fwd, attn_fwd_local, attn_fwd_ref, attn_fwd_ref_dropout, attn_fwd_ref_local,
-               check)
+               attn_fwd, attn_fwd_dropout, attn_fwd_local, attn_fwd_ref, attn_fwd_ref_dropout,
+               attn_fwd_ref_local, check)
 
 
 def _dims(q, k):
@@ -24,14 +24,15 @@ def forward(q, k, v, scale, causal, softcap=0.0, stream=None, impl="tc", dropout
             window=None):
     """O [B,H,N,d] bf16 and LSE [B,H,N] fp32: attn_fwd (tensor cores, impl
     "tc") or attn_fwd_ref (plain fp32, impl "ref"). dropout = (p_drop, seed)
-    runs attn_fwd_ref_dropout; window = (left, right) runs attn_fwd_local or
-    attn_fwd_ref_local."""
+    runs attn_fwd_dropout or attn_fwd_ref_dropout; window = (left, right) runs
+    attn_fwd_local or attn_fwd_ref_local."""
     B, H, H_kv, N, d = _dims(q, k)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if dropout is not None:
-        check(attn_fwd_ref_dropout(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap,
-                                   dropout[0], dropout[1], _stream(stream)))
+        fn = {"tc": attn_fwd_dropout, "ref": attn_fwd_ref_dropout}[impl]
+        check(fn(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap, dropout[0],
+                 dropout[1], _stream(stream)))
         return o, lse
     if window is not None:
         fn = {"tc": attn_fwd_local, "ref": attn_fwd_ref_local}[impl]

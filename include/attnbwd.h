@@ -97,6 +97,18 @@ int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* o,
                      const float* dpsum, float p_drop, unsigned long long seed, void* stream);
 
 /*
+ * attn_fwd_dropout: attn_fwd (the one-pass tensor-core forward; scale > 0)
+ * with the same dropout as attn_fwd_ref_dropout: O = (P o Z / (1 - p)) V with
+ * the keep mask Z defined above, LSE that of P. One Philox call still serves
+ * four elements: the four query rows of a call sit in four adjacent lanes,
+ * each lane draws the call of one key and a shuffle transpose hands every
+ * lane its own row's words.
+ */
+int attn_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int H_kv, int N, int d, float scale, int causal, float softcap,
+                     float p_drop, unsigned long long seed, void* stream);
+
+/*
  * attn_fwd: the same forward as attn_fwd_ref (same arguments, outputs and
  * layouts) on the tcgen05 tensor cores, in one pass with the online softmax
  * ([bwd-detail] §1.2; [FA-v1-bwd] §1.1 forward, §3.2 eq. 9-12 running

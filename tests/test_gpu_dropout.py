@@ -1,8 +1,9 @@
 """GPU parity with dropout (Philox keep mask, drawn independently on each
-side): attn_fwd_ref_dropout and attn_bwd_dropout against the fp64 oracle
-with the same (p_drop, seed). The keep decision is an integer one taken from
-the same 32-bit words on both sides, so any mask mismatch shows up as a
-gross error; the float tolerances are the usual ones."""
+side): attn_fwd_dropout (tensor cores), attn_fwd_ref_dropout (fp32) and
+attn_bwd_dropout against the fp64 oracle with the same (p_drop, seed). The
+keep decision is an integer one taken from the same 32-bit words on both
+sides, so any mask mismatch shows up as a gross error; the float tolerances
+are the usual ones."""
 import numpy as np
 import pytest
 import torch
@@ -36,6 +37,8 @@ def test_dropout_fwd_bwd_against_oracle(w, p_drop, seed):
     dev = torch.device("cuda:0")
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     o, lse = runner.forward(q, k, v, w.scale, w.causal, w.softcap, dropout=(p32, seed))
+    o_r, lse_r = runner.forward(q, k, v, w.scale, w.causal, w.softcap, dropout=(p32, seed),
+                                impl="ref")
     dq, dk, dv = runner.backward(q, k, v, o, do, lse, w.scale, w.causal, w.softcap,
                                  dropout=(p32, seed))
     torch.cuda.synchronize()
@@ -45,8 +48,9 @@ def test_dropout_fwd_bwd_against_oracle(w, p_drop, seed):
     f64 = {n: x[n].double().numpy() for n in ("q", "k", "v", "do")}
     O, LSE = attention_forward(f64["q"], f64["k"], f64["v"], w.scale, w.causal, w.softcap,
                                dropout=(p32, seed))
-    assert float(np.abs(lse.cpu().double().numpy() - LSE).max()) <= LSE_ABS
-    assert rel_max(o.cpu().double().numpy(), O) <= O_MAX_REL
+    for o_, lse_ in ((o, lse), (o_r, lse_r)):
+        assert float(np.abs(lse_.cpu().double().numpy() - LSE).max()) <= LSE_ABS
+        assert rel_max(o_.cpu().double().numpy(), O) <= O_MAX_REL
     dQ, dK, dV = attention_backward(f64["q"], f64["k"], f64["v"], f64["do"], w.scale, w.causal,
                                     w.softcap, dropout=(p32, seed))
     check_grad("dQ", dq.cpu(), dQ)
@@ -59,9 +63,27 @@ def test_dropout_zero_matches_plain():
     x = make_inputs(w)
     dev = torch.device("cuda:0")
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
-    o, lse = runner.forward(q, k, v, w.scale, w.causal, w.softcap, impl="ref")
-    o0, lse0 = runner.forward(q, k, v, w.scale, w.causal, w.softcap, dropout=(0.0, 3))
-    assert torch.equal(o, o0) and torch.equal(lse, lse0)
+    for impl in ("ref", "tc"):
+        o, lse = runner.forward(q, k, v, w.scale, w.causal, w.softcap, impl=impl)
+        o0, lse0 = runner.forward(q, k, v, w.scale, w.causal, w.softcap, dropout=(0.0, 3),
+                                  impl=impl)
+        assert torch.equal(o, o0) and torch.equal(lse, lse0)
     a = [t.clone() for t in runner.backward(q, k, v, o, do, lse, w.scale, w.causal, w.softcap)]
     b = runner.backward(q, k, v, o, do, lse, w.scale, w.causal, w.softcap, dropout=(0.0, 3))
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
+def test_dropout_fwd_keep_rate_and_rows():
+    """attn_fwd_dropout on a key-independent V (every row of V equal to 1):
+    O_i = (sum of the kept P_ij) / (1 - p), whose mean over many rows is 1,
+    and rows of different quads of lanes draw different masks."""
+    w = _w("drop_rate", 1, 1, 1, 1024, 64, False, seed=5)
+    x = make_inputs(w)
+    dev = torch.device("cuda:0")
+    q, k = (x[n].to(dev) for n in ("q", "k"))
+    v = torch.ones_like(k)
+    o, _ = runner.forward(q, k, v, w.scale, False, dropout=(0.3, 77))
+    torch.cuda.synchronize()
+    row = o[0, 0, :, 0].float()
+    assert abs(float(row.mean()) - 1.0) < 0.03
+    assert float(row.std()) > 0.01  # the mask differs from row to row
