@@ -329,15 +329,16 @@ __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t t
 template <bool MASKED>
 __device__ __forceinline__ float tile_max(const Params& p, uint32_t tS, int n0, int qrow) {
   float m0 = -INFINITY, m1 = -INFINITY;
+  // two 32-column loads per wait
 #pragma unroll
-  for (int ch = 0; ch < kBn / 32; ++ch) {
-    uint32_t raw[32];
-    tmem_ld32(tS + ch * 32, raw);
+  for (int ch2 = 0; ch2 < kBn / 64; ++ch2) {
+    uint32_t raw[64];
+    tmem_ld32x2(tS + ch2 * 64, tS + ch2 * 64 + 32, raw);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
+    for (int e = 0; e < 64; ++e) {
       float s = __uint_as_float(raw[e]);
       if (MASKED) {
-        const int key = n0 + ch * 32 + e;
+        const int key = n0 + ch2 * 64 + e;
         if (!(key < p.N && key - qrow <= p.win_right && qrow - key <= p.win_left)) s = -INFINITY;
       }
       if (e & 1)
@@ -385,34 +386,37 @@ template <bool SOFTCAP, bool MASKED, bool DROP>
 __device__ __forceinline__ float tile_p(const Params& p, uint32_t tS, int n0, int qrow,
                                         float c_log2, float cap_in, float cap_out, float shift,
                                         uint32_t bh) {
-  const uint64_t c2 = f2_make(SOFTCAP ? cap_in : c_log2, SOFTCAP ? cap_in : c_log2);
+  const uint64_t c2v = f2_make(SOFTCAP ? cap_in : c_log2, SOFTCAP ? cap_in : c_log2);
   const uint64_t out2 = f2_make(cap_out, cap_out);
   const uint64_t one2 = f2_make(1.f, 1.f), mtwo2 = f2_make(-2.f, -2.f);
   const uint64_t nsh2 = f2_make(-shift, -shift);
   uint64_t sum2 = f2_make(0.f, 0.f);
+  // two 32-column loads per wait; keys 64 c2 .. 64 c2 + 63 land in columns
+  // 32 c2 .. 32 c2 + 31
 #pragma unroll
-  for (int ch = 0; ch < kBn / 32; ++ch) {
-    uint32_t raw[32];
-    tmem_ld32(tS + ch * 32, raw);
-    const uint32_t kbits = DROP ? keep_bits32(p, qrow, n0 + ch * 32, bh) : 0xFFFFFFFFu;
-    uint32_t packed[16];
+  for (int c2 = 0; c2 < kBn / 64; ++c2) {
+    uint32_t raw[64];
+    tmem_ld32x2(tS + c2 * 64, tS + c2 * 64 + 32, raw);
+    const uint32_t kb0 = DROP ? keep_bits32(p, qrow, n0 + c2 * 64, bh) : 0xFFFFFFFFu;
+    const uint32_t kb1 = DROP ? keep_bits32(p, qrow, n0 + c2 * 64 + 32, bh) : 0xFFFFFFFFu;
+    uint32_t packed[32];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
+    for (int u = 0; u < 32; ++u) {
       const uint64_t s2 = f2_make(raw[2 * u], raw[2 * u + 1]);
       uint64_t y2;
       if (SOFTCAP) {
         // tanh(v) = 1 - 2 / (exp(2v) + 1) with v = tau s / c
-        const uint64_t v2 = f2_mul(s2, c2);
+        const uint64_t v2 = f2_mul(s2, c2v);
         const uint64_t e1 = f2_add(f2_make(ex2_approx(f2_lo(v2)), ex2_approx(f2_hi(v2))), one2);
         const uint64_t th2 =
             f2_fma(f2_make(rcp_approx(f2_lo(e1)), rcp_approx(f2_hi(e1))), mtwo2, one2);
         y2 = f2_fma(th2, out2, nsh2);
       } else {
-        y2 = f2_fma(s2, c2, nsh2);
+        y2 = f2_fma(s2, c2v, nsh2);
       }
       float y0 = f2_lo(y2), y1 = f2_hi(y2);
       if (MASKED) {
-        const int key = n0 + ch * 32 + 2 * u;
+        const int key = n0 + c2 * 64 + 2 * u;
         if (!(key < p.N && key - qrow <= p.win_right && qrow - key <= p.win_left)) y0 = -INFINITY;
         if (!(key + 1 < p.N && key + 1 - qrow <= p.win_right && qrow - key - 1 <= p.win_left))
           y1 = -INFINITY;
@@ -420,14 +424,23 @@ __device__ __forceinline__ float tile_p(const Params& p, uint32_t tS, int n0, in
       const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
       sum2 = f2_add(sum2, f2_make(p0, p1));
       if (DROP) {
-        const float d0 = (kbits >> (2 * u)) & 1u ? p0 * p.drop.inv_keep : 0.f;
-        const float d1 = (kbits >> (2 * u + 1)) & 1u ? p1 * p.drop.inv_keep : 0.f;
+        const uint32_t kb = u < 16 ? kb0 : kb1;
+        const int bit = (2 * u) & 31;
+        const float d0 = (kb >> bit) & 1u ? p0 * p.drop.inv_keep : 0.f;
+        const float d1 = (kb >> (bit + 1)) & 1u ? p1 * p.drop.inv_keep : 0.f;
         packed[u] = pack_bf16x2(d0, d1);
       } else {
         packed[u] = pack_bf16x2(p0, p1);
       }
     }
-    tmem_st16(tS + ch * 16, packed);
+    uint32_t lo[16], hi[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      lo[u] = packed[u];
+      hi[u] = packed[16 + u];
+    }
+    tmem_st16(tS + c2 * 32, lo);
+    tmem_st16(tS + c2 * 32 + 16, hi);
   }
   return f2_lo(sum2) + f2_hi(sum2);
 }
