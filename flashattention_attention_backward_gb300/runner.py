@@ -10,10 +10,34 @@ from . import (attn_bwd, attn_bwd_deterministic, attn_bwd_dq_partials_bytes, att
                attn_fwd_ref_local, check)
 
 
-def _dims(q, k):
+def _dims(q, k, *others):
+    """(B, H, H_kv, N, d) of q [B,H,N,d] and k [B,H_kv,N,d], after checking
+    what the C ABI assumes of its pointers: contiguous bf16 tensors on one
+    CUDA device, with matching shapes (k, v alike; q, o, dO alike)."""
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q and k must be 4-D ([B, heads, N, d])")
     B, H, N, d = q.shape
     H_kv = k.shape[1]
+    if k.shape != (B, H_kv, N, d):
+        raise ValueError("k has shape %s, expected %s" % (tuple(k.shape), (B, H_kv, N, d)))
+    for t in others:
+        if t.shape not in (q.shape, k.shape):
+            raise ValueError("tensor of shape %s matches neither q nor k" % (tuple(t.shape),))
+    for t in (q, k) + others:
+        if t.dtype != torch.bfloat16:
+            raise ValueError("expected bfloat16 tensors, got %s" % t.dtype)
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous (row-major [B, heads, N, d])")
+    for t in (q, k) + others:
+        if t.device != q.device or t.device.type != "cuda":
+            raise ValueError("all tensors must be on the same CUDA device")
     return B, H, H_kv, N, d
+
+
+def _check_lse(lse, B, H, N, device):
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, N) \
+            or lse.device != device:
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor on the inputs' device")
 
 
 def _stream(stream):
@@ -26,7 +50,9 @@ def forward(q, k, v, scale, causal, softcap=0.0, stream=None, impl="tc", dropout
     "tc") or attn_fwd_ref (plain fp32, impl "ref"). dropout = (p_drop, seed)
     runs attn_fwd_dropout or attn_fwd_ref_dropout; window = (left, right) runs
     attn_fwd_local or attn_fwd_ref_local."""
-    B, H, H_kv, N, d = _dims(q, k)
+    B, H, H_kv, N, d = _dims(q, k, v)
+    if v.shape != k.shape:
+        raise ValueError("v must have the shape of k")
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if dropout is not None:
@@ -63,7 +89,10 @@ def backward(q, k, v, o, do, lse, scale, causal, softcap=0.0, stream=None, bufs=
     deterministic=True, preprocess -> attn_bwd_deterministic ->
     finalize_partials (dQ identical bit for bit from run to run). window =
     (left, right) runs attn_bwd_local in place of attn_bwd."""
-    B, H, H_kv, N, d = _dims(q, k)
+    B, H, H_kv, N, d = _dims(q, k, v, o, do)
+    if v.shape != k.shape or o.shape != q.shape or do.shape != q.shape:
+        raise ValueError("v must have the shape of k, and o, dO that of q")
+    _check_lse(lse, B, H, N, q.device)
     s = _stream(stream)
     if bufs is None:
         bufs = BackwardBuffers(q, k)
