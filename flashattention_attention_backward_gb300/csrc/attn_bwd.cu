@@ -1062,13 +1062,8 @@ struct Maps {
 template <int D, bool CAUSAL, bool SOFTCAP, bool DET, bool DROP>
 int launch(const Maps& m, const Params& p, cudaStream_t stream) {
   auto kern = attn_bwd_kernel<D, CAUSAL, SOFTCAP, DET, DROP>;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Layout<D>::kBytes) != cudaSuccess)
-      return ATTN_ERR_LAUNCH;
-    configured = true;
-  }
+  static std::atomic<bool> configured[kMaxTrackedDevices];
+  if (!set_smem_limit_once(kern, Layout<D>::kBytes, configured)) return ATTN_ERR_LAUNCH;
   // persistent: one CTA per SM (or per unit, if there are fewer units)
   const int sms = sm_count();
   if (sms <= 0) return ATTN_ERR_LAUNCH;

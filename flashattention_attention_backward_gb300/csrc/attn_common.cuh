@@ -46,6 +46,25 @@ inline int sm_count() {
   return n;
 }
 
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device: the attribute belongs to the device's context, so
+// a process that drives several GPUs needs it on each. `done` is the calling
+// launcher's own record (one per kernel instantiation).
+constexpr int kMaxTrackedDevices = 64;
+template <typename Kernel>
+inline bool set_smem_limit_once(Kernel kern, int bytes,
+                                std::atomic<bool> (&done)[kMaxTrackedDevices]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const bool tracked = dev >= 0 && dev < kMaxTrackedDevices;
+  if (tracked && done[dev].load(std::memory_order_acquire)) return true;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return false;
+  if (tracked) done[dev].store(true, std::memory_order_release);
+  return true;
+}
+
 inline int launch_status() {
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;

@@ -626,13 +626,8 @@ template <int D, bool SOFTCAP, bool DROP>
 int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
            const CUtensorMap& to, const Params& p, cudaStream_t stream) {
   auto kern = attn_fwd_kernel<D, SOFTCAP, DROP>;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Layout<D>::kBytes) != cudaSuccess)
-      return ATTN_ERR_LAUNCH;
-    configured = true;
-  }
+  static std::atomic<bool> configured[kMaxTrackedDevices];
+  if (!set_smem_limit_once(kern, Layout<D>::kBytes, configured)) return ATTN_ERR_LAUNCH;
   const long long grid = static_cast<long long>(p.pairs) * p.B * p.H;
   if (grid > 0x7fffffffLL) return ATTN_ERR_TOO_LARGE;
   kern<<<static_cast<unsigned>(grid), kThreads, Layout<D>::kBytes, stream>>>(tq, tk, tv, to, p);

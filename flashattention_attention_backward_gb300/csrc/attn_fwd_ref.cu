@@ -242,13 +242,9 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_ref_kernel(const Params p) 
 
 template <int D>
 int launch(const Params& p, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(attn_fwd_ref_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Smem<D>::kBytes) != cudaSuccess)
-      return ATTN_ERR_LAUNCH;
-    configured = true;
-  }
+  static std::atomic<bool> configured[kMaxTrackedDevices];
+  if (!set_smem_limit_once(attn_fwd_ref_kernel<D>, Smem<D>::kBytes, configured))
+    return ATTN_ERR_LAUNCH;
   const long long grid = static_cast<long long>(p.q_blocks) * p.B * p.H;
   if (grid > 0x7fffffffLL) return ATTN_ERR_TOO_LARGE;
   attn_fwd_ref_kernel<D><<<static_cast<unsigned>(grid), kThreads, Smem<D>::kBytes, s>>>(p);
