@@ -87,3 +87,44 @@ def test_dropout_fwd_keep_rate_and_rows():
     row = o[0, 0, :, 0].float()
     assert abs(float(row.mean()) - 1.0) < 0.03
     assert float(row.std()) > 0.01  # the mask differs from row to row
+
+
+def test_dropout_causal_gqa_full_size_sampled():
+    """The causal GQA workload at full size (B=2, H=32, H_kv=8, N=4096,
+    d=128) with p = 0.1, the launch configuration the bench times: O and LSE
+    of attn_fwd_dropout and dQ, dK, dV of attn_bwd_dropout against the oracle
+    on one seeded (batch, KV head) slice. The oracle runs per query head with
+    the keep mask of the library's head index b * H + h."""
+    from flashattention_attention_backward_gb300.inputs import WORKLOADS, sample_slices
+    from oracle.attention import head_backward
+    from oracle.philox import dropout_keep_mask
+    w = WORKLOADS["causal_gqa"]
+    p32, seed = float(np.float32(0.1)), 1234
+    x = make_inputs(w)
+    dev = torch.device("cuda:0")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = runner.forward(q, k, v, w.scale, True, dropout=(p32, seed))
+    dq, dk, dv = runner.backward(q, k, v, o, do, lse, w.scale, True, dropout=(p32, seed))
+    torch.cuda.synchronize()
+    import flashattention_attention_backward_gb300 as attn
+    rc, status = attn.attn_device_status(clear=True)
+    assert rc == 0 and status == 0
+    G = w.G
+    for (b, g) in sample_slices(w, 1):
+        kk = x["k"][b, g].double().numpy()
+        vv = x["v"][b, g].double().numpy()
+        dK = np.zeros_like(kk)
+        dV = np.zeros_like(vv)
+        for h in range(g * G, (g + 1) * G):
+            keep = dropout_keep_mask(seed, b * w.H + h, w.N, w.N, p32)
+            r = head_backward(x["q"][b, h].double().numpy(), kk, vv,
+                              x["do"][b, h].double().numpy(), w.scale, True, 0.0, keep=keep,
+                              p_drop=p32)
+            assert float(np.abs(lse[b, h].cpu().double().numpy() - r["LSE"]).max()) <= LSE_ABS
+            assert rel_max(o[b, h].cpu().double().numpy(), r["O"]) <= O_MAX_REL
+            check_grad("dQ[%d]" % h, dq[b, h].cpu(), r["dQ"])
+            dK += r["dK"]
+            dV += r["dV"]
+            del r, keep
+        check_grad("dK", dk[b, g].cpu(), dK)
+        check_grad("dV", dv[b, g].cpu(), dV)
