@@ -402,7 +402,46 @@ def all_configs(dev, peak, iters=20, warmup=3):
         torch.cuda.empty_cache()
     out["causal_gqa_window1024"] = local_window_timing(dev, peak, iters, warmup)
     out["causal_gqa_variants"] = variant_timing(dev, peak, iters, warmup)
+    out["causal_gqa_d256"] = d256_timing(dev, peak, iters, warmup)
     return out
+
+
+def d256_timing(dev, peak, iters, warmup):
+    """attn_bwd with head dimension 256 (its own kernel) on a causal GQA shape
+    of the same token count as the causal GQA workload: B=2, H=16, H_kv=4,
+    N=4096, d=256; FLOPs as for the plain backward (5 GEMMs of 2 N^2 d per
+    head, halved for causal)."""
+    import flashattention_attention_backward_gb300 as attn
+    from flashattention_attention_backward_gb300 import runner
+    from flashattention_attention_backward_gb300.inputs import Workload, make_inputs
+
+    w = Workload("causal_gqa_d256", 2, 16, 4, 4096, 256, True, seed_base=20261202 + 6000)
+    stream = torch.cuda.current_stream(dev)
+    x = make_inputs(w)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = runner.forward(q, k, v, w.scale, True)
+    bufs = runner.BackwardBuffers(q, k)
+    ts = []
+    for i in range(warmup + iters):
+        attn.check(attn.attn_bwd_preprocess(o, do, bufs.dpsum, bufs.dq_accum, w.B, w.H, w.N, w.d,
+                                            stream))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        attn.check(attn.attn_bwd(q, k, v, o, do, lse, bufs.dq_accum, bufs.dk, bufs.dv, w.B, w.H,
+                                 w.H_kv, w.N, w.d, w.scale, True, 0.0, bufs.dpsum, stream))
+        e1.record(stream)
+        if i >= warmup:
+            ts.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    rc, status = attn.attn_device_status(clear=True, stream=stream)
+    if rc != 0 or status != 0:
+        raise RuntimeError("device status %d on the d = 256 timing" % status)
+    ms = sorted(a.elapsed_time(b) for a, b in ts)[len(ts) // 2]
+    tf = w.flops() / (ms * 1e-3) / 1e12
+    del x, q, k, v, do, o, lse, bufs
+    torch.cuda.empty_cache()
+    return {"B": w.B, "H": w.H, "H_kv": w.H_kv, "N": w.N, "d": w.d, "causal": True,
+            "bwd_ms": ms, "tflops": tf, "frac_of_peak": tf / peak}
 
 
 def variant_timing(dev, peak, iters, warmup, p_drop=0.1, seed=1234):

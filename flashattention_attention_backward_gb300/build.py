@@ -17,7 +17,8 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libattnbwd.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
-SOURCES = ["attn_bwd.cu", "attn_fwd.cu", "attn_fwd_ref.cu", "attn_prepost.cu", "attn_noalloc.cu"]
+SOURCES = ["attn_bwd.cu", "attn_bwd256.cu", "attn_fwd.cu", "attn_fwd_ref.cu", "attn_prepost.cu",
+           "attn_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-fno-strict-aliasing"]

@@ -1105,13 +1105,17 @@ int run(const void* q, const void* k, const void* v, const void* dO, const float
   if (!q || !k || !v || !dO || !lse || !dq_target || !dk || !dv || !dpsum) return ATTN_ERR_NULL;
   int rc = check_shape(B, H, H_kv, N, d);
   if (rc != ATTN_OK) return rc;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  // d = 256: plain and local-window calls only (its own kernel)
+  if (d != 64 && d != 128 && !(d == 256 && !det && p_drop == 0.f)) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || scale == 0.f || std::isnan(softcap)) return ATTN_ERR_SHAPE;
   if (!(p_drop >= 0.f && p_drop < 1.f)) return ATTN_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
       !aligned16(dq_target) || !aligned16(dk) || !aligned16(dv) || !aligned16(dpsum))
     return ATTN_ERR_ALIGN;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (d == 256)
+    return bwd256_run(q, k, v, dO, lse, dq_target, dk, dv, B, H, H_kv, N, scale, causal, softcap,
+                      dpsum, window_left, window_right, as_stream(stream));
 
   Params p;
   p.lse = lse;
@@ -1213,9 +1217,10 @@ extern "C" int attn_device_status(int* status, int clear, void* stream) {
     if (cudaMemcpyToSymbol(bwd::g_status, &zero, sizeof(int)) != cudaSuccess)
       return ATTN_ERR_LAUNCH;
   }
-  int vf = 0;  // the forward kernels keep their own word
+  int vf = 0, v256 = 0;  // the forward and d = 256 kernels keep their own words
   if (fwd_status(&vf, clear != 0) != ATTN_OK) return ATTN_ERR_LAUNCH;
-  *status = v != 0 ? v : vf;
+  if (bwd256_status(&v256, clear != 0) != ATTN_OK) return ATTN_ERR_LAUNCH;
+  *status = v != 0 ? v : (vf != 0 ? vf : v256);
   return ATTN_OK;
 }
 

@@ -138,4 +138,14 @@ inline uint32_t dropout_threshold(float p) {
 // value, cleared when `clear`. Returns ATTN_OK or ATTN_ERR_LAUNCH.
 int fwd_status(int* status, bool clear);
 
+// The same for the d = 256 backward kernel (attn_bwd256.cu).
+int bwd256_status(int* status, bool clear);
+
+// attn_bwd / attn_bwd_local for d = 256 (attn_bwd256.cu), after the caller
+// has checked pointers, shapes, alignment and scale; B, H, N > 0.
+int bwd256_run(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+               float* dq_accum, void* dk, void* dv, int B, int H, int H_kv, int N, float scale,
+               int causal, float softcap, const float* dpsum, int window_left, int window_right,
+               cudaStream_t s);
+
 }  // namespace attn

@@ -265,7 +265,7 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
   int rc = check_shape(B, H, H_kv, N, d);
   if (rc != ATTN_OK) return rc;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || scale == 0.f || std::isnan(softcap)) return ATTN_ERR_SHAPE;
   if (!(p_drop >= 0.f && p_drop < 1.f)) return ATTN_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
@@ -293,6 +293,7 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
   p.drop.threshold = dropout_threshold(p_drop);
   p.drop.inv_keep = 1.f / (1.f - p_drop);
   cudaStream_t s = as_stream(stream);
+  if (d == 256) return launch<256>(p, s);
   return d == 128 ? launch<128>(p, s) : launch<64>(p, s);
 }
 

@@ -22,8 +22,10 @@
  *    [B, H, N, d]; K, V, dK, dV are [B, H_kv, N, d]; LSE and D are [B, H, N].
  *    bf16 tensors are passed as `void*` (IEEE bfloat16 bit patterns).
  *  * Query head h uses KV head h / (H / H_kv) (H must be a multiple of H_kv).
- *  * d must be 64 or 128 for attn_fwd, attn_fwd_ref and attn_bwd; preprocess and
- *    finalize accept any d that is a multiple of 4.
+ *  * d must be 64 or 128 for attn_fwd and the variants of attn_bwd (dropout,
+ *    deterministic, allocation-free); 64, 128 or 256 for attn_fwd_ref,
+ *    attn_fwd_ref_local, attn_bwd and attn_bwd_local; preprocess and finalize
+ *    accept any d that is a multiple of 4.
  *  * Every pointer must be 16-byte aligned (the kernels use TMA and 16-byte
  *    vector accesses).
  *  * `scale` is tau (usually 1/sqrt(d)); the logit is tau * q.k.
@@ -176,6 +178,10 @@ int attn_bwd_preprocess(const void* o, const void* dO, float* dpsum, float* dq_a
  * Out: dk, dv [B,H_kv,N,d] bf16, overwritten; dk includes tau; for H_kv < H
  *      they are summed over the head group.
  * `o` is accepted for interface completeness; D already carries its use.
+ * d = 256 runs a kernel of its own ([bwd-detail] §8.3 slices the d = 256
+ * GEMMs): a CTA accumulates one half of d for 128 keys over query tiles of
+ * 64, recomputing S and dP over the full d (seven GEMM-equivalents per tile
+ * instead of five); dQ accumulates the same way.
  * Order on the stream: attn_bwd_preprocess, attn_bwd, attn_bwd_finalize.
  * dQ is summed with fp32 atomics, so it may differ in the last bits from run
  * to run; dK and dV are summed on chip in a fixed order.
