@@ -306,6 +306,17 @@ __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t t
       mma_commit(bar_addr(c, BAR_DO_EMPTY));
     }
     if (!(ok = wait_warp(c, BAR_DS_FULL, ph))) break;
+    tc_fence_after();
+    // dK[:, half] += dS^T Q[:, half] (A = dS^T [key][query], K-major) first:
+    // it is the Q tile's last reader, so the next Q tile's load starts before
+    // the dQ GEMM
+    if (leader) {
+#pragma unroll
+      for (int k = 0; k < kBr / 16; ++k)
+        mma_ss(tdK, sdesc_from_lo(kDS + ((32 * k) >> 4)), sdesc_from_lo(mQ + mnmaj(k)), kIdKV,
+               (t > 0 || k > 0) ? 1u : 0u);
+      mma_commit(bar_addr(c, BAR_Q_EMPTY));
+    }
     // the dQ buffer of tile t was drained with tile t - 2
     const int qb = t & 1;
     if (t >= 2 && !(ok = wait_warp(c, BAR_DQ_EMPTY + qb, ((t >> 1) - 1) & 1))) break;
@@ -317,12 +328,6 @@ __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t t
         mma_ss(tdQ + 64 * qb, sdesc_from_lo(mK + mnmaj(k)), sdesc_from_lo(mDS + mnmaj(k)), kIdQ,
                k > 0);
       mma_commit(bar_addr(c, BAR_DQ_FULL + qb));
-      // dK[:, half] += dS^T Q[:, half] (A = dS^T [key][query], K-major)
-#pragma unroll
-      for (int k = 0; k < kBr / 16; ++k)
-        mma_ss(tdK, sdesc_from_lo(kDS + ((32 * k) >> 4)), sdesc_from_lo(mQ + mnmaj(k)), kIdKV,
-               (t > 0 || k > 0) ? 1u : 0u);
-      mma_commit(bar_addr(c, BAR_Q_EMPTY));
       mma_commit(bar_addr(c, BAR_DS_FREE));
     }
   }
