@@ -72,17 +72,20 @@ struct Layout {
   static constexpr int kLSE = 229376;   // 64 fp32 (-LSE * log2e)
   static constexpr int kDsum = 229632;  // 64 fp32 (D)
   static constexpr int kBars = 229888;
-  static constexpr int kNumBars = 16;
+  static constexpr int kNumBars = 18;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kBytes = kAbort + 12;
 };
 static_assert(Layout::kBytes <= 232448, "shared memory budget");
 
+// The Q tile's two boxes of the other half of d are read only by the tile's
+// S GEMM and have barriers of their own (QO), so the next tile's copies load
+// while this tile's own half (QH, with LSE and D) is still in use.
 enum Bar {
   BAR_KV_FULL = 0,
-  BAR_Q_FULL = 1,
-  BAR_Q_EMPTY = 2,
+  BAR_QH_FULL = 1,
+  BAR_QH_EMPTY = 2,
   BAR_DO_FULL = 3,
   BAR_DO_EMPTY = 4,
   BAR_S_FULL = 5,
@@ -94,6 +97,8 @@ enum Bar {
   BAR_DQ_EMPTY = 12,  // + buffer
   BAR_UNIT_DONE = 14,
   BAR_DRAIN = 15,     // abort path only
+  BAR_QO_FULL = 16,
+  BAR_QO_EMPTY = 17,
 };
 
 struct Params {
@@ -203,22 +208,40 @@ __device__ void producer_role(const Ctx& c, const Params& p, const Work& w, uint
   const uint64_t reuse = policy_evict_last();  // Q, dO tiles serve every key block of the head
   float* s_lse = reinterpret_cast<float*>(smem + L::kLSE);
   float* s_d = reinterpret_cast<float*>(smem + L::kDsum);
-  int issued_q = 0, issued_do = 0;
+  int issued_q = 0, issued_qo = 0, issued_do = 0;
   bool ok = true;
   for (int t = 0; t < w.T; ++t) {
     int h, m_block;
     tile_coord(w, t, h, m_block);
     const int bh = w.b * p.H + h;
     const int m0 = m_block * kBr;
-    if (t > 0 && !(ok = wait_warp(c, BAR_Q_EMPTY, (t - 1) & 1))) break;
+    // boxes of the other half of d: free once the previous S GEMM read them
+    if (t > 0 && !(ok = wait_warp(c, BAR_QO_EMPTY, (t - 1) & 1))) break;
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar_addr(c, BAR_Q_FULL), 4 * 8192);
-      for (int cb = 0; cb < 4; ++cb)
-        tma_load_3d_hint(sbase + L::kQ + cb * 8192, tm_q, bar_addr(c, BAR_Q_FULL), 64 * cb, m0, bh,
-                         reuse);
+      mbar_arrive_expect_tx(bar_addr(c, BAR_QO_FULL), 2 * 8192);
+      for (int cb = 2 * (1 - w.half); cb < 2 * (1 - w.half) + 2; ++cb)
+        tma_load_3d_hint(sbase + L::kQ + cb * 8192, tm_q, bar_addr(c, BAR_QO_FULL), 64 * cb, m0,
+                         bh, reuse);
     }
-    // the softmax read the previous tile's LSE and D before DS_FULL, which
-    // precedes the previous tile's dK GEMM and hence Q_EMPTY
+    issued_qo = t + 1;
+    if (t > 0 && !(ok = wait_warp(c, BAR_DO_EMPTY, (t - 1) & 1))) break;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_addr(c, BAR_DO_FULL), 4 * 8192);
+      for (int cb = 0; cb < 4; ++cb)
+        tma_load_3d_hint(sbase + L::kDO + cb * 8192, tm_do, bar_addr(c, BAR_DO_FULL), 64 * cb, m0,
+                         bh, reuse);
+    }
+    issued_do = t + 1;
+    // this CTA's half (also read by the dK GEMM), with LSE and D; the softmax
+    // read the previous tile's LSE and D before DS_FULL, which precedes the
+    // previous dK GEMM and hence QH_EMPTY
+    if (t > 0 && !(ok = wait_warp(c, BAR_QH_EMPTY, (t - 1) & 1))) break;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_addr(c, BAR_QH_FULL), 2 * 8192);
+      for (int cb = 2 * w.half; cb < 2 * w.half + 2; ++cb)
+        tma_load_3d_hint(sbase + L::kQ + cb * 8192, tm_q, bar_addr(c, BAR_QH_FULL), 64 * cb, m0,
+                         bh, reuse);
+    }
     {
       const long long row0 = static_cast<long long>(bh) * p.N + m0;
 #pragma unroll
@@ -232,22 +255,15 @@ __device__ void producer_role(const Ctx& c, const Params& p, const Work& w, uint
         s_lse[i] = -lv * kLog2e;
         s_d[i] = dv;
       }
-      mbar_arrive(bar_addr(c, BAR_Q_FULL));
+      mbar_arrive(bar_addr(c, BAR_QH_FULL));
     }
     issued_q = t + 1;
-    if (t > 0 && !(ok = wait_warp(c, BAR_DO_EMPTY, (t - 1) & 1))) break;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar_addr(c, BAR_DO_FULL), 4 * 8192);
-      for (int cb = 0; cb < 4; ++cb)
-        tma_load_3d_hint(sbase + L::kDO + cb * 8192, tm_do, bar_addr(c, BAR_DO_FULL), 64 * cb, m0,
-                         bh, reuse);
-    }
-    issued_do = t + 1;
     __syncwarp();
   }
   if (*c.abort) {  // the copies issued last must land before the CTA exits
     wait_drain(c, BAR_KV_FULL, 0);
-    if (issued_q > 0) wait_drain(c, BAR_Q_FULL, (issued_q - 1) & 1);
+    if (issued_q > 0) wait_drain(c, BAR_QH_FULL, (issued_q - 1) & 1);
+    if (issued_qo > 0) wait_drain(c, BAR_QO_FULL, (issued_qo - 1) & 1);
     if (issued_do > 0) wait_drain(c, BAR_DO_FULL, (issued_do - 1) & 1);
   }
 }
@@ -278,12 +294,25 @@ __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t t
   bool ok = wait_warp(c, BAR_KV_FULL, 0);
   for (int t = 0; ok && t < w.T; ++t) {
     const uint32_t ph = t & 1;
-    if (!(ok = wait_warp(c, BAR_Q_FULL, ph))) break;
+    // S^T over the other half of d first (its Q boxes land early), then over
+    // this CTA's half
+    const int ko = 8 * (1 - w.half), kh = 8 * w.half;  // first k-step of each half
+    if (!(ok = wait_warp(c, BAR_QO_FULL, ph))) break;
     tc_fence_after();
     if (leader) {
 #pragma unroll
-      for (int k = 0; k < kD / 16; ++k)
-        mma_ss(tS, sdesc_from_lo(aK + kmaj_k(k)), sdesc_from_lo(bQ + kmaj_q(k)), kIdS, k > 0);
+      for (int k = 0; k < 8; ++k)
+        mma_ss(tS, sdesc_from_lo(aK + kmaj_k(ko + k)), sdesc_from_lo(bQ + kmaj_q(ko + k)), kIdS,
+               k > 0);
+      mma_commit(bar_addr(c, BAR_QO_EMPTY));
+    }
+    if (!(ok = wait_warp(c, BAR_QH_FULL, ph))) break;
+    tc_fence_after();
+    if (leader) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        mma_ss(tS, sdesc_from_lo(aK + kmaj_k(kh + k)), sdesc_from_lo(bQ + kmaj_q(kh + k)), kIdS,
+               1u);
       mma_commit(bar_addr(c, BAR_S_FULL));
     }
     if (!(ok = wait_warp(c, BAR_DO_FULL, ph))) break;
@@ -315,7 +344,7 @@ __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t t
       for (int k = 0; k < kBr / 16; ++k)
         mma_ss(tdK, sdesc_from_lo(kDS + ((32 * k) >> 4)), sdesc_from_lo(mQ + mnmaj(k)), kIdKV,
                (t > 0 || k > 0) ? 1u : 0u);
-      mma_commit(bar_addr(c, BAR_Q_EMPTY));
+      mma_commit(bar_addr(c, BAR_QH_EMPTY));
     }
     // the dQ buffer of tile t was drained with tile t - 2
     const int qb = t & 1;
@@ -450,7 +479,8 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8
     const int m0 = m_block * kBr;
     const bool masked = tile_masked(p, m0, n0);
     const uint32_t ph = t & 1;
-    // P phase (LSE of this tile arrived with Q_FULL, which precedes S_FULL)
+    // P phase: LSE and D of the tile arrive with QH_FULL
+    if (!wait_warp(c, BAR_QH_FULL, ph)) return;
     if (!wait_warp(c, BAR_S_FULL, ph)) return;
     tc_fence_after();
     if (masked)
@@ -591,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar_addr(c, i), 1);
-    mbar_init(bar_addr(c, BAR_Q_FULL), 33);  // expect_tx arrive + 32 LSE/D lanes
+    mbar_init(bar_addr(c, BAR_QH_FULL), 33);  // expect_tx arrive + 32 LSE/D lanes
     mbar_init(bar_addr(c, BAR_P_FULL), 4);   // the 4 softmax warps
     mbar_init(bar_addr(c, BAR_DS_FULL), 4);
     mbar_init(bar_addr(c, BAR_DQ_EMPTY), 4);  // the 4 drain warps
