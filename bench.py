@@ -659,11 +659,13 @@ def kernel_only(args, w):
     between them (inputs prepared first); returns a short JSON-able record."""
     import flashattention_attention_backward_gb300 as attn
     from flashattention_attention_backward_gb300 import runner
-    from flashattention_attention_backward_gb300.inputs import make_inputs
+    from flashattention_attention_backward_gb300.inputs import Workload, make_inputs
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
+    if args.kernel_only == "attn_bwd_d256":  # the d = 256 shape of all_configs
+        w = Workload("causal_gqa_d256", 2, 16, 4, 4096, 256, True, seed_base=20261202 + 6000)
     x = make_inputs(w)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     win = (args.window_left, -1) if args.kernel_only.endswith("_local") else None
@@ -719,7 +721,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=120.0)
     ap.add_argument("--kernel-only", default=None,
-                    choices=["attn_bwd", "attn_fwd", "attn_bwd_local", "attn_fwd_local"],
+                    choices=["attn_bwd", "attn_fwd", "attn_bwd_local", "attn_fwd_local",
+                             "attn_bwd_d256"],
                     help="launch only this kernel W + K times (profiling); no bench line")
     ap.add_argument("--window-left", type=int, default=1023,
                     help="left bound of the causal sliding window of the *_local kernels")
