@@ -682,6 +682,13 @@ def kernel_only(args, w):
         if name == "attn_fwd_local":
             return attn.attn_fwd_local(q, k, v, o, lse, B, H, H_kv, N, d, w.scale, w.causal,
                                        w.softcap, win[0], win[1], stream)
+        if name == "attn_fwd_dropout":
+            return attn.attn_fwd_dropout(q, k, v, o, lse, B, H, H_kv, N, d, w.scale, w.causal,
+                                         w.softcap, args.p_drop, 1234, stream)
+        if name == "attn_bwd_dropout":
+            return attn.attn_bwd_dropout(q, k, v, o, do, lse, bufs.dq_accum, bufs.dk, bufs.dv, B,
+                                         H, H_kv, N, d, w.scale, w.causal, w.softcap, bufs.dpsum,
+                                         args.p_drop, 1234, stream)
         if name == "attn_bwd_local":
             return attn.attn_bwd_local(q, k, v, o, do, lse, bufs.dq_accum, bufs.dk, bufs.dv, B, H,
                                        H_kv, N, d, w.scale, w.causal, w.softcap, bufs.dpsum,
@@ -722,10 +729,12 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=120.0)
     ap.add_argument("--kernel-only", default=None,
                     choices=["attn_bwd", "attn_fwd", "attn_bwd_local", "attn_fwd_local",
-                             "attn_bwd_d256"],
+                             "attn_bwd_d256", "attn_fwd_dropout", "attn_bwd_dropout"],
                     help="launch only this kernel W + K times (profiling); no bench line")
     ap.add_argument("--window-left", type=int, default=1023,
                     help="left bound of the causal sliding window of the *_local kernels")
+    ap.add_argument("--p-drop", type=float, default=0.1,
+                    help="drop probability of the *_dropout kernels")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

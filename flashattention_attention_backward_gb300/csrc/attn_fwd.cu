@@ -354,38 +354,55 @@ __device__ __forceinline__ float tile_max(const Params& p, uint32_t tS, int n0, 
 // One Philox call gives the words of four consecutive query rows of one key,
 // and those rows sit in the four lanes of a quad: lane t of the quad draws
 // the call of key k0 + 4 g + t, and a 4 x 4 transpose by shuffles hands
-// every lane its own row's word of each of the four keys (round k: a lane
-// offers word (t - k) mod 4 and reads from quad lane (t + k) mod 4).
+// every lane its own row's word of each of the four keys. In round k a lane
+// offers word (t - k) mod 4 of its call and reads from quad lane
+// (t + k) mod 4, which offers word t, for key k0 + 4 g + (t + k) mod 4.
+// Everything that depends on t is done with masks, not selects on t: the
+// offered words come from one rotation of the four words by t (two masked
+// swaps), round k's bit goes to the fixed position 4 g + k, and a rotation of
+// every nibble by t at the end moves it to 4 g + (t + k) mod 4.
 __device__ __forceinline__ uint32_t keep_bits32(const Params& p, int qrow, int k0, uint32_t bh) {
   const int lane = threadIdx.x & 31;
-  const int t = lane & 3;
+  const uint32_t t = static_cast<uint32_t>(lane & 3);
   const uint32_t qgrp = static_cast<uint32_t>(qrow) >> 2;
+  const uint32_t m1 = 0u - (t & 1u), m2 = 0u - ((t >> 1) & 1u);
   uint32_t bits = 0;
 #pragma unroll
   for (int g = 0; g < 8; ++g) {
-    const PhiloxOut w = philox4x32_10(qgrp, static_cast<uint32_t>(k0 + 4 * g + t), bh, 0u,
+    const PhiloxOut w = philox4x32_10(qgrp, static_cast<uint32_t>(k0 + 4 * g) + t, bh, 0u,
                                       p.drop.seed_lo, p.drop.seed_hi);
+    // offer[k] = word (t - k) mod 4: the words in the order 0, 3, 2, 1,
+    // rotated by t (t & 1 by one place, t & 2 by two)
+    const uint32_t u[4] = {w.w[0], w.w[3], w.w[2], w.w[1]};
+    uint32_t r1[4], offer[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) r1[k] = (u[(k + 3) & 3] & m1) | (u[k] & ~m1);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) offer[k] = (r1[(k + 2) & 3] & m2) | (r1[k] & ~m2);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int off = (t - k) & 3;
-      const uint32_t give = off == 0 ? w.w[0] : off == 1 ? w.w[1] : off == 2 ? w.w[2] : w.w[3];
       const uint32_t got =
-          k == 0 ? give : __shfl_sync(0xffffffffu, give, (lane & ~3) | ((t + k) & 3));
-      bits |= (got >= p.drop.threshold ? 1u : 0u) << (4 * g + ((t + k) & 3));
+          k == 0 ? offer[0]
+                 : __shfl_sync(0xffffffffu, offer[k], (lane & ~3) | static_cast<int>((t + k) & 3));
+      bits |= (got >= p.drop.threshold ? 1u : 0u) << (4 * g + k);
     }
   }
-  return bits;
+  // nibble bit k -> bit (k + t) mod 4, in all eight nibbles
+  const uint32_t hi_mask = 0x11111111u * ((0xFu << t) & 0xFu);
+  const uint32_t lo_mask = 0x11111111u * (0xFu >> (4u - t));
+  return ((bits << t) & hi_mask) | ((bits >> (4u - t)) & lo_mask);
 }
 
 // P = 2^(x - shift) of one S tile as bf16 pairs over the first half of the
 // buffer; returns the row sum of P (fp32, before rounding and before
-// dropout). With DROP the bf16 values are P o Z / (1 - p) (Z the keep mask);
-// the row sum stays that of P. Keys 32 ch .. 32 ch + 31 land in columns
+// dropout). With DROP the bf16 values are P o Z / (1 - p), Z the keep mask
+// whose bit j of kbits[j / 32] belongs to key n0 + j; the row sum stays that
+// of P. Keys 32 ch .. 32 ch + 31 land in columns
 // 16 ch .. 16 ch + 15, whose S values were read in this or an earlier chunk.
 template <bool SOFTCAP, bool MASKED, bool DROP>
 __device__ __forceinline__ float tile_p(const Params& p, uint32_t tS, int n0, int qrow,
                                         float c_log2, float cap_in, float cap_out, float shift,
-                                        uint32_t bh) {
+                                        const uint32_t (&kbits)[kBn / 32]) {
   const uint64_t c2v = f2_make(SOFTCAP ? cap_in : c_log2, SOFTCAP ? cap_in : c_log2);
   const uint64_t out2 = f2_make(cap_out, cap_out);
   const uint64_t one2 = f2_make(1.f, 1.f), mtwo2 = f2_make(-2.f, -2.f);
@@ -397,8 +414,8 @@ __device__ __forceinline__ float tile_p(const Params& p, uint32_t tS, int n0, in
   for (int c2 = 0; c2 < kBn / 64; ++c2) {
     uint32_t raw[64];
     tmem_ld32x2(tS + c2 * 64, tS + c2 * 64 + 32, raw);
-    const uint32_t kb0 = DROP ? keep_bits32(p, qrow, n0 + c2 * 64, bh) : 0xFFFFFFFFu;
-    const uint32_t kb1 = DROP ? keep_bits32(p, qrow, n0 + c2 * 64 + 32, bh) : 0xFFFFFFFFu;
+    const uint32_t kb0 = DROP ? kbits[2 * c2] : 0xFFFFFFFFu;
+    const uint32_t kb1 = DROP ? kbits[2 * c2 + 1] : 0xFFFFFFFFu;
     uint32_t packed[32];
 #pragma unroll
     for (int u = 0; u < 32; ++u) {
@@ -468,9 +485,17 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint3
   if (nt == 0) return;
   float m_used = -INFINITY, l = 0.f;
   bool ok = true;
+  const uint32_t bh = static_cast<uint32_t>(w.bh);
   for (int t = 0; t < nt; ++t) {
     const int n0 = (w.j0[q] + t) * kBn;
     const int m0 = w.m0[q];
+    // The keep mask depends on no score: it is drawn while the S GEMM of this
+    // block runs, with no tensor-memory rows held in registers, so that many
+    // Philox calls are in flight at once.
+    uint32_t kbits[kBn / 32];
+#pragma unroll
+    for (int i = 0; i < kBn / 32; ++i)
+      kbits[i] = DROP ? keep_bits32(p, qrow, n0 + 32 * i, bh) : 0xFFFFFFFFu;
     // the warpgroup meets at its named barrier below: one decision for all
     ok = named_bar_and(bar_wg, 128, wait(c, BAR_S_FULL + q, t & 1));
     if (!ok) break;
@@ -526,10 +551,10 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint3
     ok = named_bar_and(bar_wg, 128, ok);
     if (!ok) break;
     const float shift = m_used > -INFINITY ? m_used : 0.f;
-    const uint32_t bh = static_cast<uint32_t>(w.bh);
-    l += masked
-             ? tile_p<SOFTCAP, true, DROP>(p, tS, n0, qrow, c_log2, cap_in, cap_out, shift, bh)
-             : tile_p<SOFTCAP, false, DROP>(p, tS, n0, qrow, c_log2, cap_in, cap_out, shift, bh);
+    l += masked ? tile_p<SOFTCAP, true, DROP>(p, tS, n0, qrow, c_log2, cap_in, cap_out, shift,
+                                              kbits)
+                : tile_p<SOFTCAP, false, DROP>(p, tS, n0, qrow, c_log2, cap_in, cap_out, shift,
+                                               kbits);
     tmem_wait_st();
     tc_fence_before();
     named_bar_sync(bar_wg, 128);
