@@ -168,6 +168,34 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- our arm
+def hbm_bytes_preprocess(B, H, N, d):
+    """Algorithmic DRAM bytes of attn_bwd_preprocess: O and dO read (bf16),
+    D written (fp32), dQaccum zeroed (fp32)."""
+    return B * H * N * (2 * d * 2 + 4 + d * 4)
+
+
+def hbm_bytes_finalize(B, H, N, d):
+    """Algorithmic DRAM bytes of attn_bwd_finalize: dQaccum read (fp32), dQ
+    written (bf16)."""
+    return B * H * N * d * (4 + 2)
+
+
+def step_kernels(w, pre_ms, bwd_ms, fin_ms, peaks):
+    """Mean time per launch of each kernel of the step (CUDA events between
+    the launches of up to 200 steps run right after the timed region); the
+    two HBM-bound kernels against the measured copy bandwidth."""
+    mean = lambda xs: sum(xs) / len(xs)  # noqa: E731
+    out = {"attn_bwd": {"ms": mean(bwd_ms), "bound": "tensor"}}
+    for name, xs, nbytes in (
+            ("attn_bwd_preprocess", pre_ms, hbm_bytes_preprocess(w.B, w.H, w.N, w.d)),
+            ("attn_bwd_finalize", fin_ms, hbm_bytes_finalize(w.B, w.H, w.N, w.d))):
+        ms = mean(xs)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms": ms, "bound": "hbm", "bytes": nbytes, "GB/s": gbs,
+                     "peak_GB/s": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"]}
+    return out
+
+
 def run_ours(args, w):
     import flashattention_attention_backward_gb300 as attn
     from flashattention_attention_backward_gb300 import runner
@@ -187,15 +215,21 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
     B, H, H_kv, N, d = w.B, w.H, w.H_kv, w.N, w.d
 
-    def step(ev_pair=None):
+    def step(ev=None):
+        # ev: events around the launches: two (around attn_bwd) or four
+        # (before preprocess, before attn_bwd, after attn_bwd, after finalize)
+        if ev is not None and len(ev) == 4:
+            ev[0].record(stream)
         attn.check(attn.attn_bwd_preprocess(o, do, bufs.dpsum, bufs.dq_accum, B, H, N, d, stream))
-        if ev_pair is not None:
-            ev_pair[0].record(stream)
+        if ev is not None:
+            ev[-3 if len(ev) == 4 else 0].record(stream)
         attn.check(attn.attn_bwd(q, k, v, o, do, lse, bufs.dq_accum, bufs.dk, bufs.dv, B, H, H_kv,
                                  N, d, w.scale, w.causal, w.softcap, bufs.dpsum, stream))
-        if ev_pair is not None:
-            ev_pair[1].record(stream)
+        if ev is not None:
+            ev[-2 if len(ev) == 4 else 1].record(stream)
         attn.check(attn.attn_bwd_finalize(bufs.dq_accum, bufs.dq, w.scale, B, H, N, d, stream))
+        if ev is not None and len(ev) == 4:
+            ev[3].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -204,7 +238,7 @@ def run_ours(args, w):
     if rc != 0 or status != 0:
         raise RuntimeError("device status %d after warm-up" % status)
 
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    kev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2))
            for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank) if rank == 0 else None
@@ -221,7 +255,18 @@ def run_ours(args, w):
     barrier(world)
     clock_info = clocks.stop() if clocks else None
     ms_total = t0.elapsed_time(t1)
-    bwd_ms = [a.elapsed_time(b) for a, b in kev]
+    bwd_ms = [e[0].elapsed_time(e[1]) for e in kev]
+    # each launch of the step on its own: the same steps again, with events
+    # between all three launches (kept out of the headline loop, whose only
+    # events are the two around attn_bwd)
+    kev4 = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4))
+            for _ in range(min(args.steps, 200))]
+    for e in kev4:
+        step(e)
+    torch.cuda.synchronize(dev)
+    pre_ms = [e[0].elapsed_time(e[1]) for e in kev4]
+    bwd4_ms = [e[1].elapsed_time(e[2]) for e in kev4]
+    fin_ms = [e[2].elapsed_time(e[3]) for e in kev4]
     rc, status = attn.attn_device_status(clear=True, stream=stream)
     if rc != 0 or status != 0:
         raise RuntimeError("device status %d after the timed region" % status)
@@ -331,6 +376,7 @@ def run_ours(args, w):
             "kernel": "attn_bwd_kernel<128, causal>",
             "peak_source": "%s burst dense bf16 (MEASURED_PEAKS.json)" % peaks["source"],
         },
+        "kernels": step_kernels(w, pre_ms, bwd4_ms, fin_ms, peaks),
         "clocks": clock_info,
         "gpu_launches": 3 * args.steps,
         "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,

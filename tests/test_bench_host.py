@@ -34,3 +34,32 @@ def test_visible_pairs_closed_forms():
     assert bench.visible_pairs(N, True, -1, -1) == N * (N + 1) // 2
     L = 1023  # causal window of L + 1 keys: row i sees min(i, L) + 1 keys
     assert bench.visible_pairs(N, True, L, -1) == (L + 1) * (L + 2) // 2 + (N - L - 1) * (L + 1)
+
+
+@pytest.mark.parametrize("B,H,N,d", [(2, 32, 4096, 128), (1, 2, 256, 64), (8, 16, 1024, 64)])
+def test_hbm_bytes_of_the_memory_bound_kernels(B, H, N, d):
+    """The algorithmic bytes of preprocess and finalize are the sizes of the
+    tensors each one reads and writes once."""
+    import torch
+
+    def nbytes(shape, dtype):
+        return torch.empty(shape, dtype=dtype, device="meta").nbytes
+
+    o = do = nbytes((B, H, N, d), torch.bfloat16)
+    dpsum = nbytes((B, H, N), torch.float32)
+    dq_accum = nbytes((B, H, N, d), torch.float32)
+    dq = nbytes((B, H, N, d), torch.bfloat16)
+    assert bench.hbm_bytes_preprocess(B, H, N, d) == o + do + dpsum + dq_accum
+    assert bench.hbm_bytes_finalize(B, H, N, d) == dq_accum + dq
+
+
+def test_step_kernels_fractions():
+    class W:
+        B, H, N, d = 2, 32, 4096, 128
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0}
+    k = bench.step_kernels(W, [0.05, 0.05], [0.5, 0.7], [0.04, 0.02], peaks)
+    assert k["attn_bwd"]["ms"] == pytest.approx(0.6)
+    pre = k["attn_bwd_preprocess"]
+    assert pre["GB/s"] == pytest.approx(bench.hbm_bytes_preprocess(2, 32, 4096, 128) / 0.05e-3 / 1e9)
+    assert pre["frac"] == pytest.approx(pre["GB/s"] / 6000.0)
+    assert k["attn_bwd_finalize"]["ms"] == pytest.approx(0.03)
