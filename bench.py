@@ -215,21 +215,20 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
     B, H, H_kv, N, d = w.B, w.H, w.H_kv, w.N, w.d
 
-    def step(ev=None):
-        # ev: events around the launches: two (around attn_bwd) or four
-        # (before preprocess, before attn_bwd, after attn_bwd, after finalize)
-        if ev is not None and len(ev) == 4:
-            ev[0].record(stream)
+    def step(before_pre=None, before_bwd=None, after_bwd=None, after_fin=None):
+        # optional CUDA events recorded between the three launches
+        def mark(e):
+            if e is not None:
+                e.record(stream)
+
+        mark(before_pre)
         attn.check(attn.attn_bwd_preprocess(o, do, bufs.dpsum, bufs.dq_accum, B, H, N, d, stream))
-        if ev is not None:
-            ev[-3 if len(ev) == 4 else 0].record(stream)
+        mark(before_bwd)
         attn.check(attn.attn_bwd(q, k, v, o, do, lse, bufs.dq_accum, bufs.dk, bufs.dv, B, H, H_kv,
                                  N, d, w.scale, w.causal, w.softcap, bufs.dpsum, stream))
-        if ev is not None:
-            ev[-2 if len(ev) == 4 else 1].record(stream)
+        mark(after_bwd)
         attn.check(attn.attn_bwd_finalize(bufs.dq_accum, bufs.dq, w.scale, B, H, N, d, stream))
-        if ev is not None and len(ev) == 4:
-            ev[3].record(stream)
+        mark(after_fin)
 
     for _ in range(args.warmup):
         step()
@@ -249,7 +248,7 @@ def run_ours(args, w):
         time.sleep(0.25)
     t0.record(stream)
     for i in range(args.steps):
-        step(kev[i])
+        step(before_bwd=kev[i][0], after_bwd=kev[i][1])
     t1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -262,7 +261,7 @@ def run_ours(args, w):
     kev4 = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4))
             for _ in range(min(args.steps, 200))]
     for e in kev4:
-        step(e)
+        step(*e)
     torch.cuda.synchronize(dev)
     pre_ms = [e[0].elapsed_time(e[1]) for e in kev4]
     bwd4_ms = [e[1].elapsed_time(e[2]) for e in kev4]
