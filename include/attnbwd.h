@@ -22,10 +22,12 @@
  *    [B, H, N, d]; K, V, dK, dV are [B, H_kv, N, d]; LSE and D are [B, H, N].
  *    bf16 tensors are passed as `void*` (IEEE bfloat16 bit patterns).
  *  * Query head h uses KV head h / (H / H_kv) (H must be a multiple of H_kv).
- *  * d must be 64 or 128 for attn_fwd and the variants of attn_bwd (dropout,
- *    deterministic, allocation-free); 64, 128 or 256 for attn_fwd_ref,
+ *  * d must be 64 or 128 for attn_fwd and its variants, the dropout calls
+ *    (attn_fwd_ref_dropout with p_drop > 0 included) and the deterministic and
+ *    allocation-free backward; 64, 128 or 256 for attn_fwd_ref,
  *    attn_fwd_ref_local, attn_bwd and attn_bwd_local; preprocess and finalize
- *    accept any d that is a multiple of 4.
+ *    accept any d that is a multiple of 4. Other values return
+ *    ATTN_ERR_UNSUPPORTED.
  *  * Every pointer must be 16-byte aligned (the kernels use TMA and 16-byte
  *    vector accesses).
  *  * `scale` is tau (usually 1/sqrt(d)); the logit is tau * q.k.

@@ -131,3 +131,42 @@ def test_other_entry_points_validation(lib):
         lib.ATTN_ERR_UNSUPPORTED
     # preprocess may skip the accumulator
     assert lib.attn_bwd_preprocess(a, a, a, None, 1, 1, 0, 64) == lib.ATTN_OK
+
+
+def test_dropout_and_d256_validation(lib):
+    a = FAKE
+    ok9 = (a, a, a, a, a, a, a, a, a)
+    seed = 1234
+    # drop probability outside [0, 1)
+    for p in (-0.1, 1.0, 1.5, float("nan")):
+        assert lib.attn_fwd_dropout(a, a, a, a, a, 1, 1, 1, 64, 64, 0.1, 0, 0.0, p, seed) == \
+            lib.ATTN_ERR_SHAPE
+        assert lib.attn_fwd_ref_dropout(a, a, a, a, a, 1, 1, 1, 64, 64, 0.1, 0, 0.0, p, seed) == \
+            lib.ATTN_ERR_SHAPE
+        assert lib.attn_bwd_dropout(*ok9, 1, 2, 2, 128, 128, 0.1, 1, 0.0, a, p, seed) == \
+            lib.ATTN_ERR_SHAPE
+    # null pointers
+    assert lib.attn_fwd_dropout(0, a, a, a, a, 1, 1, 1, 64, 64, 0.1, 0, 0.0, 0.1, seed) == \
+        lib.ATTN_ERR_NULL
+    assert lib.attn_bwd_dropout(*ok9, 1, 2, 2, 128, 128, 0.1, 1, 0.0, 0, 0.1, seed) == \
+        lib.ATTN_ERR_NULL
+    # dropout is not offered for d = 256 (no backward replays it there)
+    assert lib.attn_fwd_dropout(a, a, a, a, a, 1, 1, 1, 64, 256, 0.1, 0, 0.0, 0.1, seed) == \
+        lib.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_fwd_ref_dropout(a, a, a, a, a, 1, 1, 1, 64, 256, 0.1, 0, 0.0, 0.1, seed) == \
+        lib.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_bwd_dropout(*ok9, 1, 2, 2, 128, 256, 0.1, 1, 0.0, a, 0.1, seed) == \
+        lib.ATTN_ERR_UNSUPPORTED
+    # ... while p_drop = 0 is the plain forward, which takes d = 256
+    assert lib.attn_fwd_ref_dropout(a, a, a, a, a, 0, 1, 1, 64, 256, 0.1, 0, 0.0, 0.0, seed) == \
+        lib.ATTN_OK
+    # d = 256: the plain and local backward accept it, the other variants do not
+    assert lib.attn_bwd(*ok9, 0, 2, 2, 128, 256, 0.1, 1, 0.0, a) == lib.ATTN_OK
+    assert lib.attn_bwd_local(*ok9, 0, 2, 2, 128, 256, 0.1, 1, 0.0, a, 64, -1) == lib.ATTN_OK
+    assert lib.attn_bwd_deterministic(*ok9, 1, 2, 2, 128, 256, 0.1, 1, 0.0, a) == \
+        lib.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_fwd(a, a, a, a, a, 1, 1, 1, 64, 256, 0.1, 0, 0.0) == lib.ATTN_ERR_UNSUPPORTED
+    # empty problems succeed without touching the device
+    assert lib.attn_fwd_dropout(a, a, a, a, a, 0, 1, 1, 64, 64, 0.1, 0, 0.0, 0.1, seed) == \
+        lib.ATTN_OK
+    assert lib.attn_bwd_dropout(*ok9, 1, 2, 2, 0, 128, 0.1, 1, 0.0, a, 0.1, seed) == lib.ATTN_OK
