@@ -1098,10 +1098,15 @@ int dispatch(const Maps& m, const Params& p, cudaStream_t s, int d, bool cs, boo
 
 // Shared by attn_bwd (dQ added into dq_target) and attn_bwd_deterministic
 // (dQ tiles stored into the partials buffer dq_target).
+// `before_launch`, when given, runs once every argument check and tensor-map
+// encoding has passed, right before the kernel is enqueued (d = 64 and 128
+// only); a non-zero return ends the call with that code and nothing more is
+// enqueued.
 int run(const void* q, const void* k, const void* v, const void* dO, const float* lse,
         float* dq_target, void* dk, void* dv, int B, int H, int H_kv, int N, int d, float scale,
         int causal, float softcap, const float* dpsum, void* stream, bool det, float p_drop = 0.f,
-        unsigned long long seed = 0, int window_left = -1, int window_right = -1) {
+        unsigned long long seed = 0, int window_left = -1, int window_right = -1,
+        int (*before_launch)(void*) = nullptr, void* before_ctx = nullptr) {
   if (!q || !k || !v || !dO || !lse || !dq_target || !dk || !dv || !dpsum) return ATTN_ERR_NULL;
   int rc = check_shape(B, H, H_kv, N, d);
   if (rc != ATTN_OK) return rc;
@@ -1113,6 +1118,7 @@ int run(const void* q, const void* k, const void* v, const void* dO, const float
       !aligned16(dq_target) || !aligned16(dk) || !aligned16(dv) || !aligned16(dpsum))
     return ATTN_ERR_ALIGN;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (d == 256 && before_launch != nullptr) return ATTN_ERR_UNSUPPORTED;
   if (d == 256)
     return bwd256_run(q, k, v, dO, lse, dq_target, dk, dv, B, H, H_kv, N, scale, causal, softcap,
                       dpsum, window_left, window_right, as_stream(stream));
@@ -1158,6 +1164,10 @@ int run(const void* q, const void* k, const void* v, const void* dO, const float
       !encode_bf16_3d(&m.dv, dv, d, N, hk, kBc))
     return ATTN_ERR_LAUNCH;
 
+  if (before_launch != nullptr) {
+    rc = before_launch(before_ctx);
+    if (rc != ATTN_OK) return rc;
+  }
   cudaStream_t s = as_stream(stream);
   const bool cs = causal != 0;
   if (drop) return dispatch<false, true>(m, p, s, d, cs, cap);  // not combined with det
@@ -1205,6 +1215,18 @@ extern "C" int attn_bwd_deterministic(const void* q, const void* k, const void* 
   return bwd::run(q, k, v, dO, lse, dq_partials, dk, dv, B, H, H_kv, N, d, scale, causal,
                   softcap, dpsum, stream, true);
 }
+
+namespace attn {
+
+int bwd_run_hooked(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                   float* dq_accum, void* dk, void* dv, int B, int H, int H_kv, int N, int d,
+                   float scale, int causal, float softcap, const float* dpsum, void* stream,
+                   int (*before_launch)(void*), void* ctx) {
+  return bwd::run(q, k, v, dO, lse, dq_accum, dk, dv, B, H, H_kv, N, d, scale, causal, softcap,
+                  dpsum, stream, false, 0.f, 0, -1, -1, before_launch, ctx);
+}
+
+}  // namespace attn
 
 extern "C" int attn_device_status(int* status, int clear, void* stream) {
   if (!status) return ATTN_ERR_NULL;

@@ -148,4 +148,14 @@ int bwd256_run(const void* q, const void* k, const void* v, const void* dO, cons
                int causal, float softcap, const float* dpsum, int window_left, int window_right,
                cudaStream_t s);
 
+// attn_bwd (d = 64 or 128) with a hook: before_launch(ctx) runs after every
+// argument check and tensor-map encoding has passed and right before the main
+// kernel is enqueued, so a caller can enqueue work that must precede the
+// kernel only once the whole call is known to be valid. A non-zero return from
+// the hook ends the call with that code; d = 256 returns ATTN_ERR_UNSUPPORTED.
+int bwd_run_hooked(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                   float* dq_accum, void* dk, void* dv, int B, int H, int H_kv, int N, int d,
+                   float scale, int causal, float softcap, const float* dpsum, void* stream,
+                   int (*before_launch)(void*), void* ctx);
+
 }  // namespace attn

@@ -241,7 +241,12 @@ int attn_bwd_finalize(const float* dq_accum, void* dq, float scale, int B, int H
  * Scratch: the fp32 dQ accumulator and D live in one file-scope device array
  * of 8,388,608 floats (32 MiB) that every device loading the library keeps
  * until the process exits. A problem needs B*H*N*d + B*H*N floats; larger
- * problems return ATTN_ERR_TOO_LARGE and nothing is launched.
+ * problems return ATTN_ERR_TOO_LARGE.
+ * Every check of the three steps (pointers, shapes, d = 64 or 128, scale
+ * finite and non-zero, softcap not NaN, 16-byte alignment of all nine
+ * pointers, the size limit) runs before the first launch: an argument error
+ * enqueues nothing and leaves the array untouched. Only ATTN_ERR_LAUNCH, an
+ * error CUDA reports at a launch, can come after a step was enqueued.
  * All calls share that array: calls whose GPU work overlaps (unordered
  * streams, several host threads) race and give wrong results. The first call
  * on a device looks up the array's address with that device current; make it

@@ -170,3 +170,30 @@ def test_dropout_and_d256_validation(lib):
     assert lib.attn_fwd_dropout(a, a, a, a, a, 0, 1, 1, 64, 64, 0.1, 0, 0.0, 0.1, seed) == \
         lib.ATTN_OK
     assert lib.attn_bwd_dropout(*ok9, 1, 2, 2, 0, 128, 0.1, 1, 0.0, a, 0.1, seed) == lib.ATTN_OK
+
+
+def test_noalloc_argument_validation(lib):
+    """attn_bwd_noalloc runs every check of its three steps before its first
+    launch, so each of these returns its code without touching a device."""
+    a = FAKE
+    ok9 = (a, a, a, a, a, a, a, a, a)
+    shape = (1, 2, 2, 128, 128)
+    assert lib.attn_bwd_noalloc(0, *ok9[1:], *shape, 0.1, 1, 0.0) == lib.ATTN_ERR_NULL
+    for bad_scale in (float("nan"), float("inf"), -float("inf"), 0.0):
+        assert lib.attn_bwd_noalloc(*ok9, *shape, bad_scale, 1, 0.0) == lib.ATTN_ERR_SHAPE
+    assert lib.attn_bwd_noalloc(*ok9, *shape, 0.1, 1, float("nan")) == lib.ATTN_ERR_SHAPE
+    # every one of the nine pointers is checked for 16-byte alignment, o and
+    # the output dq included (the main kernel alone never sees them)
+    for i in range(9):
+        bad = list(ok9)
+        bad[i] = a + 8
+        assert lib.attn_bwd_noalloc(*bad, *shape, 0.1, 1, 0.0) == lib.ATTN_ERR_ALIGN, i
+    assert lib.attn_bwd_noalloc(*ok9, 1, 2, 2, 128, 256, 0.1, 1, 0.0) == lib.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_bwd_noalloc(*ok9, 1, 3, 2, 128, 128, 0.1, 1, 0.0) == lib.ATTN_ERR_SHAPE
+    # the array holds 8,388,608 floats and a problem needs B*H*N*(d + 1):
+    # N = 65028 at B = H = 1, d = 128 is one row more than fits (65027 rows)
+    assert 65027 * 129 <= 8388608 < 65028 * 129
+    assert lib.attn_bwd_noalloc(*ok9, 1, 1, 1, 65028, 128, 0.1, 1, 0.0) == lib.ATTN_ERR_TOO_LARGE
+    assert 129055 * 65 <= 8388608 < 129056 * 65
+    assert lib.attn_bwd_noalloc(*ok9, 1, 1, 1, 129056, 64, 0.1, 0, 0.0) == lib.ATTN_ERR_TOO_LARGE
+    assert lib.attn_bwd_noalloc(*ok9, 0, 2, 2, 128, 128, 0.1, 1, 0.0) == lib.ATTN_OK
