@@ -381,6 +381,62 @@ def test_keep_mask_rate_and_layout():
     assert dropout_keep_mask(1, 0, 8, 8, 0.0).all()
 
 
+# The keep threshold for drop probability p is round(p32 * 2^32), half up,
+# where p32 is the float32 value of p: the library receives p as a C float,
+# and the keep decision is an integer decision both sides must take alike.
+# Values worked out by hand from float32 bit patterns:
+#   0.5  = 2^-1                 -> 2^31
+#   0.25 = 2^-2                 -> 2^30
+#   float32(0.1) = 13421773 * 2^-27 (0x3DCCCCCD) -> 13421773 * 2^5 = 429496736
+#       (a float64 p would give 0.1 * 2^32 = 429496729.6 -> 429496730)
+#   2^-33                       -> 0.5 exactly -> 1 (half up; half-even and
+#                                  truncation both give 0)
+#   3 * 2^-33                   -> 1.5 -> 2
+#   1 - 2^-24 (largest float32 below 1) -> 2^32 - 2^8 = 4294967040
+#   0                           -> 0 (every word keeps)
+KEEP_THRESHOLD_PINS = [
+    (0.5, 2**31),
+    (0.25, 2**30),
+    (np.float32(0.1), 429496736),
+    (0.1, 429496736),
+    (2.0**-33, 1),
+    (3 * 2.0**-33, 2),
+    (1.0 - 2.0**-24, 4294967040),
+    (0.0, 0),
+]
+
+
+@pytest.mark.parametrize("p,want", KEEP_THRESHOLD_PINS)
+def test_keep_threshold_hand_values(p, want):
+    assert keep_threshold(p) == want
+
+
+def test_keep_threshold_float32_reading_differs_from_float64():
+    # 0.1 as float64 times 2^32 rounds to 429496730; the float32 reading taken
+    # here must not give that
+    assert keep_threshold(0.1) != 429496730
+    assert keep_threshold(np.float64(0.1)) == keep_threshold(np.float32(0.1))
+
+
+def test_keep_mask_seed_words_and_threshold_edge():
+    """A seed of 2^40 + 7 splits into key (7, 256); a word equal to the
+    threshold keeps its element and one below it drops (u >= threshold)."""
+    seed, bh, p = 2**40 + 7, 5, 0.2
+    keep = dropout_keep_mask(seed, bh, 12, 9, p)
+    thr = keep_threshold(p)
+    for i in range(12):
+        for j in range(9):
+            w = philox4x32_10(i // 4, j, bh, 0, 7, 256)
+            assert keep[i, j] == (int(w[i % 4]) >= thr)
+    # choose p so that the threshold equals one of the words exactly: that
+    # element is kept, and with the threshold one above it, dropped
+    w00 = int(philox4x32_10(0, 0, bh, 0, 7, 256)[0])
+    p_eq = float(np.float32(w00 / 2.0**32))
+    t_eq = keep_threshold(p_eq)
+    assert dropout_keep_mask(seed, bh, 1, 1, p_eq)[0, 0] == (w00 >= t_eq)
+    assert abs(t_eq - w00) <= 256  # float32 p resolves the word to 2^8 at most
+
+
 DROP_CASES = [
     # B, H, H_kv, N, d, causal, softcap, p_drop
     (1, 1, 1, 5, 2, False, 0.0, 0.4),
