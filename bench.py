@@ -22,7 +22,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -44,7 +43,7 @@ UNIT = "TFLOPS"
 PEAK_FALLBACK = {"bf16_tflops": 1890.0, "hbm_gbs": 6800.0, "source": "fallback"}
 KERNEL_SOURCES = ["flashattention_attention_backward_gb300/csrc/attn_bwd.cu",
                   "flashattention_attention_backward_gb300/csrc/sm103_ptx.cuh"]
-TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "attn_bwd_causal_gqa_ncu.md")
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "attn_bwd_causal_gqa_traffic.json")
 
 
 # ---------------------------------------------------------------- helpers
@@ -98,17 +97,15 @@ def kernel_source_hash():
 
 
 def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
+    """DRAM bytes per launch from the committed ncu counters of the timed
+    kernel, if they were taken on the current kernel source (else None)."""
     try:
-        text = open(TRAFFIC_PROFILE).read()
-    except OSError:
+        with open(TRAFFIC_PROFILE) as f:
+            rec = json.load(f)
+        sha, nbytes = rec["kernel_source_sha256"], float(rec["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError, TypeError):
         return None
-    m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
-    m_bytes = re.search(r"dram_bytes_per_launch_full_workload:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
-        return None
-    return float(m_bytes.group(1))
+    return nbytes if sha == kernel_source_hash() else None
 
 
 class ClockSampler:
