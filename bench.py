@@ -480,10 +480,28 @@ def d256_timing(dev, peak, iters, warmup):
         raise RuntimeError("device status %d on the d = 256 timing" % status)
     ms = sorted(a.elapsed_time(b) for a, b in ts)[len(ts) // 2]
     tf = w.flops() / (ms * 1e-3) / 1e12
+    # the tensor-core forward at d = 256 (one query tile per CTA): 2 GEMMs of
+    # 2 N^2 d per head, halved for causal
+    fts = []
+    for i in range(warmup + iters):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        attn.check(attn.attn_fwd(q, k, v, o, lse, w.B, w.H, w.H_kv, w.N, w.d, w.scale, True, 0.0,
+                                 stream))
+        e1.record(stream)
+        if i >= warmup:
+            fts.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    rc, status = attn.attn_device_status(clear=True, stream=stream)
+    if rc != 0 or status != 0:
+        raise RuntimeError("device status %d on the d = 256 forward timing" % status)
+    fms = sorted(a.elapsed_time(b) for a, b in fts)[len(fts) // 2]
+    ftf = w.flops() * 2 / 5 / (fms * 1e-3) / 1e12
     del x, q, k, v, do, o, lse, bufs
     torch.cuda.empty_cache()
     return {"B": w.B, "H": w.H, "H_kv": w.H_kv, "N": w.N, "d": w.d, "causal": True,
-            "bwd_ms": ms, "tflops": tf, "frac_of_peak": tf / peak}
+            "bwd_ms": ms, "tflops": tf, "frac_of_peak": tf / peak,
+            "fwd_ms": fms, "fwd_tflops": ftf, "fwd_frac_of_peak": ftf / peak}
 
 
 def variant_timing(dev, peak, iters, warmup, p_drop=0.1, seed=1234):
@@ -706,7 +724,7 @@ def kernel_only(args, w):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
-    if args.kernel_only == "attn_bwd_d256":  # the d = 256 shape of all_configs
+    if args.kernel_only in ("attn_bwd_d256", "attn_fwd_d256"):  # the d = 256 shape of all_configs
         w = Workload("causal_gqa_d256", 2, 16, 4, 4096, 256, True, seed_base=20261202 + 6000)
     x = make_inputs(w)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
@@ -718,7 +736,7 @@ def kernel_only(args, w):
 
     def launch():
         name = args.kernel_only
-        if name == "attn_fwd":
+        if name in ("attn_fwd", "attn_fwd_d256"):
             return attn.attn_fwd(q, k, v, o, lse, B, H, H_kv, N, d, w.scale, w.causal, w.softcap,
                                  stream)
         if name == "attn_fwd_local":
@@ -771,7 +789,8 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=120.0)
     ap.add_argument("--kernel-only", default=None,
                     choices=["attn_bwd", "attn_fwd", "attn_bwd_local", "attn_fwd_local",
-                             "attn_bwd_d256", "attn_fwd_dropout", "attn_bwd_dropout"],
+                             "attn_bwd_d256", "attn_fwd_d256", "attn_fwd_dropout",
+                             "attn_bwd_dropout"],
                     help="launch only this kernel W + K times (profiling); no bench line")
     ap.add_argument("--window-left", type=int, default=1023,
                     help="left bound of the causal sliding window of the *_local kernels")

@@ -1110,8 +1110,7 @@ int run(const void* q, const void* k, const void* v, const void* dO, const float
   if (!q || !k || !v || !dO || !lse || !dq_target || !dk || !dv || !dpsum) return ATTN_ERR_NULL;
   int rc = check_shape(B, H, H_kv, N, d);
   if (rc != ATTN_OK) return rc;
-  // d = 256: plain and local-window calls only (its own kernel)
-  if (d != 64 && d != 128 && !(d == 256 && !det && p_drop == 0.f)) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;  // d = 256: its own kernel
   if (!std::isfinite(scale) || scale == 0.f || std::isnan(softcap)) return ATTN_ERR_SHAPE;
   if (!(p_drop >= 0.f && p_drop < 1.f)) return ATTN_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
@@ -1119,9 +1118,16 @@ int run(const void* q, const void* k, const void* v, const void* dO, const float
     return ATTN_ERR_ALIGN;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
   if (d == 256 && before_launch != nullptr) return ATTN_ERR_UNSUPPORTED;
-  if (d == 256)
+  if (d == 256) {
+    // dQ partials: one tile of 128 query rows per (query block, key block)
+    // pair, as for d <= 128
+    const long long mb = (N + kBr - 1) / kBr, nb = (N + kBc - 1) / kBc;
+    const long long pairs256 = causal ? mb * (mb + 1) / 2 : mb * nb;
+    if (det && static_cast<long long>(B) * H * pairs256 > 0x7fffffffLL) return ATTN_ERR_TOO_LARGE;
     return bwd256_run(q, k, v, dO, lse, dq_target, dk, dv, B, H, H_kv, N, scale, causal, softcap,
-                      dpsum, window_left, window_right, as_stream(stream));
+                      dpsum, window_left, window_right, det, static_cast<int>(pairs256), p_drop,
+                      seed, as_stream(stream));
+  }
 
   Params p;
   p.lse = lse;

@@ -17,6 +17,11 @@
 //   dQ_i[:, half] += dS K_j[:, half]      (transposed: dQ^T = K^T dS^T,
 //                                          fp32 TMA reductions)
 //
+// Template flags as in the d <= 128 kernel: DROP replays the dropout keep
+// mask of philox.cuh (P^T for dV is P o Z / (1 - p), and dP passes through
+// the same mask before dS); DET stores each dQ tile into the partials
+// workspace of attn_bwd_deterministic instead of adding it.
+//
 // S and dP are recomputed by the CTAs of both halves: seven GEMM-equivalents
 // of 2 * 128 * 64 * 128 flops per tile and half instead of five.
 //
@@ -43,6 +48,7 @@
 #include <cuda_bf16.h>
 
 #include "attn_common.cuh"
+#include "philox.cuh"
 #include "sm103_ptx.cuh"
 
 namespace attn {
@@ -112,6 +118,12 @@ struct Params {
   // key j is visible to query i iff i - win_left <= j <= i + win_right (the
   // causal mask is win_right = 0; an unbounded side holds N)
   int win_left, win_right;
+  // DET: dQ tiles go to partials [B*H*pairs, 128, 256]; the pair of query
+  // block m (128 rows) and key block n is m (m + 1) / 2 + n (causal) or
+  // m * n_blocks + n, and a 64-query tile fills rows (m0 mod 128) .. + 63
+  int pairs;
+  int causal;
+  Dropout drop;  // DROP: keep mask of philox.cuh
 };
 
 struct Work {
@@ -369,10 +381,14 @@ __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t t
 }
 
 // ------------------------------------------------------------------ softmax
-template <bool SOFTCAP, bool MASKED>
+// With DROP, the keep bits of the thread's 64 query columns are drawn in the
+// P phase (one Philox call per four queries of its key) and kept in km[] for
+// the dS phase.
+template <bool SOFTCAP, bool MASKED, bool DROP>
 __device__ __forceinline__ void softmax_tile(const Params& p, uint8_t* smem, uint32_t sbase,
                                              uint32_t tS, uint32_t tdP, int r, int key, int m0,
-                                             uint64_t (&pk)[32], bool dp_phase) {
+                                             uint64_t (&pk)[32], uint32_t (&km)[2], uint32_t bh,
+                                             bool dp_phase) {
   using L = Layout;
   const float* s_lse = reinterpret_cast<const float*>(smem + L::kLSE);
   const float* s_d = reinterpret_cast<const float*>(smem + L::kDsum);
@@ -387,6 +403,19 @@ __device__ __forceinline__ void softmax_tile(const Params& p, uint8_t* smem, uin
                    mtwo2 = f2_make(-2.f, -2.f);
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
+      if (DROP) {
+        uint32_t bits = 0;
+#pragma unroll
+        for (int g4 = 0; g4 < 8; ++g4) {  // queries m0 + 32 pass + 4 g4 .. + 3
+          const PhiloxOut rr = philox4x32_10(
+              static_cast<uint32_t>((m0 + 32 * pass + 4 * g4) >> 2), static_cast<uint32_t>(key),
+              bh, 0u, p.drop.seed_lo, p.drop.seed_hi);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            bits |= (rr.w[e] >= p.drop.threshold ? 1u : 0u) << (4 * g4 + e);
+        }
+        km[pass] = bits;
+      }
       uint32_t raw[32];
       tmem_ld32(tS + 32 * pass, raw);
 #pragma unroll
@@ -421,6 +450,11 @@ __device__ __forceinline__ void softmax_tile(const Params& p, uint8_t* smem, uin
             kp[e] = ok ? kp[e] : 0.f;
           }
         }
+        if (DROP) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            pr[e] = (km[pass] >> (2 * u + e)) & 1u ? pr[e] * p.drop.inv_keep : 0.f;
+        }
         raw[u] = pack_bf16x2(pr[0], pr[1]);
         pk[16 * pass + u] = f2_make(kp[0], kp[1]);
       }
@@ -447,7 +481,15 @@ __device__ __forceinline__ void softmax_tile(const Params& p, uint8_t* smem, uin
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
       const int j = 32 * hh + 2 * u;
-      const uint64_t dp2 = f2_make(raw[2 * u], raw[2 * u + 1]);
+      uint32_t dp0 = raw[2 * u], dp1 = raw[2 * u + 1];
+      if (DROP) {
+        dp0 = (km[hh] >> (2 * u)) & 1u ? __float_as_uint(__uint_as_float(dp0) * p.drop.inv_keep)
+                                       : 0u;
+        dp1 = (km[hh] >> (2 * u + 1)) & 1u
+                  ? __float_as_uint(__uint_as_float(dp1) * p.drop.inv_keep)
+                  : 0u;
+      }
+      const uint64_t dp2 = f2_make(dp0, dp1);
       const uint64_t dd2 = f2_make(s_d[j], s_d[j + 1]);
       const uint64_t r2 =
           f2_mul(pk[16 * hh + u], SOFTCAP ? f2_sub(dd2, dp2) : f2_sub(dp2, dd2));
@@ -462,7 +504,7 @@ __device__ __forceinline__ void softmax_tile(const Params& p, uint8_t* smem, uin
   }
 }
 
-template <bool SOFTCAP>
+template <bool SOFTCAP, bool DROP>
 __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8_t* smem,
                              uint32_t sbase, uint32_t tmem) {
   const int warp = threadIdx.x >> 5;
@@ -473,10 +515,12 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8
   const int n0 = w.n_block * kBc;
   const int key = n0 + r;
   uint64_t pk[32];
+  uint32_t km[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};  // dropout keep bits of the 64 columns
   for (int t = 0; t < w.T; ++t) {
     int h, m_block;
     tile_coord(w, t, h, m_block);
     const int m0 = m_block * kBr;
+    const uint32_t bh = static_cast<uint32_t>(w.b * p.H + h);
     const bool masked = tile_masked(p, m0, n0);
     const uint32_t ph = t & 1;
     // P phase: LSE and D of the tile arrive with QH_FULL
@@ -484,9 +528,9 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8
     if (!wait_warp(c, BAR_S_FULL, ph)) return;
     tc_fence_after();
     if (masked)
-      softmax_tile<SOFTCAP, true>(p, smem, sbase, tS, tdP, r, key, m0, pk, false);
+      softmax_tile<SOFTCAP, true, DROP>(p, smem, sbase, tS, tdP, r, key, m0, pk, km, bh, false);
     else
-      softmax_tile<SOFTCAP, false>(p, smem, sbase, tS, tdP, r, key, m0, pk, false);
+      softmax_tile<SOFTCAP, false, DROP>(p, smem, sbase, tS, tdP, r, key, m0, pk, km, bh, false);
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
@@ -496,9 +540,9 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8
     if (t > 0 && !wait_warp(c, BAR_DS_FREE, (t - 1) & 1)) return;
     tc_fence_after();
     if (masked)
-      softmax_tile<SOFTCAP, true>(p, smem, sbase, tS, tdP, r, key, m0, pk, true);
+      softmax_tile<SOFTCAP, true, DROP>(p, smem, sbase, tS, tdP, r, key, m0, pk, km, bh, true);
     else
-      softmax_tile<SOFTCAP, false>(p, smem, sbase, tS, tdP, r, key, m0, pk, true);
+      softmax_tile<SOFTCAP, false, DROP>(p, smem, sbase, tS, tdP, r, key, m0, pk, km, bh, true);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncwarp();
@@ -514,6 +558,7 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8
 // dO buffers and TMA stores.
 constexpr int kBarDrain = 1;  // named barrier of the drain warpgroup
 
+template <bool DET>
 __device__ void drain_role(const Ctx& c, const Params& p, const Work& w, uint32_t sbase,
                            uint32_t tmem, const CUtensorMap* tm_dq, const CUtensorMap* tm_dk,
                            const CUtensorMap* tm_dv) {
@@ -549,7 +594,14 @@ __device__ void drain_role(const Ctx& c, const Params& p, const Work& w, uint32_
       fence_proxy_async_smem();
       named_bar_sync(kBarDrain, 128);
       const int row = m0 + 32 * ch;
-      if (leader && row < p.N) {
+      if (DET) {
+        if (leader) {
+          const int m = m0 >> 7, n = w.n_block;
+          const int pi = p.causal ? (m * (m + 1) >> 1) + n : m * p.n_blocks + n;
+          tma_store_3d(tm_dq, stage, kDh * w.half, (m0 & 127) + 32 * ch, bh * p.pairs + pi);
+          bulk_commit_group();
+        }
+      } else if (leader && row < p.N) {
         tma_reduce_add_3d(tm_dq, stage, kDh * w.half, row, bh);
         bulk_commit_group();
       }
@@ -599,7 +651,7 @@ __device__ void drain_role(const Ctx& c, const Params& p, const Work& w, uint32_
 }
 
 // ------------------------------------------------------------------ kernel
-template <bool SOFTCAP>
+template <bool SOFTCAP, bool DET, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd256_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -643,9 +695,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     mma_role(c, w, sbase, tmem);
   } else if (warp >= 4 && warp < 8) {
-    softmax_role<SOFTCAP>(c, p, w, smem, sbase, tmem);
+    softmax_role<SOFTCAP, DROP>(c, p, w, smem, sbase, tmem);
   } else if (warp >= 8) {
-    drain_role(c, p, w, sbase, tmem, &tm_dq, &tm_dk, &tm_dv);
+    drain_role<DET>(c, p, w, sbase, tmem, &tm_dq, &tm_dk, &tm_dv);
   }
   tc_fence_before();
   __syncthreads();
@@ -655,9 +707,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool SOFTCAP>
+template <bool SOFTCAP, bool DET, bool DROP>
 int launch(const CUtensorMap (&m)[7], const Params& p, long long grid, cudaStream_t s) {
-  auto kern = attn_bwd256_kernel<SOFTCAP>;
+  auto kern = attn_bwd256_kernel<SOFTCAP, DET, DROP>;
   static std::atomic<bool> configured[kMaxTrackedDevices];
   if (!set_smem_limit_once(kern, Layout::kBytes, configured)) return ATTN_ERR_LAUNCH;
   kern<<<static_cast<unsigned>(grid), kThreads, Layout::kBytes, s>>>(m[0], m[1], m[2], m[3],
@@ -681,12 +733,14 @@ int bwd256_status(int* status, bool clear) {
   return ATTN_OK;
 }
 
-// attn_bwd (and attn_bwd_local) with d = 256: the arguments have been checked
-// by the caller (pointers, shape, alignment, scale), B, H, N > 0.
+// attn_bwd (and its local, dropout and deterministic forms) with d = 256:
+// the arguments have been checked by the caller (pointers, shape, alignment,
+// scale, drop probability), B, H, N > 0. With det, dq_target is the partials
+// workspace (`pairs` tiles per query head), else the dQ accumulator.
 int bwd256_run(const void* q, const void* k, const void* v, const void* dO, const float* lse,
-               float* dq_accum, void* dk, void* dv, int B, int H, int H_kv, int N, float scale,
+               float* dq_target, void* dk, void* dv, int B, int H, int H_kv, int N, float scale,
                int causal, float softcap, const float* dpsum, int window_left, int window_right,
-               cudaStream_t s) {
+               bool det, int pairs, float p_drop, unsigned long long seed, cudaStream_t s) {
   using namespace bwd256;
   Params p;
   p.lse = lse;
@@ -702,16 +756,27 @@ int bwd256_run(const void* q, const void* k, const void* v, const void* dO, cons
   p.softcap = cap ? softcap : 0.f;
   p.win_left = (window_left < 0 || window_left > N) ? N : window_left;
   p.win_right = causal ? 0 : ((window_right < 0 || window_right > N) ? N : window_right);
+  p.pairs = pairs;
+  p.causal = causal != 0 ? 1 : 0;
+  p.drop.seed_lo = static_cast<uint32_t>(seed);
+  p.drop.seed_hi = static_cast<uint32_t>(seed >> 32);
+  p.drop.threshold = dropout_threshold(p_drop);
+  p.drop.inv_keep = 1.f / (1.f - p_drop);
   const long long grid = 2LL * p.n_blocks * H_kv * B;
   if (grid > 0x7fffffffLL) return ATTN_ERR_TOO_LARGE;
   CUtensorMap m[7];  // q, k, v, dO, dq (reduce), dk, dv (store)
   const long long hq = static_cast<long long>(B) * H, hk = static_cast<long long>(B) * H_kv;
   if (!encode_bf16_3d(&m[0], q, kD, N, hq, kBr) || !encode_bf16_3d(&m[1], k, kD, N, hk, kBc) ||
       !encode_bf16_3d(&m[2], v, kD, N, hk, kBc) || !encode_bf16_3d(&m[3], dO, kD, N, hq, kBr) ||
-      !encode_f32_3d(&m[4], dq_accum, kD, N, hq, 32, kDh) ||
+      !(det ? encode_f32_3d(&m[4], dq_target, kD, 128, hq * pairs, 32, kDh)
+            : encode_f32_3d(&m[4], dq_target, kD, N, hq, 32, kDh)) ||
       !encode_bf16_3d(&m[5], dk, kD, N, hk, kBc) || !encode_bf16_3d(&m[6], dv, kD, N, hk, kBc))
     return ATTN_ERR_LAUNCH;
-  return cap ? launch<true>(m, p, grid, s) : launch<false>(m, p, grid, s);
+  if (p_drop > 0.f)  // not combined with det
+    return cap ? launch<true, false, true>(m, p, grid, s) : launch<false, false, true>(m, p, grid, s);
+  if (det)
+    return cap ? launch<true, true, false>(m, p, grid, s) : launch<false, true, false>(m, p, grid, s);
+  return cap ? launch<true, false, false>(m, p, grid, s) : launch<false, false, false>(m, p, grid, s);
 }
 
 }  // namespace attn

@@ -141,12 +141,14 @@ int fwd_status(int* status, bool clear);
 // The same for the d = 256 backward kernel (attn_bwd256.cu).
 int bwd256_status(int* status, bool clear);
 
-// attn_bwd / attn_bwd_local for d = 256 (attn_bwd256.cu), after the caller
-// has checked pointers, shapes, alignment and scale; B, H, N > 0.
+// attn_bwd and its local, dropout and deterministic forms for d = 256
+// (attn_bwd256.cu), after the caller has checked pointers, shapes, alignment,
+// scale and drop probability; B, H, N > 0. With det, dq_target is the
+// partials workspace of `pairs` tiles per query head, else the accumulator.
 int bwd256_run(const void* q, const void* k, const void* v, const void* dO, const float* lse,
-               float* dq_accum, void* dk, void* dv, int B, int H, int H_kv, int N, float scale,
+               float* dq_target, void* dk, void* dv, int B, int H, int H_kv, int N, float scale,
                int causal, float softcap, const float* dpsum, int window_left, int window_right,
-               cudaStream_t s);
+               bool det, int pairs, float p_drop, unsigned long long seed, cudaStream_t s);
 
 // attn_bwd (d = 64 or 128) with a hook: before_launch(ctx) runs after every
 // argument check and tensor-map encoding has passed and right before the main

@@ -34,6 +34,13 @@
 // Tensor memory (512 columns for d = 128): S buffers of tiles 0 and 1 at
 // [0,128) and [128,256) (P overwrites the first half of its buffer), O_0 at
 // [256, 256 + d), O_1 at [256 + d, 256 + 2d).
+//
+// d = 256: two tiles' S and O would need 768 columns, so a CTA owns one tile
+// of 128 queries. Its key blocks alternate between the two S buffers, so
+// S(j + 1) runs on the tensor cores while the softmax works on S(j), and O
+// (256 columns) sits at [256, 512). K and V get one 64 KB stage each in
+// shared memory (Q 64 KB; 192 KB in all); K(j + 1) is requested as soon as
+// S(j) has read K(j), V(j) as soon as P(j - 1) V has read V(j - 1).
 // Every mbarrier wait is bounded, as in attn_bwd.
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -75,14 +82,33 @@ struct Layout {
 };
 static_assert(Layout<128>::kBytes <= 232448, "shared memory budget");
 
+// d = 256: one query tile per CTA and one K and one V stage (64 KB each);
+// the Q buffer stages O at the end.
+template <>
+struct Layout<256> {
+  static constexpr int kTileBytes = 128 * 256 * 2;
+  static constexpr int kQ0 = 0;
+  static constexpr int kQ1 = kQ0;  // a single tile
+  static constexpr int kK0 = kQ0 + kTileBytes;
+  static constexpr int kK1 = kK0;  // a single stage
+  static constexpr int kV0 = kK0 + kTileBytes;
+  static constexpr int kV1 = kV0;
+  static constexpr int kBars = kV0 + kTileBytes;
+  static constexpr int kNumBars = 17;
+  static constexpr int kTmemSlot = kBars + kNumBars * 8;
+  static constexpr int kAbort = kTmemSlot + 4;
+  static constexpr int kBytes = kAbort + 12;
+};
+static_assert(Layout<256>::kBytes <= 232448, "shared memory budget");
+
 enum Bar {
   BAR_Q_FULL = 0,    // + tile
   BAR_K_FULL = 2,    // + stage
   BAR_K_EMPTY = 4,   // + stage
   BAR_V_FULL = 6,    // + stage
   BAR_V_EMPTY = 8,   // + stage
-  BAR_S_FULL = 10,   // + tile: S_q(j) in its buffer
-  BAR_P_FULL = 12,   // + tile: P_q(j) written (and O_q rescaled if needed)
+  BAR_S_FULL = 10,   // + tile (d = 256: + S buffer): S_q(j) in its buffer
+  BAR_P_FULL = 12,   // + tile (d = 256: + S buffer): P_q(j) written (and O_q rescaled if needed)
   BAR_O_DONE = 14,   // + tile: P_q(j) V_j completed (one phase per key block of the tile)
   BAR_DRAIN = 16,    // abort path only: completion of everything issued
 };
@@ -90,7 +116,7 @@ enum Bar {
 struct Params {
   float* lse;
   int B, H, H_kv, N;
-  int pairs;  // CTAs per query head: ceil(query blocks / 2)
+  int pairs;  // CTAs per query head: ceil(query blocks / 2) (d = 256: query blocks)
   float scale;
   float softcap;
   // visibility band: key j is visible to query i iff
@@ -155,6 +181,8 @@ struct Work {
   }
 };
 
+// d = 256: one tile per CTA, m0[0] = 128 * pair; tile 1 is empty.
+template <int D>
 __device__ __forceinline__ Work work_of(const Params& p) {
   Work w;
   const int heads = p.B * p.H;
@@ -168,7 +196,7 @@ __device__ __forceinline__ Work work_of(const Params& p) {
   const int last_block = (p.N + kBn - 1) / kBn - 1;
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
-    w.m0[q] = pair * 2 * kBm + q * kBm;
+    w.m0[q] = D == 256 ? (q == 0 ? pair * kBm : p.N) : pair * 2 * kBm + q * kBm;
     if (w.m0[q] >= p.N) {
       w.j0[q] = 0;
       w.nt[q] = 0;
@@ -312,6 +340,120 @@ __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t t
       }
       --v_left[st];
       if (w.has(q, j + 1) && !(ok = issue_s(q, j + 1))) break;
+    }
+  }
+  if (__any_sync(0xffffffffu, !ok || *c.abort != 0)) {
+    // completion of everything issued before tensor memory is released
+    if (leader) mma_commit(bar_addr(c, BAR_DRAIN));
+    wait_drain(c, BAR_DRAIN, 0);
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ d = 256 roles
+// Producer of the one-tile form: Q, K(0) and V(0) at once; then K(t) once
+// S(t - 1) has read the K stage, and V(t - 1) once P(t - 2) V has read the V
+// stage. The tensor cores finish in the order S(t - 1), P(t - 2) V, S(t),
+// P(t - 1) V, ..., which is the order of the waits, so each load starts as
+// soon as its stage is free.
+__device__ void producer_role256(const Ctx& c, const Work& w, uint32_t sbase,
+                                 const CUtensorMap* tq, const CUtensorMap* tk,
+                                 const CUtensorMap* tv) {
+  using L = Layout<256>;
+  constexpr uint32_t kTileBytes = L::kTileBytes;
+  const int lane = threadIdx.x & 31;
+  const int nt = w.nt[0];
+  if (lane == 0) {
+    prefetch_tmap(tq);
+    prefetch_tmap(tk);
+    prefetch_tmap(tv);
+    if (nt > 0) {
+      mbar_arrive_expect_tx(bar_addr(c, BAR_Q_FULL), kTileBytes);
+      for (int cb = 0; cb < 4; ++cb)
+        tma_load_3d(sbase + L::kQ0 + cb * 16384, tq, bar_addr(c, BAR_Q_FULL), 64 * cb, w.m0[0],
+                    w.bh);
+    }
+  }
+  const uint64_t keep = policy_evict_last();  // K, V are read by every query block of the head
+  int issued_k = 0, issued_v = 0;
+  bool ok = true;
+  for (int t = 0; t <= nt && ok; ++t) {
+    if (t < nt) {
+      if (t > 0 && !(ok = wait_warp(c, BAR_K_EMPTY, (t - 1) & 1))) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar_addr(c, BAR_K_FULL), kTileBytes);
+        for (int cb = 0; cb < 4; ++cb)
+          tma_load_3d_hint(sbase + L::kK0 + cb * 16384, tk, bar_addr(c, BAR_K_FULL), 64 * cb,
+                           (w.j0[0] + t) * kBn, w.kvh, keep);
+      }
+      issued_k = t + 1;
+    }
+    // V(0) goes with K(0); V(t - 1) follows K(t) from t = 2 on
+    if ((t == 0 && nt > 0) || (t >= 2 && t - 1 < nt)) {
+      const int tv_ = t == 0 ? 0 : t - 1;
+      if (tv_ > 0 && !(ok = wait_warp(c, BAR_V_EMPTY, (tv_ - 1) & 1))) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar_addr(c, BAR_V_FULL), kTileBytes);
+        for (int cb = 0; cb < 4; ++cb)
+          tma_load_3d_hint(sbase + L::kV0 + cb * 16384, tv, bar_addr(c, BAR_V_FULL), 64 * cb,
+                           (w.j0[0] + tv_) * kBn, w.kvh, keep);
+      }
+      issued_v = tv_ + 1;
+    }
+    __syncwarp();
+  }
+  // When aborting, the copies in flight must land before the CTA exits.
+  if (!ok || *c.abort) {
+    if (nt > 0) wait_drain(c, BAR_Q_FULL, 0);
+    if (issued_k > 0) wait_drain(c, BAR_K_FULL, (issued_k - 1) & 1);
+    if (issued_v > 0) wait_drain(c, BAR_V_FULL, (issued_v - 1) & 1);
+  }
+}
+
+// MMA issuer of the one-tile form: S(0); then per key block t, S(t + 1) into
+// the other S buffer (its P(t - 1) was read by P(t - 1) V, issued before),
+// then P(t) V once the softmax has written P(t).
+__device__ void mma_role256(const Ctx& c, const Work& w, uint32_t sbase, uint32_t tmem) {
+  using L = Layout<256>;
+  const bool leader = elect_one_sync() != 0;
+  constexpr uint32_t kIdS = make_idesc_bf16(kBm, kBn, false, false);  // S = Q K^T
+  constexpr uint32_t kIdO = make_idesc_bf16(kBm, 256, false, true);   // O += P V, N = 256
+  const uint32_t q_lo = sdesc_lo(sbase + L::kQ0, 16), k_lo = sdesc_lo(sbase + L::kK0, 16);
+  const uint32_t v_mn = sdesc_lo(sbase + L::kV0, 16384);
+  auto kmaj = [](int k) { return static_cast<uint32_t>(((k >> 2) * 16384 + (k & 3) * 32) >> 4); };
+  auto mnmaj = [](int k) { return static_cast<uint32_t>((2048 * k) >> 4); };
+  const int nt = w.nt[0];
+  bool ok = true;
+  auto issue_s = [&](int t) -> bool {
+    if (!wait_warp(c, BAR_K_FULL, t & 1)) return false;
+    tc_fence_after();
+    if (leader) {
+#pragma unroll
+      for (int k = 0; k < 256 / 16; ++k)
+        mma_ss(tmem + (t & 1) * 128, sdesc_from_lo(q_lo + kmaj(k)), sdesc_from_lo(k_lo + kmaj(k)),
+               kIdS, k > 0);
+      mma_commit(bar_addr(c, BAR_S_FULL + (t & 1)));
+      mma_commit(bar_addr(c, BAR_K_EMPTY));
+    }
+    return true;
+  };
+  if (nt > 0) {
+    ok = wait_warp(c, BAR_Q_FULL, 0);
+    if (ok) ok = issue_s(0);
+  }
+  for (int t = 0; ok && t < nt; ++t) {
+    if (t + 1 < nt && !(ok = issue_s(t + 1))) break;
+    if (!(ok = wait_warp(c, BAR_P_FULL + (t & 1), (t >> 1) & 1))) break;
+    if (!(ok = wait_warp(c, BAR_V_FULL, t & 1))) break;
+    tc_fence_after();
+    if (leader) {
+      // A = P (bf16 pairs, keys along columns 8k .. of the S buffer of block t)
+#pragma unroll
+      for (int k = 0; k < kBn / 16; ++k)
+        mma_ts(tmem + 256, tmem + (t & 1) * 128 + 8 * k, sdesc_from_lo(v_mn + mnmaj(k)), kIdO,
+               (t > 0 || k > 0) ? 1u : 0u);
+      mma_commit(bar_addr(c, BAR_O_DONE));
+      mma_commit(bar_addr(c, BAR_V_EMPTY));
     }
   }
   if (__any_sync(0xffffffffu, !ok || *c.abort != 0)) {
@@ -474,7 +616,8 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint3
   const int q = (warp - 4) >> 2;  // the tile this warpgroup owns
   const int r = ((warp & 3) << 5) + lane;
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
-  const uint32_t tS = tmem + lane_base + q * 128;
+  // d = 256: the key blocks of the one tile alternate between the S buffers
+  constexpr bool kAlt = D == 256;
   const uint32_t tO = tmem + lane_base + 256 + q * D;
   const int qrow = w.m0[q] + r;
   const int bar_wg = 1 + q;  // named barrier of this warpgroup (128 threads)
@@ -489,6 +632,9 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint3
   for (int t = 0; t < nt; ++t) {
     const int n0 = (w.j0[q] + t) * kBn;
     const int m0 = w.m0[q];
+    const uint32_t tS = tmem + lane_base + (kAlt ? (t & 1) : q) * 128;
+    const int bar_s = kAlt ? BAR_S_FULL + (t & 1) : BAR_S_FULL + q;
+    const uint32_t par_s = kAlt ? (t >> 1) & 1 : t & 1;
     // The keep mask depends on no score: it is drawn while the S GEMM of this
     // block runs, with no tensor-memory rows held in registers, so that many
     // Philox calls are in flight at once.
@@ -497,7 +643,7 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint3
     for (int i = 0; i < kBn / 32; ++i)
       kbits[i] = DROP ? keep_bits32(p, qrow, n0 + 32 * i, bh) : 0xFFFFFFFFu;
     // the warpgroup meets at its named barrier below: one decision for all
-    ok = named_bar_and(bar_wg, 128, wait(c, BAR_S_FULL + q, t & 1));
+    ok = named_bar_and(bar_wg, 128, wait(c, bar_s, par_s));
     if (!ok) break;
     tc_fence_after();
     const bool masked =
@@ -558,11 +704,15 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint3
     tmem_wait_st();
     tc_fence_before();
     named_bar_sync(bar_wg, 128);
-    if (r == 0) mbar_arrive(bar_addr(c, BAR_P_FULL + q));
+    if (r == 0) mbar_arrive(bar_addr(c, (kAlt ? BAR_P_FULL + (t & 1) : BAR_P_FULL + q)));
   }
   // ---- epilogue: O / l -> bf16 rows in the tile's Q buffer (free once its
   // last S GEMM is done, which precedes the last P V) -> TMA tensor store;
   // LSE in natural log
+  // d = 256 issues S(j + 1) before P(j) V, so P(nt - 2) V may still run:
+  // its phase of O_DONE completes first (a wait on the parity of the last
+  // phase would pass while the one before it is still open)
+  if (ok && kAlt && nt >= 2) ok = wait(c, BAR_O_DONE + q, (nt - 2) & 1);
   if (ok) ok = wait(c, BAR_O_DONE + q, (nt - 1) & 1);
   if (!named_bar_and(bar_wg, 128, ok)) return;
   tc_fence_after();
@@ -631,11 +781,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
-  const Work w = work_of(p);
+  const Work w = work_of<D>(p);
   if (warp == 0) {
-    producer_role<D>(c, w, sbase, &tm_q, &tm_k, &tm_v);
+    if constexpr (D == 256)
+      producer_role256(c, w, sbase, &tm_q, &tm_k, &tm_v);
+    else
+      producer_role<D>(c, w, sbase, &tm_q, &tm_k, &tm_v);
   } else if (warp == 1) {
-    mma_role<D>(c, w, sbase, tmem);
+    if constexpr (D == 256)
+      mma_role256(c, w, sbase, tmem);
+    else
+      mma_role<D>(c, w, sbase, tmem);
   } else if (warp >= 4) {
     softmax_role<D, SOFTCAP, DROP>(c, p, w, sbase, tmem, &tm_o);
   }
@@ -685,6 +841,9 @@ namespace fwdtc {
 template <bool DROP>
 int dispatch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
              const CUtensorMap& to, const Params& p, cudaStream_t s, int d, bool cap) {
+  if (d == 256)
+    return cap ? launch<256, true, DROP>(tq, tk, tv, to, p, s)
+               : launch<256, false, DROP>(tq, tk, tv, to, p, s);
   if (d == 128)
     return cap ? launch<128, true, DROP>(tq, tk, tv, to, p, s)
                : launch<128, false, DROP>(tq, tk, tv, to, p, s);
@@ -698,7 +857,7 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
   if (!q || !k || !v || !o || !lse) return ATTN_ERR_NULL;
   int rc = check_shape(B, H, H_kv, N, d);
   if (rc != ATTN_OK) return rc;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
   // tau > 0: the kernel takes a row's largest logit at its largest score
   if (!std::isfinite(scale) || !(scale > 0.f) || std::isnan(softcap)) return ATTN_ERR_SHAPE;
   if (!(p_drop >= 0.f && p_drop < 1.f)) return ATTN_ERR_SHAPE;
@@ -716,7 +875,7 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
   p.H = H;
   p.H_kv = H_kv;
   p.N = N;
-  p.pairs = ((N + kBm - 1) / kBm + 1) / 2;
+  p.pairs = d == 256 ? (N + kBm - 1) / kBm : ((N + kBm - 1) / kBm + 1) / 2;
   p.scale = scale;
   const bool cap = softcap > 0.f;
   p.softcap = cap ? softcap : 0.f;

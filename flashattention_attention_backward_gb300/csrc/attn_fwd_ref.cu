@@ -268,8 +268,6 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
   if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || scale == 0.f || std::isnan(softcap)) return ATTN_ERR_SHAPE;
   if (!(p_drop >= 0.f && p_drop < 1.f)) return ATTN_ERR_SHAPE;
-  // dropout is offered where a backward replays it: d = 64 and 128
-  if (d == 256 && p_drop > 0.f) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_ALIGN;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;

@@ -174,7 +174,7 @@ extern "C" int attn_bwd_finalize_partials(const float* dq_partials, void* dq, fl
   if (!dq_partials || !dq) return ATTN_ERR_NULL;
   int rc = check_shape(B, H, H > 0 ? 1 : 0, N, d);
   if (rc != ATTN_OK) return rc;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return ATTN_ERR_SHAPE;
   if (!aligned16(dq_partials) || !aligned16(dq)) return ATTN_ERR_ALIGN;
   const long long rows = static_cast<long long>(B) * H * N;

@@ -47,8 +47,7 @@ def _stream(stream):
 def forward(q, k, v, scale, causal, softcap=0.0, stream=None, impl="tc", dropout=None,
             window=None):
     """O [B,H,N,d] bf16 and LSE [B,H,N] fp32: attn_fwd (tensor cores, impl
-    "tc"; d = 256 always takes attn_fwd_ref) or attn_fwd_ref (plain fp32, impl
-    "ref"). dropout = (p_drop, seed)
+    "tc") or attn_fwd_ref (plain fp32, impl "ref"). dropout = (p_drop, seed)
     runs attn_fwd_dropout or attn_fwd_ref_dropout; window = (left, right) runs
     attn_fwd_local or attn_fwd_ref_local."""
     B, H, H_kv, N, d = _dims(q, k, v)
@@ -61,8 +60,6 @@ def forward(q, k, v, scale, causal, softcap=0.0, stream=None, impl="tc", dropout
         check(fn(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap, dropout[0],
                  dropout[1], _stream(stream)))
         return o, lse
-    if d == 256:
-        impl = "ref"  # the tensor-core forward takes d = 64 or 128
     if window is not None:
         fn = {"tc": attn_fwd_local, "ref": attn_fwd_ref_local}[impl]
         check(fn(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, softcap, window[0], window[1],

@@ -22,12 +22,12 @@
  *    [B, H, N, d]; K, V, dK, dV are [B, H_kv, N, d]; LSE and D are [B, H, N].
  *    bf16 tensors are passed as `void*` (IEEE bfloat16 bit patterns).
  *  * Query head h uses KV head h / (H / H_kv) (H must be a multiple of H_kv).
- *  * d must be 64 or 128 for attn_fwd and its variants, the dropout calls
- *    (attn_fwd_ref_dropout with p_drop > 0 included) and the deterministic and
- *    allocation-free backward; 64, 128 or 256 for attn_fwd_ref,
- *    attn_fwd_ref_local, attn_bwd and attn_bwd_local; preprocess and finalize
- *    accept any d that is a multiple of 4. Other values return
- *    ATTN_ERR_UNSUPPORTED.
+ *  * d must be 64 or 128 for the allocation-free backward; 64, 128 or 256
+ *    for every other forward and backward call (attn_fwd, attn_fwd_ref and
+ *    their local and dropout forms, attn_bwd, attn_bwd_local,
+ *    attn_bwd_dropout, attn_bwd_deterministic, attn_bwd_finalize_partials);
+ *    preprocess and finalize accept any d that is a multiple of 4. Other
+ *    values return ATTN_ERR_UNSUPPORTED.
  *  * Every pointer must be 16-byte aligned (the kernels use TMA and 16-byte
  *    vector accesses).
  *  * `scale` is tau (usually 1/sqrt(d)); the logit is tau * q.k.
@@ -120,7 +120,9 @@ int attn_fwd_dropout(const void* q, const void* k, const void* v, void* o, float
  * walks the visible key blocks once; O accumulates un-normalised in fp32
  * tensor memory, rescaled only when a row maximum grows by more than 2^8,
  * and is divided by the row sum at the end. P enters the PV GEMM as bf16.
- * d must be 64 or 128, and scale must be > 0 (ATTN_ERR_SHAPE otherwise).
+ * d = 256 takes one block of 128 queries per CTA (two tiles' S and O would
+ * exceed tensor memory) and alternates two S buffers over its key blocks.
+ * scale must be > 0 (ATTN_ERR_SHAPE otherwise).
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
              int H_kv, int N, int d, float scale, int causal, float softcap, void* stream);
@@ -183,7 +185,8 @@ int attn_bwd_preprocess(const void* o, const void* dO, float* dpsum, float* dq_a
  * d = 256 runs a kernel of its own ([bwd-detail] §8.3 slices the d = 256
  * GEMMs): a CTA accumulates one half of d for 128 keys over query tiles of
  * 64, recomputing S and dP over the full d (seven GEMM-equivalents per tile
- * instead of five); dQ accumulates the same way.
+ * instead of five); dQ accumulates the same way. That kernel also serves
+ * attn_bwd_local, attn_bwd_dropout and attn_bwd_deterministic at d = 256.
  * Order on the stream: attn_bwd_preprocess, attn_bwd, attn_bwd_finalize.
  * dQ is summed with fp32 atomics, so it may differ in the last bits from run
  * to run; dK and dV are summed on chip in a fixed order.

@@ -150,22 +150,32 @@ def test_dropout_and_d256_validation(lib):
         lib.ATTN_ERR_NULL
     assert lib.attn_bwd_dropout(*ok9, 1, 2, 2, 128, 128, 0.1, 1, 0.0, 0, 0.1, seed) == \
         lib.ATTN_ERR_NULL
-    # dropout is not offered for d = 256 (no backward replays it there)
-    assert lib.attn_fwd_dropout(a, a, a, a, a, 1, 1, 1, 64, 256, 0.1, 0, 0.0, 0.1, seed) == \
-        lib.ATTN_ERR_UNSUPPORTED
-    assert lib.attn_fwd_ref_dropout(a, a, a, a, a, 1, 1, 1, 64, 256, 0.1, 0, 0.0, 0.1, seed) == \
-        lib.ATTN_ERR_UNSUPPORTED
-    assert lib.attn_bwd_dropout(*ok9, 1, 2, 2, 128, 256, 0.1, 1, 0.0, a, 0.1, seed) == \
-        lib.ATTN_ERR_UNSUPPORTED
-    # ... while p_drop = 0 is the plain forward, which takes d = 256
-    assert lib.attn_fwd_ref_dropout(a, a, a, a, a, 0, 1, 1, 64, 256, 0.1, 0, 0.0, 0.0, seed) == \
+    # d = 256 is offered by the dropout, deterministic and local backward and
+    # the fp32 forward with dropout; other head dimensions are not
+    for d in (256,):
+        assert lib.attn_fwd_ref_dropout(a, a, a, a, a, 0, 1, 1, 64, d, 0.1, 0, 0.0, 0.1, seed) == \
+            lib.ATTN_OK
+        assert lib.attn_bwd_dropout(*ok9, 0, 2, 2, 128, d, 0.1, 1, 0.0, a, 0.1, seed) == \
+            lib.ATTN_OK
+        assert lib.attn_bwd(*ok9, 0, 2, 2, 128, d, 0.1, 1, 0.0, a) == lib.ATTN_OK
+        assert lib.attn_bwd_local(*ok9, 0, 2, 2, 128, d, 0.1, 1, 0.0, a, 64, -1) == lib.ATTN_OK
+        assert lib.attn_bwd_deterministic(*ok9, 0, 2, 2, 128, d, 0.1, 1, 0.0, a) == lib.ATTN_OK
+        assert lib.attn_bwd_finalize_partials(a, a, 0.1, 0, 1, 64, d, 1) == lib.ATTN_OK
+    for d in (96, 192, 320):
+        assert lib.attn_fwd_ref_dropout(a, a, a, a, a, 1, 1, 1, 64, d, 0.1, 0, 0.0, 0.1, seed) == \
+            lib.ATTN_ERR_UNSUPPORTED
+        assert lib.attn_bwd_dropout(*ok9, 1, 2, 2, 128, d, 0.1, 1, 0.0, a, 0.1, seed) == \
+            lib.ATTN_ERR_UNSUPPORTED
+        assert lib.attn_bwd_deterministic(*ok9, 1, 2, 2, 128, d, 0.1, 1, 0.0, a) == \
+            lib.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_bwd_dq_partials_bytes(1, 2, 300, 256, 1) == 2 * 6 * 128 * 256 * 4
+    # the tensor-core forwards take d = 256 too
+    assert lib.attn_fwd(a, a, a, a, a, 0, 1, 1, 64, 256, 0.1, 0, 0.0) == lib.ATTN_OK
+    assert lib.attn_fwd_local(a, a, a, a, a, 0, 1, 1, 64, 256, 0.1, 1, 0.0, 8, -1) == lib.ATTN_OK
+    assert lib.attn_fwd_dropout(a, a, a, a, a, 0, 1, 1, 64, 256, 0.1, 0, 0.0, 0.1, seed) == \
         lib.ATTN_OK
-    # d = 256: the plain and local backward accept it, the other variants do not
-    assert lib.attn_bwd(*ok9, 0, 2, 2, 128, 256, 0.1, 1, 0.0, a) == lib.ATTN_OK
-    assert lib.attn_bwd_local(*ok9, 0, 2, 2, 128, 256, 0.1, 1, 0.0, a, 64, -1) == lib.ATTN_OK
-    assert lib.attn_bwd_deterministic(*ok9, 1, 2, 2, 128, 256, 0.1, 1, 0.0, a) == \
-        lib.ATTN_ERR_UNSUPPORTED
-    assert lib.attn_fwd(a, a, a, a, a, 1, 1, 1, 64, 256, 0.1, 0, 0.0) == lib.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_fwd(a, a, a, a, a, 1, 1, 1, 64, 192, 0.1, 0, 0.0) == lib.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_fwd(a, a, a, a, a, 1, 1, 1, 64, 256, -0.1, 0, 0.0) == lib.ATTN_ERR_SHAPE
     # empty problems succeed without touching the device
     assert lib.attn_fwd_dropout(a, a, a, a, a, 0, 1, 1, 64, 64, 0.1, 0, 0.0, 0.1, seed) == \
         lib.ATTN_OK

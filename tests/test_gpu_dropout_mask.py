@@ -8,7 +8,7 @@ kernels' masks must equal the oracle's element for element, not only within
 the float tolerances of the gradients. Each mask is read out through a
 one-hot operand:
 
-* forward: V is one-hot over 128 (or 64) keys, V_j = e_(j - j0) for
+* forward: V is one-hot over d keys (64, 128 or 256), V_j = e_(j - j0) for
   j0 <= j < j0 + d and 0 elsewhere. Then O[i, c] = P~[i, j0 + c] with
   P~ = P o Z / (1 - p), so O is zero exactly where the key is dropped (or
   masked by causality) and nonzero where it is kept: inputs of small spread
@@ -64,6 +64,8 @@ def _one_hot_rows(shape, start, d, device):
     (333, 128, True, (0, 128, 205)),
     (200, 64, False, (0, 64, 136)),
     (200, 64, True, (37, 136)),
+    (333, 256, False, (0, 100)),
+    (333, 256, True, (77,)),
 ])
 def test_forward_keep_mask_bit_exact(impl, N, d, causal, j0s):
     B, H, H_kv = 2, 2, 1
@@ -94,6 +96,8 @@ def test_forward_keep_mask_bit_exact(impl, N, d, causal, j0s):
     (333, 128, True, (128, 205)),
     (200, 64, False, (0, 136)),
     (200, 64, True, (64, 150)),
+    (333, 256, False, (0, 77)),
+    (333, 256, True, (0,)),
 ])
 def test_backward_keep_mask_bit_exact(N, d, causal, i0s):
     B, H, H_kv = 2, 4, 2
