@@ -45,9 +45,12 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "attn_common.cuh"
 #include "philox.cuh"
 #include "sm103_ptx.cuh"
+#include "softcap_math.cuh"
 
 namespace attn {
 namespace fwdtc {
@@ -547,7 +550,8 @@ __device__ __forceinline__ float tile_p(const Params& p, uint32_t tS, int n0, in
                                         const uint32_t (&kbits)[kBn / 32]) {
   const uint64_t c2v = f2_make(SOFTCAP ? cap_in : c_log2, SOFTCAP ? cap_in : c_log2);
   const uint64_t out2 = f2_make(cap_out, cap_out);
-  const uint64_t one2 = f2_make(1.f, 1.f), mtwo2 = f2_make(-2.f, -2.f);
+  const float cap_u = SOFTCAP ? p.scale / p.softcap : 0.f;  // u = tau s / c
+  const uint64_t cu2 = f2_make(cap_u, cap_u);
   const uint64_t nsh2 = f2_make(-shift, -shift);
   uint64_t sum2 = f2_make(0.f, 0.f);
   // two 32-column loads per wait; keys 64 c2 .. 64 c2 + 63 land in columns
@@ -559,16 +563,17 @@ __device__ __forceinline__ float tile_p(const Params& p, uint32_t tS, int n0, in
     const uint32_t kb0 = DROP ? kbits[2 * c2] : 0xFFFFFFFFu;
     const uint32_t kb1 = DROP ? kbits[2 * c2 + 1] : 0xFFFFFFFFu;
     uint32_t packed[32];
+    // FAST: tanh by the polynomial (every |u| of the warp's 64 keys <= 1)
+    auto p_group = [&](auto fast_tag) {
+      constexpr bool FAST = decltype(fast_tag)::value;
 #pragma unroll
     for (int u = 0; u < 32; ++u) {
       const uint64_t s2 = f2_make(raw[2 * u], raw[2 * u + 1]);
       uint64_t y2;
       if (SOFTCAP) {
-        // tanh(v) = 1 - 2 / (exp(2v) + 1) with v = tau s / c
-        const uint64_t v2 = f2_mul(s2, c2v);
-        const uint64_t e1 = f2_add(f2_make(ex2_approx(f2_lo(v2)), ex2_approx(f2_hi(v2))), one2);
-        const uint64_t th2 =
-            f2_fma(f2_make(rcp_approx(f2_lo(e1)), rcp_approx(f2_hi(e1))), mtwo2, one2);
+        // tanh(v), v = tau s / c
+        const uint64_t th2 = FAST ? softcap::tanh_poly2(f2_mul(s2, cu2))
+                                  : softcap::tanh_mufu2(f2_mul(s2, c2v));
         y2 = f2_fma(th2, out2, nsh2);
       } else {
         y2 = f2_fma(s2, c2v, nsh2);
@@ -591,6 +596,15 @@ __device__ __forceinline__ float tile_p(const Params& p, uint32_t tS, int n0, in
       } else {
         packed[u] = pack_bf16x2(p0, p1);
       }
+    }
+    };
+    if constexpr (SOFTCAP) {
+      if (__all_sync(0xffffffffu, softcap::max_abs(raw) * cap_u <= softcap::kPolyMax))
+        p_group(std::true_type{});
+      else
+        p_group(std::false_type{});
+    } else {
+      p_group(std::false_type{});
     }
     uint32_t lo[16], hi[16];
 #pragma unroll

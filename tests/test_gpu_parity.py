@@ -42,6 +42,10 @@ SMALL = [
     _w("softcap_sat_d64", 1, 2, 2, 256, 64, False, softcap=2.0, sigma_qkv=2.0),
     _w("softcap_sat_d128_causal", 1, 2, 1, 320, 128, True, softcap=2.0, sigma_qkv=2.0),
     _w("softcap30_d128", 1, 2, 2, 256, 128, True, softcap=30.0, sigma_qkv=2.0),
+    # |u| = |tau s / c| of about 0.5 sigma: groups of scores take the polynomial
+    # tanh or, when one |u| of the warp's group exceeds 1, the exp2/rcp form
+    _w("softcap8_mixed_d64", 2, 2, 2, 384, 64, False, softcap=8.0, sigma_qkv=2.0),
+    _w("softcap8_mixed_d128_causal", 1, 4, 2, 333, 128, True, softcap=8.0, sigma_qkv=2.0),
     # more key blocks than SMs: every CTA walks several units (192 and 160)
     _w("many_units_gqa_d128_causal", 16, 8, 4, 300, 128, True),
     _w("many_units_d64_softcap", 40, 4, 2, 200, 64, False, softcap=5.0, sigma_qkv=2.0),
