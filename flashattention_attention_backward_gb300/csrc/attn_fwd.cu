@@ -3,44 +3,44 @@
 // "解析 FlashAttention（3）" §1.1 forward and §3.2 eq. 9-12, the running
 // (max, sum) statistics of the online softmax).
 //
-// One CTA owns two blocks of 128 queries (tiles 0 and 1) of one query head
-// and walks, once, the key blocks (128 keys) their masks let them see. Per
-// key block j and tile q:
-//   S_q(j)  = Q_q K_j^T                          (tensor cores, fp32 in TMEM)
-//   m       = running row maximum of x = logit * log2e; the shift m_used is
-//             moved only when the maximum grows by more than kRescale (in
-//             log2 units), and then O_q and l are multiplied by
-//             2^(m_used_old - m_used_new)
-//   P_q(j)  = 2^(x - m_used) as bf16 pairs over the S buffer, l += sum P
-//   O_q    += P_q(j) V_j                         (P read from TMEM)
-// and at the end O = O_q / l, LSE = (m_used + log2 l) ln 2. The values of P
+// Two forms share the per-block arithmetic below. Queries sit on the
+// tensor-memory lanes: thread r of a softmax warpgroup owns query row r, so
+// row maxima and sums need no reduction across rows. Per key block j:
+//   S(j)  = Q K_j^T                             (tensor cores, fp32 in TMEM)
+//   m     = running row maximum of x = logit * log2e; the shift m_used is
+//           moved only when the maximum grows by more than kRescale (in
+//           log2 units), and then O and l are multiplied by
+//           2^(m_used_old - m_used_new)
+//   P(j)  = 2^(x - m_used) as bf16 pairs over the S buffer, l += sum P
+//   O    += P(j) V_j                            (P read from TMEM)
+// and at the end O = O / l, LSE = (m_used + log2 l) ln 2. The values of P
 // stay below 2^kRescale, so neither the bf16 P nor the fp32 O can overflow.
 //
-// The two tiles ping-pong on the tensor cores: while the softmax of tile 0
-// works on S_0(j), the tensor cores run P_1(j-1) V and S_1(j), and the other
-// way round. K_j and V_j serve both tiles.
-//
-// Queries sit on the tensor-memory lanes: thread r of softmax warpgroup q
-// owns row r of tile q, so row maxima and sums need no cross-thread
-// reduction.
-//
-// Warp roles (384 threads):
+// Two-tile form (d = 64). One CTA owns two blocks of 128 queries (tiles 0
+// and 1) of one query head and walks, once, the key blocks their masks let
+// them see. The tiles ping-pong on the tensor cores: while the softmax of
+// tile 0 works on S_0(j), the tensor cores run P_1(j-1) V and S_1(j), and the
+// other way round; K_j and V_j serve both tiles.
 //   warp 0      TMA producer: Q_0, Q_1 once; K_j, V_j in two-stage rings
 //   warp 1      tcgen05 MMA issuer (whole warp, one elected lane issues)
 //   warps 4-7   softmax of tile 0, then its epilogue (O / l -> bf16 ->
 //               shared -> TMA store; LSE)
 //   warps 8-11  the same for tile 1
+// Tensor memory: S buffers of the tiles at [0,128) and [128,256) (P
+// overwrites the first half of its buffer), O_0 at [256, 256 + d), O_1 at
+// [256 + d, 256 + 2d).
 //
-// Tensor memory (512 columns for d = 128): S buffers of tiles 0 and 1 at
-// [0,128) and [128,256) (P overwrites the first half of its buffer), O_0 at
-// [256, 256 + d), O_1 at [256 + d, 256 + 2d).
-//
-// d = 256: two tiles' S and O would need 768 columns, so a CTA owns one tile
-// of 128 queries. Its key blocks alternate between the two S buffers, so
-// S(j + 1) runs on the tensor cores while the softmax works on S(j), and O
-// (256 columns) sits at [256, 512). K and V get one 64 KB stage each in
-// shared memory (Q 64 KB; 192 KB in all); K(j + 1) is requested as soon as
-// S(j) has read K(j), V(j) as soon as P(j - 1) V has read V(j - 1).
+// One-tile form (d = 128 and 256; two tiles' S and O would need 768 columns
+// at d = 256). One CTA owns one block of 128 queries. Its key blocks
+// alternate between two S buffers ([0,128) and [128,256)), so S(j + 1) runs
+// on the tensor cores while the softmax works on S(j); O sits at
+// [256, 256 + d). Both softmax warpgroups work on the one tile, warpgroup h
+// on keys 64 h .. 64 h + 63 of each block and on columns h d/2 .. of O; they
+// exchange the half-row maxima through shared memory once per block.
+//   warp 0      Q once; K_j in a ring of 2 stages (d = 128) or 1 (d = 256)
+//   warp 2      V_j in the same kind of ring
+//   warp 1      MMA issuer: S(0), then per block S(j + 1), P(j) V
+//   warps 4-11  softmax, then the epilogue (each warpgroup its half of O)
 // Every mbarrier wait is bounded, as in attn_bwd.
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -85,24 +85,38 @@ struct Layout {
 };
 static_assert(Layout<128>::kBytes <= 232448, "shared memory budget");
 
-// d = 256: one query tile per CTA and one K and one V stage (64 KB each);
-// the Q buffer stages O at the end.
-template <>
-struct Layout<256> {
-  static constexpr int kTileBytes = 128 * 256 * 2;
+// The one-tile form (d = 256): one query tile per CTA and one K and one V
+// stage; the Q buffer stages O at the end. It asks for more than half of the
+// SM's shared memory, so that a second CTA never waits on the first one's
+// tensor memory.
+template <int D>
+constexpr bool kOneTile = D >= 128;
+
+template <int D>
+struct LayoutOne {
+  static constexpr int kTileBytes = 128 * D * 2;
+  // K and V stages: two where they fit (d <= 128), one at d = 256
+  static constexpr int kStages = D <= 128 ? 2 : 1;
   static constexpr int kQ0 = 0;
   static constexpr int kQ1 = kQ0;  // a single tile
   static constexpr int kK0 = kQ0 + kTileBytes;
-  static constexpr int kK1 = kK0;  // a single stage
-  static constexpr int kV0 = kK0 + kTileBytes;
-  static constexpr int kV1 = kV0;
-  static constexpr int kBars = kV0 + kTileBytes;
+  static constexpr int kK1 = kK0 + (kStages - 1) * kTileBytes;
+  static constexpr int kV0 = kK1 + kTileBytes;
+  static constexpr int kV1 = kV0 + (kStages - 1) * kTileBytes;
+  // the two softmax warpgroups' half-row maxima (two blocks in flight) and
+  // row sums: [2][2][128] + [2][128] fp32
+  static constexpr int kXchg = kV1 + kTileBytes;
+  static constexpr int kBars = kXchg + 6 * 128 * 4;
   static constexpr int kNumBars = 17;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
-  static constexpr int kBytes = kAbort + 12;
+  static constexpr int kUsed = kAbort + 12;
+  static constexpr int kBytes = kUsed > 120 * 1024 ? kUsed : 120 * 1024;
 };
-static_assert(Layout<256>::kBytes <= 232448, "shared memory budget");
+static_assert(LayoutOne<256>::kBytes <= 232448, "shared memory budget");
+
+template <int D>
+using LayoutFor = std::conditional_t<kOneTile<D>, LayoutOne<D>, Layout<D>>;
 
 enum Bar {
   BAR_Q_FULL = 0,    // + tile
@@ -184,7 +198,7 @@ struct Work {
   }
 };
 
-// d = 256: one tile per CTA, m0[0] = 128 * pair; tile 1 is empty.
+// The one-tile form: m0[0] = 128 * pair; tile 1 is empty.
 template <int D>
 __device__ __forceinline__ Work work_of(const Params& p) {
   Work w;
@@ -199,7 +213,7 @@ __device__ __forceinline__ Work work_of(const Params& p) {
   const int last_block = (p.N + kBn - 1) / kBn - 1;
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
-    w.m0[q] = D == 256 ? (q == 0 ? pair * kBm : p.N) : pair * 2 * kBm + q * kBm;
+    w.m0[q] = kOneTile<D> ? (q == 0 ? pair * kBm : p.N) : pair * 2 * kBm + q * kBm;
     if (w.m0[q] >= p.N) {
       w.j0[q] = 0;
       w.nt[q] = 0;
@@ -353,90 +367,85 @@ __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t t
   __syncwarp();
 }
 
-// ------------------------------------------------------------------ d = 256 roles
-// Producer of the one-tile form: Q, K(0) and V(0) at once; then K(t) once
-// S(t - 1) has read the K stage, and V(t - 1) once P(t - 2) V has read the V
-// stage. The tensor cores finish in the order S(t - 1), P(t - 2) V, S(t),
-// P(t - 1) V, ..., which is the order of the waits, so each load starts as
-// soon as its stage is free.
-__device__ void producer_role256(const Ctx& c, const Work& w, uint32_t sbase,
-                                 const CUtensorMap* tq, const CUtensorMap* tk,
-                                 const CUtensorMap* tv) {
-  using L = Layout<256>;
+// ------------------------------------------------------------------ one-tile roles
+// Loaders of the one-tile form. Warp 0 loads Q and the K blocks, warp 2 the
+// V blocks, each into its own ring of kStages stages: K(t) once S(t - kStages)
+// has read its stage, V(t) once P(t - kStages) V has. Each warp waits on its
+// own barriers in the order the tensor cores finish them, so no load waits
+// behind another operand's.
+template <int D>
+__device__ void loader_role_one(const Ctx& c, const Work& w, uint32_t sbase,
+                                const CUtensorMap* tq, const CUtensorMap* tkv, bool is_v) {
+  using L = LayoutOne<D>;
+  constexpr int kBoxes = D / 64;
   constexpr uint32_t kTileBytes = L::kTileBytes;
+  constexpr int kS = L::kStages;
   const int lane = threadIdx.x & 31;
   const int nt = w.nt[0];
   if (lane == 0) {
-    prefetch_tmap(tq);
-    prefetch_tmap(tk);
-    prefetch_tmap(tv);
-    if (nt > 0) {
+    prefetch_tmap(tkv);
+    if (!is_v && nt > 0) {
+      prefetch_tmap(tq);
       mbar_arrive_expect_tx(bar_addr(c, BAR_Q_FULL), kTileBytes);
-      for (int cb = 0; cb < 4; ++cb)
+      for (int cb = 0; cb < kBoxes; ++cb)
         tma_load_3d(sbase + L::kQ0 + cb * 16384, tq, bar_addr(c, BAR_Q_FULL), 64 * cb, w.m0[0],
                     w.bh);
     }
   }
   const uint64_t keep = policy_evict_last();  // K, V are read by every query block of the head
-  int issued_k = 0, issued_v = 0;
+  const int bar_full = is_v ? BAR_V_FULL : BAR_K_FULL;
+  const int bar_empty = is_v ? BAR_V_EMPTY : BAR_K_EMPTY;
+  const uint32_t base = sbase + (is_v ? L::kV0 : L::kK0);
+  int issued = 0;
   bool ok = true;
-  for (int t = 0; t <= nt && ok; ++t) {
-    if (t < nt) {
-      if (t > 0 && !(ok = wait_warp(c, BAR_K_EMPTY, (t - 1) & 1))) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar_addr(c, BAR_K_FULL), kTileBytes);
-        for (int cb = 0; cb < 4; ++cb)
-          tma_load_3d_hint(sbase + L::kK0 + cb * 16384, tk, bar_addr(c, BAR_K_FULL), 64 * cb,
-                           (w.j0[0] + t) * kBn, w.kvh, keep);
-      }
-      issued_k = t + 1;
+  for (int t = 0; t < nt; ++t) {
+    const int st = t % kS;
+    if (t >= kS && !(ok = wait_warp(c, bar_empty + st, ((t / kS) - 1) & 1))) break;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_addr(c, bar_full + st), kTileBytes);
+      for (int cb = 0; cb < kBoxes; ++cb)
+        tma_load_3d_hint(base + st * kTileBytes + cb * 16384, tkv, bar_addr(c, bar_full + st),
+                         64 * cb, (w.j0[0] + t) * kBn, w.kvh, keep);
     }
-    // V(0) goes with K(0); V(t - 1) follows K(t) from t = 2 on
-    if ((t == 0 && nt > 0) || (t >= 2 && t - 1 < nt)) {
-      const int tv_ = t == 0 ? 0 : t - 1;
-      if (tv_ > 0 && !(ok = wait_warp(c, BAR_V_EMPTY, (tv_ - 1) & 1))) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar_addr(c, BAR_V_FULL), kTileBytes);
-        for (int cb = 0; cb < 4; ++cb)
-          tma_load_3d_hint(sbase + L::kV0 + cb * 16384, tv, bar_addr(c, BAR_V_FULL), 64 * cb,
-                           (w.j0[0] + tv_) * kBn, w.kvh, keep);
-      }
-      issued_v = tv_ + 1;
-    }
+    issued = t + 1;
     __syncwarp();
   }
   // When aborting, the copies in flight must land before the CTA exits.
   if (!ok || *c.abort) {
-    if (nt > 0) wait_drain(c, BAR_Q_FULL, 0);
-    if (issued_k > 0) wait_drain(c, BAR_K_FULL, (issued_k - 1) & 1);
-    if (issued_v > 0) wait_drain(c, BAR_V_FULL, (issued_v - 1) & 1);
+    if (!is_v && nt > 0) wait_drain(c, BAR_Q_FULL, 0);
+    for (int t = issued - kS < 0 ? 0 : issued - kS; t < issued; ++t)
+      wait_drain(c, bar_full + t % kS, (t / kS) & 1);
   }
 }
 
 // MMA issuer of the one-tile form: S(0); then per key block t, S(t + 1) into
 // the other S buffer (its P(t - 1) was read by P(t - 1) V, issued before),
 // then P(t) V once the softmax has written P(t).
-__device__ void mma_role256(const Ctx& c, const Work& w, uint32_t sbase, uint32_t tmem) {
-  using L = Layout<256>;
+template <int D>
+__device__ void mma_role_one(const Ctx& c, const Work& w, uint32_t sbase, uint32_t tmem) {
+  using L = LayoutOne<D>;
+  constexpr int kS = L::kStages;
   const bool leader = elect_one_sync() != 0;
   constexpr uint32_t kIdS = make_idesc_bf16(kBm, kBn, false, false);  // S = Q K^T
-  constexpr uint32_t kIdO = make_idesc_bf16(kBm, 256, false, true);   // O += P V, N = 256
-  const uint32_t q_lo = sdesc_lo(sbase + L::kQ0, 16), k_lo = sdesc_lo(sbase + L::kK0, 16);
-  const uint32_t v_mn = sdesc_lo(sbase + L::kV0, 16384);
+  constexpr uint32_t kIdO = make_idesc_bf16(kBm, D, false, true);     // O += P V
+  const uint32_t q_lo = sdesc_lo(sbase + L::kQ0, 16);
+  const uint32_t k_lo[2] = {sdesc_lo(sbase + L::kK0, 16), sdesc_lo(sbase + L::kK1, 16)};
+  const uint32_t v_mn[2] = {sdesc_lo(sbase + L::kV0, 16384), sdesc_lo(sbase + L::kV1, 16384)};
   auto kmaj = [](int k) { return static_cast<uint32_t>(((k >> 2) * 16384 + (k & 3) * 32) >> 4); };
   auto mnmaj = [](int k) { return static_cast<uint32_t>((2048 * k) >> 4); };
   const int nt = w.nt[0];
   bool ok = true;
   auto issue_s = [&](int t) -> bool {
-    if (!wait_warp(c, BAR_K_FULL, t & 1)) return false;
+    const int st = t % kS;
+    if (!wait_warp(c, BAR_K_FULL + st, (t / kS) & 1)) return false;
     tc_fence_after();
     if (leader) {
 #pragma unroll
-      for (int k = 0; k < 256 / 16; ++k)
-        mma_ss(tmem + (t & 1) * 128, sdesc_from_lo(q_lo + kmaj(k)), sdesc_from_lo(k_lo + kmaj(k)),
-               kIdS, k > 0);
+      for (int k = 0; k < D / 16; ++k)
+        mma_ss(tmem + (t & 1) * 128, sdesc_from_lo(q_lo + kmaj(k)),
+               sdesc_from_lo(k_lo[st] + kmaj(k)), kIdS, k > 0);
       mma_commit(bar_addr(c, BAR_S_FULL + (t & 1)));
-      mma_commit(bar_addr(c, BAR_K_EMPTY));
+      mma_commit(bar_addr(c, BAR_K_EMPTY + st));
     }
     return true;
   };
@@ -447,16 +456,18 @@ __device__ void mma_role256(const Ctx& c, const Work& w, uint32_t sbase, uint32_
   for (int t = 0; ok && t < nt; ++t) {
     if (t + 1 < nt && !(ok = issue_s(t + 1))) break;
     if (!(ok = wait_warp(c, BAR_P_FULL + (t & 1), (t >> 1) & 1))) break;
-    if (!(ok = wait_warp(c, BAR_V_FULL, t & 1))) break;
+    const int vs = t % kS;
+    if (!(ok = wait_warp(c, BAR_V_FULL + vs, (t / kS) & 1))) break;
     tc_fence_after();
     if (leader) {
-      // A = P (bf16 pairs, keys along columns 8k .. of the S buffer of block t)
+      // A = P (bf16 pairs in the S buffer of block t: keys 0-63 in columns
+      // 0-31, keys 64-127 in columns 64-95, one half per softmax warpgroup)
 #pragma unroll
       for (int k = 0; k < kBn / 16; ++k)
-        mma_ts(tmem + 256, tmem + (t & 1) * 128 + 8 * k, sdesc_from_lo(v_mn + mnmaj(k)), kIdO,
-               (t > 0 || k > 0) ? 1u : 0u);
+        mma_ts(tmem + 256, tmem + (t & 1) * 128 + 8 * k + (k >= 4 ? 32 : 0),
+               sdesc_from_lo(v_mn[vs] + mnmaj(k)), kIdO, (t > 0 || k > 0) ? 1u : 0u);
       mma_commit(bar_addr(c, BAR_O_DONE));
-      mma_commit(bar_addr(c, BAR_V_EMPTY));
+      mma_commit(bar_addr(c, BAR_V_EMPTY + vs));
     }
   }
   if (__any_sync(0xffffffffu, !ok || *c.abort != 0)) {
@@ -468,31 +479,34 @@ __device__ void mma_role256(const Ctx& c, const Work& w, uint32_t sbase, uint32_
 }
 
 // ------------------------------------------------------------------ softmax
-// Row maximum of one S tile (raw scores; with tau > 0 the logit grows with
-// the score, softcap included). MASKED tiles (a band's edge, the sequence's
-// end) leave invisible keys out.
+// Row maximum over 64 keys (key0 .. key0 + 63, S columns src .. src + 63)
+// of raw scores; with tau > 0 the logit grows with the score, softcap
+// included. MASKED chunks (a band's edge, the sequence's end) leave
+// invisible keys out.
 template <bool MASKED>
-__device__ __forceinline__ float tile_max(const Params& p, uint32_t tS, int n0, int qrow) {
+__device__ __forceinline__ float chunk_max(const Params& p, uint32_t src, int key0, int qrow) {
   float m0 = -INFINITY, m1 = -INFINITY;
-  // two 32-column loads per wait
+  uint32_t raw[64];
+  tmem_ld32x2(src, src + 32, raw);  // two 32-column loads per wait
 #pragma unroll
-  for (int ch2 = 0; ch2 < kBn / 64; ++ch2) {
-    uint32_t raw[64];
-    tmem_ld32x2(tS + ch2 * 64, tS + ch2 * 64 + 32, raw);
-#pragma unroll
-    for (int e = 0; e < 64; ++e) {
-      float s = __uint_as_float(raw[e]);
-      if (MASKED) {
-        const int key = n0 + ch2 * 64 + e;
-        if (!(key < p.N && key - qrow <= p.win_right && qrow - key <= p.win_left)) s = -INFINITY;
-      }
-      if (e & 1)
-        m1 = fmaxf(m1, s);
-      else
-        m0 = fmaxf(m0, s);
+  for (int e = 0; e < 64; ++e) {
+    float s = __uint_as_float(raw[e]);
+    if (MASKED) {
+      const int key = key0 + e;
+      if (!(key < p.N && key - qrow <= p.win_right && qrow - key <= p.win_left)) s = -INFINITY;
     }
+    if (e & 1)
+      m1 = fmaxf(m1, s);
+    else
+      m0 = fmaxf(m0, s);
   }
   return fmaxf(m0, m1);
+}
+
+// Row maximum of one S tile (both 64-key chunks).
+template <bool MASKED>
+__device__ __forceinline__ float tile_max(const Params& p, uint32_t tS, int n0, int qrow) {
+  return fmaxf(chunk_max<MASKED>(p, tS, n0, qrow), chunk_max<MASKED>(p, tS + 64, n0 + 64, qrow));
 }
 
 // Dropout keep bits of keys k0 .. k0 + 31 for this thread's query row.
@@ -538,34 +552,28 @@ __device__ __forceinline__ uint32_t keep_bits32(const Params& p, int qrow, int k
   return ((bits << t) & hi_mask) | ((bits >> (4u - t)) & lo_mask);
 }
 
-// P = 2^(x - shift) of one S tile as bf16 pairs over the first half of the
-// buffer; returns the row sum of P (fp32, before rounding and before
-// dropout). With DROP the bf16 values are P o Z / (1 - p), Z the keep mask
-// whose bit j of kbits[j / 32] belongs to key n0 + j; the row sum stays that
-// of P. Keys 32 ch .. 32 ch + 31 land in columns
-// 16 ch .. 16 ch + 15, whose S values were read in this or an earlier chunk.
+// P = 2^(x - shift) of 64 keys (key0 .. key0 + 63, S columns src .. src +
+// 63) as bf16 pairs in columns dst .. dst + 31; returns their sum of P (fp32,
+// before rounding and before dropout). With DROP the bf16 values are
+// P o Z / (1 - p), Z the keep mask whose bit j of kb0 (kb1) belongs to key
+// key0 + j (key0 + 32 + j); the sum stays that of P. dst may overlap src:
+// every S value of the chunk is read before the first P is written.
 template <bool SOFTCAP, bool MASKED, bool DROP>
-__device__ __forceinline__ float tile_p(const Params& p, uint32_t tS, int n0, int qrow,
-                                        float c_log2, float cap_in, float cap_out, float shift,
-                                        const uint32_t (&kbits)[kBn / 32]) {
+__device__ __forceinline__ float chunk_p(const Params& p, uint32_t src, uint32_t dst, int key0,
+                                         int qrow, float c_log2, float cap_in, float cap_out,
+                                         float shift, uint32_t kb0, uint32_t kb1) {
   const uint64_t c2v = f2_make(SOFTCAP ? cap_in : c_log2, SOFTCAP ? cap_in : c_log2);
   const uint64_t out2 = f2_make(cap_out, cap_out);
   const float cap_u = SOFTCAP ? p.scale / p.softcap : 0.f;  // u = tau s / c
   const uint64_t cu2 = f2_make(cap_u, cap_u);
   const uint64_t nsh2 = f2_make(-shift, -shift);
   uint64_t sum2 = f2_make(0.f, 0.f);
-  // two 32-column loads per wait; keys 64 c2 .. 64 c2 + 63 land in columns
-  // 32 c2 .. 32 c2 + 31
-#pragma unroll
-  for (int c2 = 0; c2 < kBn / 64; ++c2) {
-    uint32_t raw[64];
-    tmem_ld32x2(tS + c2 * 64, tS + c2 * 64 + 32, raw);
-    const uint32_t kb0 = DROP ? kbits[2 * c2] : 0xFFFFFFFFu;
-    const uint32_t kb1 = DROP ? kbits[2 * c2 + 1] : 0xFFFFFFFFu;
-    uint32_t packed[32];
-    // FAST: tanh by the polynomial (every |u| of the warp's 64 keys <= 1)
-    auto p_group = [&](auto fast_tag) {
-      constexpr bool FAST = decltype(fast_tag)::value;
+  uint32_t raw[64];
+  tmem_ld32x2(src, src + 32, raw);  // two 32-column loads per wait
+  uint32_t packed[32];
+  // FAST: tanh by the polynomial (every |u| of the warp's 64 keys <= 1)
+  auto p_group = [&](auto fast_tag) {
+    constexpr bool FAST = decltype(fast_tag)::value;
 #pragma unroll
     for (int u = 0; u < 32; ++u) {
       const uint64_t s2 = f2_make(raw[2 * u], raw[2 * u + 1]);
@@ -580,7 +588,7 @@ __device__ __forceinline__ float tile_p(const Params& p, uint32_t tS, int n0, in
       }
       float y0 = f2_lo(y2), y1 = f2_hi(y2);
       if (MASKED) {
-        const int key = n0 + c2 * 64 + 2 * u;
+        const int key = key0 + 2 * u;
         if (!(key < p.N && key - qrow <= p.win_right && qrow - key <= p.win_left)) y0 = -INFINITY;
         if (!(key + 1 < p.N && key + 1 - qrow <= p.win_right && qrow - key - 1 <= p.win_left))
           y1 = -INFINITY;
@@ -597,25 +605,38 @@ __device__ __forceinline__ float tile_p(const Params& p, uint32_t tS, int n0, in
         packed[u] = pack_bf16x2(p0, p1);
       }
     }
-    };
-    if constexpr (SOFTCAP) {
-      if (__all_sync(0xffffffffu, softcap::max_abs(raw) * cap_u <= softcap::kPolyMax))
-        p_group(std::true_type{});
-      else
-        p_group(std::false_type{});
-    } else {
+  };
+  if constexpr (SOFTCAP) {
+    if (__all_sync(0xffffffffu, softcap::max_abs(raw) * cap_u <= softcap::kPolyMax))
+      p_group(std::true_type{});
+    else
       p_group(std::false_type{});
-    }
-    uint32_t lo[16], hi[16];
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      lo[u] = packed[u];
-      hi[u] = packed[16 + u];
-    }
-    tmem_st16(tS + c2 * 32, lo);
-    tmem_st16(tS + c2 * 32 + 16, hi);
+  } else {
+    p_group(std::false_type{});
   }
+  uint32_t lo[16], hi[16];
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    lo[u] = packed[u];
+    hi[u] = packed[16 + u];
+  }
+  tmem_st16(dst, lo);
+  tmem_st16(dst + 16, hi);
   return f2_lo(sum2) + f2_hi(sum2);
+}
+
+// P of one S tile over the first half of its buffer: keys 64 c .. 64 c + 63
+// land in columns 32 c .. 32 c + 31, whose S values were read in this or an
+// earlier chunk; returns the row sum of P.
+template <bool SOFTCAP, bool MASKED, bool DROP>
+__device__ __forceinline__ float tile_p(const Params& p, uint32_t tS, int n0, int qrow,
+                                        float c_log2, float cap_in, float cap_out, float shift,
+                                        const uint32_t (&kbits)[kBn / 32]) {
+  const float s0 = chunk_p<SOFTCAP, MASKED, DROP>(p, tS, tS, n0, qrow, c_log2, cap_in, cap_out,
+                                                  shift, kbits[0], kbits[1]);
+  const float s1 = chunk_p<SOFTCAP, MASKED, DROP>(p, tS + 64, tS + 32, n0 + 64, qrow, c_log2,
+                                                  cap_in, cap_out, shift, kbits[2], kbits[3]);
+  return s0 + s1;
 }
 
 // Softmax warpgroup q (thread = query row r of tile q): per key block, the
@@ -624,14 +645,14 @@ __device__ __forceinline__ float tile_p(const Params& p, uint32_t tS, int n0, in
 template <int D, bool SOFTCAP, bool DROP>
 __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint32_t sbase,
                              uint32_t tmem, const CUtensorMap* to) {
-  using L = Layout<D>;
+  using L = LayoutFor<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int q = (warp - 4) >> 2;  // the tile this warpgroup owns
   const int r = ((warp & 3) << 5) + lane;
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
-  // d = 256: the key blocks of the one tile alternate between the S buffers
-  constexpr bool kAlt = D == 256;
+  // the one-tile form: its key blocks alternate between the S buffers
+  constexpr bool kAlt = kOneTile<D>;
   const uint32_t tO = tmem + lane_base + 256 + q * D;
   const int qrow = w.m0[q] + r;
   const int bar_wg = 1 + q;  // named barrier of this warpgroup (128 threads)
@@ -723,7 +744,7 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint3
   // ---- epilogue: O / l -> bf16 rows in the tile's Q buffer (free once its
   // last S GEMM is done, which precedes the last P V) -> TMA tensor store;
   // LSE in natural log
-  // d = 256 issues S(j + 1) before P(j) V, so P(nt - 2) V may still run:
+  // the one-tile form issues S(j + 1) before P(j) V, so P(nt - 2) V may still run:
   // its phase of O_DONE completes first (a wait on the parity of the last
   // phase would pass while the one before it is still open)
   if (ok && kAlt && nt >= 2) ok = wait(c, BAR_O_DONE + q, (nt - 2) & 1);
@@ -764,6 +785,161 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint3
         l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
 }
 
+// Softmax of the one-tile form: the two warpgroups share the tile, warpgroup
+// h taking keys 64 h .. 64 h + 63 of every key block (thread = query row r
+// in both). Per block they exchange the half-row maxima through shared
+// memory, so both take the same shift; each keeps the row sum of its half,
+// writes P of its keys (warpgroup 1 into columns 64-95, so that it never
+// overwrites S values warpgroup 0 still reads) and rescales its half of the
+// O row. At the end the two row sums are added, and warpgroup h writes
+// columns h d/2 .. of O. Every decision is taken by both warpgroups together
+// (a 256-thread barrier with an AND), so an abort leaves none of them behind.
+constexpr int kBarBoth = 3;  // named barrier of both softmax warpgroups
+
+template <int D, bool SOFTCAP, bool DROP>
+__device__ void softmax_role_split(const Ctx& c, const Params& p, const Work& w, uint8_t* smem,
+                                   uint32_t sbase, uint32_t tmem, const CUtensorMap* to) {
+  using L = LayoutOne<D>;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = (warp - 4) >> 2;  // which half of the keys (and of O's columns)
+  const int r = ((warp & 3) << 5) + lane;
+  const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
+  const uint32_t tO = tmem + lane_base + 256 + h * (D / 2);
+  float* xmax = reinterpret_cast<float*>(smem + L::kXchg);  // [block parity][half][row]
+  float* xsum = xmax + 4 * 128;                              // [half][row]
+  const int qrow = w.m0[0] + r;
+  const int bar_wg = 1 + h;
+  const float c_log2 = p.scale * kLog2e;
+  const float cap_in = SOFTCAP ? 2.f * kLog2e * p.scale / p.softcap : 0.f;  // 2 log2e tau/c
+  const float cap_out = SOFTCAP ? p.softcap * kLog2e : 0.f;                 // c log2e
+  const int nt = w.nt[0];
+  float m_used = -INFINITY, l = 0.f;
+  bool ok = true;
+  const uint32_t bh = static_cast<uint32_t>(w.bh);
+  const int m0 = w.m0[0];
+  for (int t = 0; t < nt; ++t) {
+    const int n0 = (w.j0[0] + t) * kBn;
+    const int key0 = n0 + 64 * h;
+    const uint32_t tS = tmem + lane_base + (t & 1) * 128;
+    const uint32_t src = tS + 64 * h;
+    // the keep bits of this half's 64 keys, drawn while the S GEMM runs
+    const uint32_t kb0 = DROP ? keep_bits32(p, qrow, key0, bh) : 0xFFFFFFFFu;
+    const uint32_t kb1 = DROP ? keep_bits32(p, qrow, key0 + 32, bh) : 0xFFFFFFFFu;
+    ok = named_bar_and(kBarBoth, 256, wait(c, BAR_S_FULL + (t & 1), (t >> 1) & 1));
+    if (!ok) break;
+    tc_fence_after();
+    const bool masked =
+        n0 + kBn - 1 - m0 > p.win_right || m0 + kBm - 1 - n0 > p.win_left || n0 + kBn > p.N;
+    const float hmax =
+        masked ? chunk_max<true>(p, src, key0, qrow) : chunk_max<false>(p, src, key0, qrow);
+    float* slot = xmax + (t & 1) * 256;
+    slot[h * 128 + r] = hmax;
+    named_bar_sync(kBarBoth, 256);
+    const float smax = fmaxf(hmax, slot[(1 - h) * 128 + r]);
+    float m_tile = -INFINITY;  // row maximum of x = logit * log2e over this block
+    if (smax > -INFINITY) {
+      if (SOFTCAP) {
+        const float ex = ex2_approx(smax * cap_in);
+        m_tile = (1.f - 2.f * rcp_approx(ex + 1.f)) * cap_out;
+      } else {
+        m_tile = smax * c_log2;
+      }
+    }
+    // move the shift when the maximum outgrows it by more than kRescale (the
+    // same decision in both warpgroups: they see the same maxima)
+    const bool need = m_tile > m_used + kRescale;
+    if (__any_sync(0xffffffffu, need)) {
+      const float m_new = need ? m_tile : m_used;
+      const float f = need ? ex2_approx(m_used - m_new) : 1.f;  // 0 while m_used = -inf
+      // this half of the O row, once P(t - 1) V has completed
+      if (__any_sync(0xffffffffu, need && m_used > -INFINITY) && t > 0) {
+        if (!wait_warp(c, BAR_O_DONE, (t - 1) & 1)) ok = false;
+        if (ok) {
+          tc_fence_after();
+          const uint64_t f2 = f2_make(f, f);
+#pragma unroll
+          for (int c32 = 0; c32 < D / 64; ++c32) {
+            uint32_t o[32];
+            tmem_ld32(tO + c32 * 32, o);
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const uint64_t v = f2_mul(f2_make(o[2 * u], o[2 * u + 1]), f2);
+              o[2 * u] = static_cast<uint32_t>(v);
+              o[2 * u + 1] = static_cast<uint32_t>(v >> 32);
+            }
+            uint32_t lo[16], hi[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              lo[u] = o[u];
+              hi[u] = o[16 + u];
+            }
+            tmem_st16(tO + c32 * 32, lo);
+            tmem_st16(tO + c32 * 32 + 16, hi);
+          }
+        }
+      }
+      l *= f;
+      m_used = m_new;
+    }
+    ok = named_bar_and(kBarBoth, 256, ok);
+    if (!ok) break;
+    const float shift = m_used > -INFINITY ? m_used : 0.f;
+    const uint32_t dst = tS + 64 * h;  // keys 0-63 -> columns 0-31, 64-127 -> 64-95
+    l += masked ? chunk_p<SOFTCAP, true, DROP>(p, src, dst, key0, qrow, c_log2, cap_in, cap_out,
+                                               shift, kb0, kb1)
+                : chunk_p<SOFTCAP, false, DROP>(p, src, dst, key0, qrow, c_log2, cap_in, cap_out,
+                                                shift, kb0, kb1);
+    tmem_wait_st();
+    tc_fence_before();
+    named_bar_sync(bar_wg, 128);
+    if (r == 0) mbar_arrive(bar_addr(c, BAR_P_FULL + (t & 1)));
+  }
+  // ---- epilogue. S(j + 1) is issued before P(j) V, so P(nt - 2) V may still
+  // run: its phase of O_DONE completes first (a wait on the parity of the
+  // last phase alone would pass while the one before it is still open).
+  if (ok && nt >= 2) ok = wait(c, BAR_O_DONE, (nt - 2) & 1);
+  if (ok) ok = wait(c, BAR_O_DONE, (nt - 1) & 1);
+  xsum[h * 128 + r] = l;
+  if (!named_bar_and(kBarBoth, 256, ok)) return;
+  tc_fence_after();
+  const float lt = xsum[r] + xsum[128 + r];
+  const float inv = lt > 0.f ? 1.f / lt : 0.f;
+  const uint64_t inv2 = f2_make(inv, inv);
+  // O / l of this half's columns -> bf16 rows in the Q buffer (free once the
+  // last S GEMM is done, which precedes the last P V) -> TMA tensor stores
+  const uint32_t buf = sbase + L::kQ0;
+#pragma unroll
+  for (int c16 = 0; c16 < D / 32; ++c16) {
+    const int col = h * (D / 2) + c16 * 16;  // column of O
+    uint32_t raw[16];
+    tmem_ld16(tO + c16 * 16, raw);
+    uint32_t packed[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint64_t v = f2_mul(f2_make(raw[2 * u], raw[2 * u + 1]), inv2);
+      packed[u] = pack_bf16x2(f2_lo(v), f2_hi(v));
+    }
+    // columns col .. col + 15: box col / 64, 16-byte chunks (col % 64) / 8, + 1
+    const uint32_t row_addr = buf + (col >> 6) * 16384 + r * 128;
+    const int c0 = (col & 63) >> 3;
+    st_shared_v4(row_addr + ((c0 ^ (r & 7)) << 4), packed[0], packed[1], packed[2], packed[3]);
+    st_shared_v4(row_addr + (((c0 + 1) ^ (r & 7)) << 4), packed[4], packed[5], packed[6],
+                 packed[7]);
+  }
+  fence_proxy_async_smem();
+  named_bar_sync(bar_wg, 128);
+  if (r == 0) {
+    for (int cb = h * (D / 128); cb < (h + 1) * (D / 128); ++cb)
+      tma_store_3d(to, buf + cb * 16384, 64 * cb, m0, w.bh);
+    bulk_commit_group();
+    bulk_wait_all();
+  }
+  if (h == 0 && qrow < p.N)
+    p.lse[static_cast<long long>(w.bh) * p.N + qrow] =
+        lt > 0.f ? (m_used + __log2f(lt)) * kLn2 : -INFINITY;
+}
+
 // ------------------------------------------------------------------ kernel
 template <int D, bool SOFTCAP, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -771,7 +947,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_o, const Params p) {
-  using L = Layout<D>;
+  using L = LayoutFor<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {  // the 128-byte swizzle atoms need 1024-byte alignment
@@ -784,6 +960,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar_addr(c, i), 1);
+    if (kOneTile<D>) {  // P of a block: one arrival per softmax warpgroup
+      mbar_init(bar_addr(c, BAR_P_FULL), 2);
+      mbar_init(bar_addr(c, BAR_P_FULL + 1), 2);
+    }
     *c.abort = 0;
     fence_barrier_init();
   }
@@ -797,17 +977,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
   const Work w = work_of<D>(p);
   if (warp == 0) {
-    if constexpr (D == 256)
-      producer_role256(c, w, sbase, &tm_q, &tm_k, &tm_v);
+    if constexpr (kOneTile<D>)
+      loader_role_one<D>(c, w, sbase, &tm_q, &tm_k, false);
     else
       producer_role<D>(c, w, sbase, &tm_q, &tm_k, &tm_v);
   } else if (warp == 1) {
-    if constexpr (D == 256)
-      mma_role256(c, w, sbase, tmem);
+    if constexpr (kOneTile<D>)
+      mma_role_one<D>(c, w, sbase, tmem);
     else
       mma_role<D>(c, w, sbase, tmem);
+  } else if (warp == 2) {
+    if constexpr (kOneTile<D>) loader_role_one<D>(c, w, sbase, &tm_q, &tm_v, true);
   } else if (warp >= 4) {
-    softmax_role<D, SOFTCAP, DROP>(c, p, w, sbase, tmem, &tm_o);
+    if constexpr (kOneTile<D>)
+      softmax_role_split<D, SOFTCAP, DROP>(c, p, w, smem, sbase, tmem, &tm_o);
+    else
+      softmax_role<D, SOFTCAP, DROP>(c, p, w, sbase, tmem, &tm_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -822,10 +1007,10 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
            const CUtensorMap& to, const Params& p, cudaStream_t stream) {
   auto kern = attn_fwd_kernel<D, SOFTCAP, DROP>;
   static std::atomic<bool> configured[kMaxTrackedDevices];
-  if (!set_smem_limit_once(kern, Layout<D>::kBytes, configured)) return ATTN_ERR_LAUNCH;
+  if (!set_smem_limit_once(kern, LayoutFor<D>::kBytes, configured)) return ATTN_ERR_LAUNCH;
   const long long grid = static_cast<long long>(p.pairs) * p.B * p.H;
   if (grid > 0x7fffffffLL) return ATTN_ERR_TOO_LARGE;
-  kern<<<static_cast<unsigned>(grid), kThreads, Layout<D>::kBytes, stream>>>(tq, tk, tv, to, p);
+  kern<<<static_cast<unsigned>(grid), kThreads, LayoutFor<D>::kBytes, stream>>>(tq, tk, tv, to, p);
   return launch_status();
 }
 
@@ -889,7 +1074,8 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
   p.H = H;
   p.H_kv = H_kv;
   p.N = N;
-  p.pairs = d == 256 ? (N + kBm - 1) / kBm : ((N + kBm - 1) / kBm + 1) / 2;
+  const bool one_tile = d == 256 ? kOneTile<256> : (d == 128 ? kOneTile<128> : kOneTile<64>);
+  p.pairs = one_tile ? (N + kBm - 1) / kBm : ((N + kBm - 1) / kBm + 1) / 2;
   p.scale = scale;
   const bool cap = softcap > 0.f;
   p.softcap = cap ? softcap : 0.f;

@@ -116,13 +116,14 @@ int attn_fwd_dropout(const void* q, const void* k, const void* v, void* o, float
  * attn_fwd: the same forward as attn_fwd_ref (same arguments, outputs and
  * layouts) on the tcgen05 tensor cores, in one pass with the online softmax
  * ([bwd-detail] §1.2; [FA-v1-bwd] §1.1 forward, §3.2 eq. 9-12 running
- * statistics): one CTA takes two blocks of 128 queries of a query head and
- * walks the visible key blocks once; O accumulates un-normalised in fp32
- * tensor memory, rescaled only when a row maximum grows by more than 2^8,
- * and is divided by the row sum at the end. P enters the PV GEMM as bf16.
- * d = 256 takes one block of 128 queries per CTA (two tiles' S and O would
- * exceed tensor memory) and alternates two S buffers over its key blocks.
- * scale must be > 0 (ATTN_ERR_SHAPE otherwise).
+ * statistics): a CTA walks the visible key blocks of its queries once; O
+ * accumulates un-normalised in fp32 tensor memory, rescaled only when a row
+ * maximum grows by more than 2^8, and is divided by the row sum at the end.
+ * P enters the PV GEMM as bf16. d = 64: a CTA takes two blocks of 128
+ * queries that ping-pong on the tensor cores; d = 128 and 256: one block of
+ * 128 queries, its key blocks alternating between two S buffers and its
+ * keys split between two softmax warpgroups. scale must be > 0
+ * (ATTN_ERR_SHAPE otherwise).
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
              int H_kv, int N, int d, float scale, int causal, float softcap, void* stream);
