@@ -484,10 +484,9 @@ __device__ void mma_role_one(const Ctx& c, const Work& w, uint32_t sbase, uint32
 // included. MASKED chunks (a band's edge, the sequence's end) leave
 // invisible keys out.
 template <bool MASKED>
-__device__ __forceinline__ float chunk_max(const Params& p, uint32_t src, int key0, int qrow) {
+__device__ __forceinline__ float chunk_max_regs(const Params& p, const uint32_t (&raw)[64],
+                                                int key0, int qrow) {
   float m0 = -INFINITY, m1 = -INFINITY;
-  uint32_t raw[64];
-  tmem_ld32x2(src, src + 32, raw);  // two 32-column loads per wait
 #pragma unroll
   for (int e = 0; e < 64; ++e) {
     float s = __uint_as_float(raw[e]);
@@ -501,6 +500,13 @@ __device__ __forceinline__ float chunk_max(const Params& p, uint32_t src, int ke
       m0 = fmaxf(m0, s);
   }
   return fmaxf(m0, m1);
+}
+
+template <bool MASKED>
+__device__ __forceinline__ float chunk_max(const Params& p, uint32_t src, int key0, int qrow) {
+  uint32_t raw[64];
+  tmem_ld32x2(src, src + 32, raw);  // two 32-column loads per wait
+  return chunk_max_regs<MASKED>(p, raw, key0, qrow);
 }
 
 // Row maximum of one S tile (both 64-key chunks).
@@ -559,17 +565,16 @@ __device__ __forceinline__ uint32_t keep_bits32(const Params& p, int qrow, int k
 // key0 + j (key0 + 32 + j); the sum stays that of P. dst may overlap src:
 // every S value of the chunk is read before the first P is written.
 template <bool SOFTCAP, bool MASKED, bool DROP>
-__device__ __forceinline__ float chunk_p(const Params& p, uint32_t src, uint32_t dst, int key0,
-                                         int qrow, float c_log2, float cap_in, float cap_out,
-                                         float shift, uint32_t kb0, uint32_t kb1) {
+__device__ __forceinline__ float chunk_p_regs(const Params& p, const uint32_t (&raw)[64],
+                                              uint32_t dst, int key0, int qrow, float c_log2,
+                                              float cap_in, float cap_out, float shift,
+                                              uint32_t kb0, uint32_t kb1) {
   const uint64_t c2v = f2_make(SOFTCAP ? cap_in : c_log2, SOFTCAP ? cap_in : c_log2);
   const uint64_t out2 = f2_make(cap_out, cap_out);
   const float cap_u = SOFTCAP ? p.scale / p.softcap : 0.f;  // u = tau s / c
   const uint64_t cu2 = f2_make(cap_u, cap_u);
   const uint64_t nsh2 = f2_make(-shift, -shift);
   uint64_t sum2 = f2_make(0.f, 0.f);
-  uint32_t raw[64];
-  tmem_ld32x2(src, src + 32, raw);  // two 32-column loads per wait
   uint32_t packed[32];
   // FAST: tanh by the polynomial (every |u| of the warp's 64 keys <= 1)
   auto p_group = [&](auto fast_tag) {
@@ -623,6 +628,16 @@ __device__ __forceinline__ float chunk_p(const Params& p, uint32_t src, uint32_t
   tmem_st16(dst, lo);
   tmem_st16(dst + 16, hi);
   return f2_lo(sum2) + f2_hi(sum2);
+}
+
+template <bool SOFTCAP, bool MASKED, bool DROP>
+__device__ __forceinline__ float chunk_p(const Params& p, uint32_t src, uint32_t dst, int key0,
+                                         int qrow, float c_log2, float cap_in, float cap_out,
+                                         float shift, uint32_t kb0, uint32_t kb1) {
+  uint32_t raw[64];
+  tmem_ld32x2(src, src + 32, raw);  // two 32-column loads per wait
+  return chunk_p_regs<SOFTCAP, MASKED, DROP>(p, raw, dst, key0, qrow, c_log2, cap_in, cap_out,
+                                             shift, kb0, kb1);
 }
 
 // P of one S tile over the first half of its buffer: keys 64 c .. 64 c + 63
@@ -826,16 +841,27 @@ __device__ void softmax_role_split(const Ctx& c, const Params& p, const Work& w,
     // the keep bits of this half's 64 keys, drawn while the S GEMM runs
     const uint32_t kb0 = DROP ? keep_bits32(p, qrow, key0, bh) : 0xFFFFFFFFu;
     const uint32_t kb1 = DROP ? keep_bits32(p, qrow, key0 + 32, bh) : 0xFFFFFFFFu;
-    ok = named_bar_and(kBarBoth, 256, wait(c, BAR_S_FULL + (t & 1), (t >> 1) & 1));
-    if (!ok) break;
-    tc_fence_after();
+    // The scores are read from tensor memory once and kept in registers for
+    // the maximum and P. The one barrier of both warpgroups per block carries
+    // the half-row maxima and the abort decision (a wait that gave up, here
+    // or at the previous block's O rescale).
+    const bool got = wait(c, BAR_S_FULL + (t & 1), (t >> 1) & 1);
+    uint32_t raw[64];
+    if (got) {
+      tc_fence_after();
+      tmem_ld32x2(src, src + 32, raw);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 64; ++e) raw[e] = 0u;
+    }
     const bool masked =
         n0 + kBn - 1 - m0 > p.win_right || m0 + kBm - 1 - n0 > p.win_left || n0 + kBn > p.N;
-    const float hmax =
-        masked ? chunk_max<true>(p, src, key0, qrow) : chunk_max<false>(p, src, key0, qrow);
+    const float hmax = masked ? chunk_max_regs<true>(p, raw, key0, qrow)
+                              : chunk_max_regs<false>(p, raw, key0, qrow);
     float* slot = xmax + (t & 1) * 256;
     slot[h * 128 + r] = hmax;
-    named_bar_sync(kBarBoth, 256);
+    ok = named_bar_and(kBarBoth, 256, ok && got);
+    if (!ok) break;
     const float smax = fmaxf(hmax, slot[(1 - h) * 128 + r]);
     float m_tile = -INFINITY;  // row maximum of x = logit * log2e over this block
     if (smax > -INFINITY) {
@@ -852,7 +878,8 @@ __device__ void softmax_role_split(const Ctx& c, const Params& p, const Work& w,
     if (__any_sync(0xffffffffu, need)) {
       const float m_new = need ? m_tile : m_used;
       const float f = need ? ex2_approx(m_used - m_new) : 1.f;  // 0 while m_used = -inf
-      // this half of the O row, once P(t - 1) V has completed
+      // this half of the O row, once P(t - 1) V has completed; a wait that
+      // gives up is voted on at the next barrier
       if (__any_sync(0xffffffffu, need && m_used > -INFINITY) && t > 0) {
         if (!wait_warp(c, BAR_O_DONE, (t - 1) & 1)) ok = false;
         if (ok) {
@@ -882,18 +909,16 @@ __device__ void softmax_role_split(const Ctx& c, const Params& p, const Work& w,
       l *= f;
       m_used = m_new;
     }
-    ok = named_bar_and(kBarBoth, 256, ok);
-    if (!ok) break;
     const float shift = m_used > -INFINITY ? m_used : 0.f;
     const uint32_t dst = tS + 64 * h;  // keys 0-63 -> columns 0-31, 64-127 -> 64-95
-    l += masked ? chunk_p<SOFTCAP, true, DROP>(p, src, dst, key0, qrow, c_log2, cap_in, cap_out,
-                                               shift, kb0, kb1)
-                : chunk_p<SOFTCAP, false, DROP>(p, src, dst, key0, qrow, c_log2, cap_in, cap_out,
-                                                shift, kb0, kb1);
+    l += masked ? chunk_p_regs<SOFTCAP, true, DROP>(p, raw, dst, key0, qrow, c_log2, cap_in,
+                                                    cap_out, shift, kb0, kb1)
+                : chunk_p_regs<SOFTCAP, false, DROP>(p, raw, dst, key0, qrow, c_log2, cap_in,
+                                                     cap_out, shift, kb0, kb1);
     tmem_wait_st();
     tc_fence_before();
-    named_bar_sync(bar_wg, 128);
-    if (r == 0) mbar_arrive(bar_addr(c, BAR_P_FULL + (t & 1)));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_addr(c, BAR_P_FULL + (t & 1)));  // one arrival per warp
   }
   // ---- epilogue. S(j + 1) is issued before P(j) V, so P(nt - 2) V may still
   // run: its phase of O_DONE completes first (a wait on the parity of the
@@ -960,9 +985,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNumBars; ++i) mbar_init(bar_addr(c, i), 1);
-    if (kOneTile<D>) {  // P of a block: one arrival per softmax warpgroup
-      mbar_init(bar_addr(c, BAR_P_FULL), 2);
-      mbar_init(bar_addr(c, BAR_P_FULL + 1), 2);
+    if (kOneTile<D>) {  // P of a block: one arrival per softmax warp
+      mbar_init(bar_addr(c, BAR_P_FULL), 8);
+      mbar_init(bar_addr(c, BAR_P_FULL + 1), 8);
     }
     *c.abort = 0;
     fence_barrier_init();
