@@ -272,7 +272,7 @@ __device__ void producer_role(const Ctx& c, const Params& p, const Work& w, uint
     issued_q = t + 1;
     __syncwarp();
   }
-  if (*c.abort) {  // the copies issued last must land before the CTA exits
+  if (!ok || *c.abort) {  // the copies issued last must land before the CTA exits
     wait_drain(c, BAR_KV_FULL, 0);
     if (issued_q > 0) wait_drain(c, BAR_QH_FULL, (issued_q - 1) & 1);
     if (issued_qo > 0) wait_drain(c, BAR_QO_FULL, (issued_qo - 1) & 1);
