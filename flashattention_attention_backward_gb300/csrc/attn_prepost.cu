@@ -3,11 +3,13 @@
 //
 //  * preprocess: D_i = sum_k dO_ik O_ik ("解析 FlashAttention（3）" §2.4 eq. 6;
 //    "反向传播算法详解" §2.1(3): dPsum can be formed before the backward kernel
-//    starts) and dq_accum := 0, in one pass. One warp per row: the row of O
-//    and dO is read once (4 bf16 per lane per step), reduced with shuffles,
-//    and the matching fp32 dQ-accumulator row is cleared with 16-byte stores.
+//    starts) and dq_accum := 0, in one pass. For d = 64, 128, 256 a row is
+//    read by d / 8 lanes with 16-byte loads (two steps in flight per
+//    thread), reduced with shuffles, and the matching fp32 dQ-accumulator
+//    row is cleared with 16-byte stores; other d, one warp per row.
 //  * finalize: dq = bf16(tau * dq_accum) ("解析 FlashAttention（3）" eq. 7),
-//    16 bytes read / 8 bytes written per thread step.
+//    16 bytes read / 8 bytes written per element group, four groups in
+//    flight per thread.
 //  * finalize_partials (deterministic dQ): dq = bf16(tau * sum over key
 //    blocks n, in increasing n, of the stored partial tiles dS_mn K_n of
 //    query block m) ("反向传播算法详解" §6.4: a fixed order of the
@@ -52,19 +54,90 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// The same for d = 64, 128 and 256 with 16-byte loads: d / 8 lanes share a
+// row (a warp covers 32 / (d / 8) rows per step), and each thread keeps two
+// steps in flight, so that the loads in flight per SM cover the memory
+// latency while the L2 also writes back what the backward kernel left dirty.
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+    preprocess_vec_kernel(const __nv_bfloat16* __restrict__ o,
+                          const __nv_bfloat16* __restrict__ dO, float* __restrict__ dpsum,
+                          float* __restrict__ dq_accum, long long rows) {
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kRowsPerStep = 32 / kLanesPerRow;
+  constexpr int kSteps = 2;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / kLanesPerRow, li = lane % kLanesPerRow;
+  const long long warp0 = (static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * kThreads) >> 5;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long r0 = warp0 * kRowsPerStep * kSteps; r0 < rows;
+       r0 += nwarps * kRowsPerStep * kSteps) {
+    uint4 uo[kSteps], ud[kSteps];
+#pragma unroll
+    for (int u = 0; u < kSteps; ++u) {
+      const long long row = r0 + u * kRowsPerStep + sub;
+      uo[u] = make_uint4(0u, 0u, 0u, 0u);
+      ud[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (row < rows) {
+        uo[u] = __ldcs(reinterpret_cast<const uint4*>(o + row * D) + li);
+        ud[u] = __ldcs(reinterpret_cast<const uint4*>(dO + row * D) + li);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kSteps; ++u) {
+      const long long row = r0 + u * kRowsPerStep + sub;
+      const uint32_t wo[4] = {uo[u].x, uo[u].y, uo[u].z, uo[u].w};
+      const uint32_t wd[4] = {ud[u].x, ud[u].y, ud[u].z, ud[u].w};
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(__uint_as_float(wo[e] << 16), __uint_as_float(wd[e] << 16), acc);
+        acc = fmaf(__uint_as_float(wo[e] & 0xffff0000u), __uint_as_float(wd[e] & 0xffff0000u),
+                   acc);
+      }
+      // sum over the row's lanes (aligned groups of kLanesPerRow lanes)
+#pragma unroll
+      for (int off = kLanesPerRow / 2; off >= 1; off >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (row < rows) {
+        if (li == 0) dpsum[row] = acc;
+        if (dq_accum != nullptr) {
+          float4* z = reinterpret_cast<float4*>(dq_accum + row * D) + 2 * li;
+          z[0] = zero;
+          z[1] = zero;
+        }
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads)
     finalize_kernel(const float* __restrict__ dq_accum, __nv_bfloat16* __restrict__ dq,
                     float scale, long long n4) {
+  // four 16-byte loads in flight per thread before the stores
+  constexpr int kUnroll = 4;
   const long long stride = static_cast<long long>(gridDim.x) * kThreads;
-  for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < n4;
-       i += stride) {
-    const float4 a = __ldcs(reinterpret_cast<const float4*>(dq_accum) + i);
-    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * scale, a.y * scale);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * scale, a.w * scale);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&lo);
-    u.y = *reinterpret_cast<uint32_t*>(&hi);
-    __stcs(reinterpret_cast<uint2*>(dq) + i, u);
+  for (long long i0 = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i0 < n4;
+       i0 += stride * kUnroll) {
+    float4 a[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long i = i0 + u * stride;
+      a[u] = i < n4 ? __ldcs(reinterpret_cast<const float4*>(dq_accum) + i)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long i = i0 + u * stride;
+      if (i >= n4) break;
+      __nv_bfloat162 lo = __floats2bfloat162_rn(a[u].x * scale, a[u].y * scale);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(a[u].z * scale, a[u].w * scale);
+      uint2 v;
+      v.x = *reinterpret_cast<uint32_t*>(&lo);
+      v.y = *reinterpret_cast<uint32_t*>(&hi);
+      __stcs(reinterpret_cast<uint2*>(dq) + i, v);
+    }
   }
 }
 
@@ -138,10 +211,26 @@ extern "C" int attn_bwd_preprocess(const void* o, const void* dO, float* dpsum, 
     return ATTN_ERR_ALIGN;
   const long long rows = static_cast<long long>(B) * H * N;
   if (rows == 0) return ATTN_OK;
+  const auto* o16 = static_cast<const __nv_bfloat16*>(o);
+  const auto* d16 = static_cast<const __nv_bfloat16*>(dO);
+  cudaStream_t s = as_stream(stream);
+  if (d == 64 || d == 128 || d == 256) {
+    // rows per CTA per grid-stride pass: 8 warps x (256 / d) rows x 2 steps
+    const unsigned grid = prepost::grid_for(rows, (prepost::kThreads / 32) * (256 / d) * 2);
+    if (d == 64)
+      prepost::preprocess_vec_kernel<64><<<grid, prepost::kThreads, 0, s>>>(o16, d16, dpsum,
+                                                                           dq_accum, rows);
+    else if (d == 128)
+      prepost::preprocess_vec_kernel<128><<<grid, prepost::kThreads, 0, s>>>(o16, d16, dpsum,
+                                                                            dq_accum, rows);
+    else
+      prepost::preprocess_vec_kernel<256><<<grid, prepost::kThreads, 0, s>>>(o16, d16, dpsum,
+                                                                            dq_accum, rows);
+    return launch_status();
+  }
   const unsigned grid = prepost::grid_for(rows, prepost::kThreads / 32);
-  prepost::preprocess_kernel<<<grid, prepost::kThreads, 0, as_stream(stream)>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), dpsum,
-      dq_accum, rows, d);
+  prepost::preprocess_kernel<<<grid, prepost::kThreads, 0, s>>>(o16, d16, dpsum, dq_accum, rows,
+                                                                d);
   return launch_status();
 }
 
@@ -155,7 +244,7 @@ extern "C" int attn_bwd_finalize(const float* dq_accum, void* dq, float scale, i
   if (!aligned16(dq_accum) || !aligned16(dq)) return ATTN_ERR_ALIGN;
   const long long n4 = static_cast<long long>(B) * H * N * d / 4;
   if (n4 == 0) return ATTN_OK;
-  const unsigned grid = prepost::grid_for(n4, prepost::kThreads);
+  const unsigned grid = prepost::grid_for(n4, prepost::kThreads * 4);
   prepost::finalize_kernel<<<grid, prepost::kThreads, 0, as_stream(stream)>>>(
       dq_accum, static_cast<__nv_bfloat16*>(dq), scale, n4);
   return launch_status();
