@@ -445,7 +445,13 @@ def all_configs(dev, peak, iters=20, warmup=3):
     out["causal_gqa_window1024"] = local_window_timing(dev, peak, iters, warmup)
     out["causal_gqa_variants"] = variant_timing(dev, peak, iters, warmup)
     out["causal_gqa_d256"] = d256_timing(dev, peak, iters, warmup)
+    out["causal_gqa_d256_variants"] = variant_timing(dev, peak, iters, warmup, w=d256_workload())
     return out
+
+
+def d256_workload():
+    from flashattention_attention_backward_gb300.inputs import Workload
+    return Workload("causal_gqa_d256", 2, 16, 4, 4096, 256, True, seed_base=20261202 + 6000)
 
 
 def d256_timing(dev, peak, iters, warmup):
@@ -455,9 +461,9 @@ def d256_timing(dev, peak, iters, warmup):
     head, halved for causal)."""
     import flashattention_attention_backward_gb300 as attn
     from flashattention_attention_backward_gb300 import runner
-    from flashattention_attention_backward_gb300.inputs import Workload, make_inputs
+    from flashattention_attention_backward_gb300.inputs import make_inputs
 
-    w = Workload("causal_gqa_d256", 2, 16, 4, 4096, 256, True, seed_base=20261202 + 6000)
+    w = d256_workload()
     stream = torch.cuda.current_stream(dev)
     x = make_inputs(w)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
@@ -504,16 +510,17 @@ def d256_timing(dev, peak, iters, warmup):
             "fwd_ms": fms, "fwd_tflops": ftf, "fwd_frac_of_peak": ftf / peak}
 
 
-def variant_timing(dev, peak, iters, warmup, p_drop=0.1, seed=1234):
+def variant_timing(dev, peak, iters, warmup, p_drop=0.1, seed=1234, w=None):
     """The deterministic-dQ step (preprocess + attn_bwd_deterministic +
     attn_bwd_finalize_partials), attn_bwd_dropout and attn_fwd_dropout on the
-    causal GQA workload, against the plain step and attn_fwd; FLOPs as for
-    the plain kernels."""
+    causal GQA workload (or `w`, a causal workload), against the plain step
+    and attn_fwd; FLOPs as for the plain kernels."""
     import flashattention_attention_backward_gb300 as attn
     from flashattention_attention_backward_gb300 import runner
     from flashattention_attention_backward_gb300.inputs import WORKLOADS, make_inputs
 
-    w = WORKLOADS["causal_gqa"]
+    if w is None:
+        w = WORKLOADS["causal_gqa"]
     B, H, H_kv, N, d = w.B, w.H, w.H_kv, w.N, w.d
     stream = torch.cuda.current_stream(dev)
     x = make_inputs(w)
@@ -719,13 +726,13 @@ def kernel_only(args, w):
     between them (inputs prepared first); returns a short JSON-able record."""
     import flashattention_attention_backward_gb300 as attn
     from flashattention_attention_backward_gb300 import runner
-    from flashattention_attention_backward_gb300.inputs import Workload, make_inputs
+    from flashattention_attention_backward_gb300.inputs import make_inputs
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     if args.kernel_only in ("attn_bwd_d256", "attn_fwd_d256"):  # the d = 256 shape of all_configs
-        w = Workload("causal_gqa_d256", 2, 16, 4, 4096, 256, True, seed_base=20261202 + 6000)
+        w = d256_workload()
     x = make_inputs(w)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     win = (args.window_left, -1) if args.kernel_only.endswith("_local") else None
