@@ -1158,6 +1158,9 @@ int run(const void* q, const void* k, const void* v, const void* dO, const float
   p.drop.seed_hi = static_cast<uint32_t>(seed >> 32);
   p.drop.threshold = dropout_threshold(p_drop);
   p.drop.inv_keep = 1.f / (1.f - p_drop);
+  p.drop.keep = 1.f - p_drop;
+  p.drop.log2_inv_keep =
+      static_cast<float>(-std::log2(1.0 - static_cast<double>(p_drop)));
 
   Maps m;
   const long long hq = static_cast<long long>(B) * H, hk = static_cast<long long>(B) * H_kv;

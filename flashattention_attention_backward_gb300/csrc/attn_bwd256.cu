@@ -762,6 +762,9 @@ int bwd256_run(const void* q, const void* k, const void* v, const void* dO, cons
   p.drop.seed_hi = static_cast<uint32_t>(seed >> 32);
   p.drop.threshold = dropout_threshold(p_drop);
   p.drop.inv_keep = 1.f / (1.f - p_drop);
+  p.drop.keep = 1.f - p_drop;
+  p.drop.log2_inv_keep =
+      static_cast<float>(-std::log2(1.0 - static_cast<double>(p_drop)));
   const long long grid = 2LL * p.n_blocks * H_kv * B;
   if (grid > 0x7fffffffLL) return ATTN_ERR_TOO_LARGE;
   CUtensorMap m[7];  // q, k, v, dO, dq (reduce), dk, dv (store)

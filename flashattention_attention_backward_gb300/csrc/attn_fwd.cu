@@ -41,6 +41,7 @@
 //   warp 2      V_j in the same kind of ring
 //   warp 1      MMA issuer: S(0), then per block S(j + 1), P(j) V
 //   warps 4-11  softmax, then the epilogue (each warpgroup its half of O)
+//   warps 12-19 with dropout only: the keep mask, one key block ahead
 // Every mbarrier wait is bounded, as in attn_bwd.
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -92,6 +93,22 @@ static_assert(Layout<128>::kBytes <= 232448, "shared memory budget");
 template <int D>
 constexpr bool kOneTile = D >= 128;
 
+// With dropout the one-tile form draws the keep mask in a warpgroup of its
+// own. Philox4x32-10 is bound by the 32 x 32 -> 64-bit multiplies (measured
+// on this GPU: about 1.3 calls per clock per SM, some 3,000 cycles for the
+// 4,096 calls of a 128 x 128 block), about as long as the softmax of a
+// block; drawn inline it adds to the softmax's critical path, drawn by
+// warps 12-15 for block j + 1 while the softmax works on block j it runs
+// beside it. The CTA then has 640 threads; setmaxnreg gives the softmax
+// warps 128 registers and the other twelve warps 72.
+template <int D, bool DROP>
+constexpr bool kMaskRole = kOneTile<D> && DROP;
+template <int D, bool DROP>
+constexpr int kThreadsFor = kMaskRole<D, DROP> ? 640 : kThreads;
+constexpr int kMaskWarps = 8;  // two per SM sub-partition
+constexpr int kRegsSoftmaxDrop = 128, kRegsOtherDrop = 72;
+static_assert(256 * kRegsSoftmaxDrop + 384 * kRegsOtherDrop <= 640 * 96, "register pool");
+
 template <int D>
 struct LayoutOne {
   static constexpr int kTileBytes = 128 * D * 2;
@@ -106,8 +123,11 @@ struct LayoutOne {
   // the two softmax warpgroups' half-row maxima (two blocks in flight) and
   // row sums: [2][2][128] + [2][128] fp32
   static constexpr int kXchg = kV1 + kTileBytes;
-  static constexpr int kBars = kXchg + 6 * 128 * 4;
-  static constexpr int kNumBars = 17;
+  // dropout keep bits of two key blocks: [block parity][key half][row] x
+  // 2 words (bit j of word w: key 64 half + 32 w + j of the block)
+  static constexpr int kMask = kXchg + 6 * 128 * 4;
+  static constexpr int kBars = kMask + 2 * 2048;
+  static constexpr int kNumBars = 21;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kUsed = kAbort + 12;
@@ -128,6 +148,8 @@ enum Bar {
   BAR_P_FULL = 12,   // + tile (d = 256: + S buffer): P_q(j) written (and O_q rescaled if needed)
   BAR_O_DONE = 14,   // + tile: P_q(j) V_j completed (one phase per key block of the tile)
   BAR_DRAIN = 16,    // abort path only: completion of everything issued
+  BAR_MASK_FULL = 17,   // + block parity (one-tile form with dropout): keep bits written
+  BAR_MASK_EMPTY = 19,  // + block parity: the softmax has read them
 };
 
 struct Params {
@@ -562,8 +584,11 @@ __device__ __forceinline__ uint32_t keep_bits32(const Params& p, int qrow, int k
 // 63) as bf16 pairs in columns dst .. dst + 31; returns their sum of P (fp32,
 // before rounding and before dropout). With DROP the bf16 values are
 // P o Z / (1 - p), Z the keep mask whose bit j of kb0 (kb1) belongs to key
-// key0 + j (key0 + 32 + j); the sum stays that of P. dst may overlap src:
-// every S value of the chunk is read before the first P is written.
+// key0 + j (key0 + 32 + j): the exponent carries log2(1 / (1 - p)), so exp2
+// gives P / (1 - p), and the sum returned is that of P / (1 - p) over every
+// key (the caller multiplies the row sum by 1 - p at the end). dst may
+// overlap src: every S value of the chunk is read before the first P is
+// written.
 template <bool SOFTCAP, bool MASKED, bool DROP>
 __device__ __forceinline__ float chunk_p_regs(const Params& p, const uint32_t (&raw)[64],
                                               uint32_t dst, int key0, int qrow, float c_log2,
@@ -573,7 +598,8 @@ __device__ __forceinline__ float chunk_p_regs(const Params& p, const uint32_t (&
   const uint64_t out2 = f2_make(cap_out, cap_out);
   const float cap_u = SOFTCAP ? p.scale / p.softcap : 0.f;  // u = tau s / c
   const uint64_t cu2 = f2_make(cap_u, cap_u);
-  const uint64_t nsh2 = f2_make(-shift, -shift);
+  const float nsh = DROP ? p.drop.log2_inv_keep - shift : -shift;
+  const uint64_t nsh2 = f2_make(nsh, nsh);
   uint64_t sum2 = f2_make(0.f, 0.f);
   uint32_t packed[32];
   // FAST: tanh by the polynomial (every |u| of the warp's 64 keys <= 1)
@@ -603,8 +629,8 @@ __device__ __forceinline__ float chunk_p_regs(const Params& p, const uint32_t (&
       if (DROP) {
         const uint32_t kb = u < 16 ? kb0 : kb1;
         const int bit = (2 * u) & 31;
-        const float d0 = (kb >> bit) & 1u ? p0 * p.drop.inv_keep : 0.f;
-        const float d1 = (kb >> (bit + 1)) & 1u ? p1 * p.drop.inv_keep : 0.f;
+        const float d0 = (kb >> bit) & 1u ? p0 : 0.f;
+        const float d1 = (kb >> (bit + 1)) & 1u ? p1 : 0.f;
         packed[u] = pack_bf16x2(d0, d1);
       } else {
         packed[u] = pack_bf16x2(p0, p1);
@@ -766,6 +792,7 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint3
   if (ok) ok = wait(c, BAR_O_DONE + q, (nt - 1) & 1);
   if (!named_bar_and(bar_wg, 128, ok)) return;
   tc_fence_after();
+  if (DROP) l *= p.drop.keep;  // the sums were of P / (1 - p)
   const float inv = l > 0.f ? 1.f / l : 0.f;
   const uint64_t inv2 = f2_make(inv, inv);
   const uint32_t buf = sbase + (q ? L::kQ1 : L::kQ0);
@@ -809,6 +836,57 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint3
 // O row. At the end the two row sums are added, and warpgroup h writes
 // columns h d/2 .. of O. Every decision is taken by both warpgroups together
 // (a 256-thread barrier with an AND), so an abort leaves none of them behind.
+// The keep mask of the one-tile form with dropout (warps 12-19, two per SM
+// sub-partition). For each key block of the CTA's tile, warp 12 + w and lane
+// q draw the Philox calls of the query quad q (rows 4q .. 4q + 3, counter
+// word 0 = (m0 + 4q) / 4) and of the 16 keys 16 w .. 16 w + 15 of the block:
+// call g gives the four rows' words of key g, so the thread ends with 16 bits
+// of each of its four rows, half of a 32-key word. Block j goes to slot
+// j mod 2 once the softmax has read block j - 2 out of it; the softmax reads
+// block j's words while the one after is drawn.
+template <int D>
+__device__ void mask_role(const Ctx& c, const Params& p, const Work& w, uint8_t* smem) {
+  using L = LayoutOne<D>;
+  const int lane = threadIdx.x & 31;
+  const int mw = (static_cast<int>(threadIdx.x) >> 5) - 12;  // 16-key group of a block
+  const uint32_t qgrp = static_cast<uint32_t>(w.m0[0] >> 2) + static_cast<uint32_t>(lane);
+  const uint32_t bh = static_cast<uint32_t>(w.bh);
+  uint16_t* mask = reinterpret_cast<uint16_t*>(smem + L::kMask);
+  const int nt = w.nt[0];
+  for (int t = 0; t < nt; ++t) {
+    const int slot = t & 1;
+    if (t >= 2 && !wait(c, BAR_MASK_EMPTY + slot, ((t >> 1) - 1) & 1)) return;
+    const uint32_t k0 = static_cast<uint32_t>((w.j0[0] + t) * kBn + 16 * mw);
+    uint32_t bits[4] = {0u, 0u, 0u, 0u};
+    constexpr int kNB = 4;  // calls in flight
+#pragma unroll 1
+    for (int g0 = 0; g0 < 16; g0 += kNB) {
+      uint32_t ctr[kNB][4];
+#pragma unroll
+      for (int u = 0; u < kNB; ++u) {
+        ctr[u][0] = qgrp;
+        ctr[u][1] = k0 + static_cast<uint32_t>(g0 + u);
+        ctr[u][2] = bh;
+        ctr[u][3] = 0u;
+      }
+      philox4x32_10_batch<kNB>(ctr, p.drop.seed_lo, p.drop.seed_hi);
+#pragma unroll
+      for (int u = 0; u < kNB; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          bits[e] |= (ctr[u][e] >= p.drop.threshold ? 1u : 0u) << (g0 + u);
+    }
+    // row 4 lane + e: 32-key word mw / 4 (key half mw / 4, word (mw / 2) mod
+    // 2), 16-bit half mw mod 2
+    const int kg = mw >> 1;
+    uint16_t* dst = mask + slot * 1024 + ((kg >> 1) * 256 + (kg & 1)) * 2 + (mw & 1);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dst[(4 * lane + e) * 4] = static_cast<uint16_t>(bits[e]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_addr(c, BAR_MASK_FULL + slot));
+  }
+}
+
 constexpr int kBarBoth = 3;  // named barrier of both softmax warpgroups
 
 template <int D, bool SOFTCAP, bool DROP>
@@ -838,9 +916,20 @@ __device__ void softmax_role_split(const Ctx& c, const Params& p, const Work& w,
     const int key0 = n0 + 64 * h;
     const uint32_t tS = tmem + lane_base + (t & 1) * 128;
     const uint32_t src = tS + 64 * h;
-    // the keep bits of this half's 64 keys, drawn while the S GEMM runs
-    const uint32_t kb0 = DROP ? keep_bits32(p, qrow, key0, bh) : 0xFFFFFFFFu;
-    const uint32_t kb1 = DROP ? keep_bits32(p, qrow, key0 + 32, bh) : 0xFFFFFFFFu;
+    // the keep bits of this half's 64 keys, drawn by the mask warpgroup
+    uint32_t kb0 = 0xFFFFFFFFu, kb1 = 0xFFFFFFFFu;
+    if (DROP) {
+      const int slot = t & 1;
+      if (wait(c, BAR_MASK_FULL + slot, (t >> 1) & 1)) {
+        const uint2 kb = reinterpret_cast<const uint2*>(smem + L::kMask)[slot * 256 + h * 128 + r];
+        kb0 = kb.x;
+        kb1 = kb.y;
+      } else {
+        ok = false;  // voted on at this block's barrier
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_addr(c, BAR_MASK_EMPTY + slot));
+    }
     // The scores are read from tensor memory once and kept in registers for
     // the maximum and P. The one barrier of both warpgroups per block carries
     // the half-row maxima and the abort decision (a wait that gave up, here
@@ -928,7 +1017,8 @@ __device__ void softmax_role_split(const Ctx& c, const Params& p, const Work& w,
   xsum[h * 128 + r] = l;
   if (!named_bar_and(kBarBoth, 256, ok)) return;
   tc_fence_after();
-  const float lt = xsum[r] + xsum[128 + r];
+  // with dropout the sums were of P / (1 - p)
+  const float lt = (xsum[r] + xsum[128 + r]) * (DROP ? p.drop.keep : 1.f);
   const float inv = lt > 0.f ? 1.f / lt : 0.f;
   const uint64_t inv2 = f2_make(inv, inv);
   // O / l of this half's columns -> bf16 rows in the Q buffer (free once the
@@ -967,7 +1057,7 @@ __device__ void softmax_role_split(const Ctx& c, const Params& p, const Work& w,
 
 // ------------------------------------------------------------------ kernel
 template <int D, bool SOFTCAP, bool DROP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsFor<D, DROP>, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
@@ -989,6 +1079,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_addr(c, BAR_P_FULL), 8);
       mbar_init(bar_addr(c, BAR_P_FULL + 1), 8);
     }
+    if (kMaskRole<D, DROP>) {
+      for (int sl = 0; sl < 2; ++sl) {
+        mbar_init(bar_addr(c, BAR_MASK_FULL + sl), kMaskWarps);
+        mbar_init(bar_addr(c, BAR_MASK_EMPTY + sl), 8);  // the softmax warps
+      }
+    }
     *c.abort = 0;
     fence_barrier_init();
   }
@@ -1001,23 +1097,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
   const Work w = work_of<D>(p);
-  if (warp == 0) {
-    if constexpr (kOneTile<D>)
-      loader_role_one<D>(c, w, sbase, &tm_q, &tm_k, false);
-    else
-      producer_role<D>(c, w, sbase, &tm_q, &tm_k, &tm_v);
-  } else if (warp == 1) {
-    if constexpr (kOneTile<D>)
-      mma_role_one<D>(c, w, sbase, tmem);
-    else
-      mma_role<D>(c, w, sbase, tmem);
-  } else if (warp == 2) {
-    if constexpr (kOneTile<D>) loader_role_one<D>(c, w, sbase, &tm_q, &tm_v, true);
-  } else if (warp >= 4) {
+  if (warp < 4) {
+    if constexpr (kMaskRole<D, DROP>) setmaxnreg_dec<kRegsOtherDrop>();
+    if (warp == 0) {
+      if constexpr (kOneTile<D>)
+        loader_role_one<D>(c, w, sbase, &tm_q, &tm_k, false);
+      else
+        producer_role<D>(c, w, sbase, &tm_q, &tm_k, &tm_v);
+    } else if (warp == 1) {
+      if constexpr (kOneTile<D>)
+        mma_role_one<D>(c, w, sbase, tmem);
+      else
+        mma_role<D>(c, w, sbase, tmem);
+    } else if (warp == 2) {
+      if constexpr (kOneTile<D>) loader_role_one<D>(c, w, sbase, &tm_q, &tm_v, true);
+    }
+  } else if (warp < 12) {
+    if constexpr (kMaskRole<D, DROP>) setmaxnreg_inc<kRegsSoftmaxDrop>();
     if constexpr (kOneTile<D>)
       softmax_role_split<D, SOFTCAP, DROP>(c, p, w, smem, sbase, tmem, &tm_o);
     else
       softmax_role<D, SOFTCAP, DROP>(c, p, w, sbase, tmem, &tm_o);
+  } else {
+    if constexpr (kMaskRole<D, DROP>) {
+      setmaxnreg_dec<kRegsOtherDrop>();
+      mask_role<D>(c, p, w, smem);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1035,7 +1140,8 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
   if (!set_smem_limit_once(kern, LayoutFor<D>::kBytes, configured)) return ATTN_ERR_LAUNCH;
   const long long grid = static_cast<long long>(p.pairs) * p.B * p.H;
   if (grid > 0x7fffffffLL) return ATTN_ERR_TOO_LARGE;
-  kern<<<static_cast<unsigned>(grid), kThreads, LayoutFor<D>::kBytes, stream>>>(tq, tk, tv, to, p);
+  kern<<<static_cast<unsigned>(grid), kThreadsFor<D, DROP>, LayoutFor<D>::kBytes, stream>>>(
+      tq, tk, tv, to, p);
   return launch_status();
 }
 
@@ -1112,6 +1218,9 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
   p.drop.seed_hi = static_cast<uint32_t>(seed >> 32);
   p.drop.threshold = dropout_threshold(p_drop);
   p.drop.inv_keep = 1.f / (1.f - p_drop);
+  p.drop.keep = 1.f - p_drop;
+  p.drop.log2_inv_keep =
+      static_cast<float>(-std::log2(1.0 - static_cast<double>(p_drop)));
   cudaStream_t s = as_stream(stream);
   return p_drop > 0.f ? dispatch<true>(tq, tk, tv, to, p, s, d, cap)
                       : dispatch<false>(tq, tk, tv, to, p, s, d, cap);

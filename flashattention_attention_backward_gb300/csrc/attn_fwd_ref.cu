@@ -292,6 +292,9 @@ int run(const void* q, const void* k, const void* v, void* o, float* lse, int B,
   p.drop.seed_hi = static_cast<uint32_t>(seed >> 32);
   p.drop.threshold = dropout_threshold(p_drop);
   p.drop.inv_keep = 1.f / (1.f - p_drop);
+  p.drop.keep = 1.f - p_drop;
+  p.drop.log2_inv_keep =
+      static_cast<float>(-std::log2(1.0 - static_cast<double>(p_drop)));
   cudaStream_t s = as_stream(stream);
   if (d == 256) return launch<256>(p, s);
   return d == 128 ? launch<128>(p, s) : launch<64>(p, s);

@@ -46,11 +46,40 @@ __device__ __forceinline__ PhiloxOut philox4x32_10(uint32_t c0, uint32_t c1, uin
   return o;
 }
 
+// NB independent calls of the same key in one pass: rounds outermost, so the
+// multiplies of different calls interleave (one call alone is a chain of ten
+// dependent rounds, and the multiply pipe is the bound). ctr[u] holds call
+// u's counter on entry and its four output words on return.
+template <int NB>
+__device__ __forceinline__ void philox4x32_10_batch(uint32_t (&ctr)[NB][4], uint32_t k0,
+                                                    uint32_t k1) {
+#pragma unroll
+  for (int rnd = 0; rnd < 10; ++rnd) {
+    if (rnd > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+#pragma unroll
+    for (int u = 0; u < NB; ++u) {
+      const uint32_t hi0 = __umulhi(0xD2511F53u, ctr[u][0]), lo0 = 0xD2511F53u * ctr[u][0];
+      const uint32_t hi1 = __umulhi(0xCD9E8D57u, ctr[u][2]), lo1 = 0xCD9E8D57u * ctr[u][2];
+      const uint32_t n0 = hi1 ^ ctr[u][1] ^ k0, n2 = hi0 ^ ctr[u][3] ^ k1;
+      ctr[u][0] = n0;
+      ctr[u][1] = lo1;
+      ctr[u][2] = n2;
+      ctr[u][3] = lo0;
+    }
+  }
+}
+
 // Dropout parameters shared by the kernels (p_drop > 0 enables it).
 struct Dropout {
   uint32_t seed_lo, seed_hi;
-  uint32_t threshold;  // keep iff word >= threshold
-  float inv_keep;      // 1 / (1 - p)
+  uint32_t threshold;   // keep iff word >= threshold
+  float inv_keep;       // 1 / (1 - p)
+  float keep;           // 1 - p
+  float log2_inv_keep;  // log2(1 / (1 - p)): the tensor-core forward adds it to
+                        // the exponent, so exp2 gives P / (1 - p) directly
 };
 
 }  // namespace attn
