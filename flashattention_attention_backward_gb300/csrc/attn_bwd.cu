@@ -1180,7 +1180,8 @@ int run(const void* q, const void* k, const void* v, const void* dO, const float
   cudaStream_t s = as_stream(stream);
   const bool cs = causal != 0;
   if (drop) return dispatch<false, true>(m, p, s, d, cs, cap);  // not combined with det
-  return det ? dispatch<true, false>(m, p, s, d, cs, cap) : dispatch<false, false>(m, p, s, d, cs, cap);
+  return det ? dispatch<true, false>(m, p, s, d, cs, cap)
+             : dispatch<false, false>(m, p, s, d, cs, cap);
 }
 
 }  // namespace bwd

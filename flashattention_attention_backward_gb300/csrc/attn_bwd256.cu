@@ -30,13 +30,15 @@
 // shared memory; Q and dO tiles (32 KB each) are single-buffered, which
 // leaves room for the dS tile and the dQ staging buffer within 227 KB.
 //
-// Warp roles (384 threads):
+// Warp roles (384 threads; 512 with dropout):
 //   warp 0      TMA producer: K, V once; per tile Q (+LSE, D) and dO
 //   warp 1      MMA issuer (whole warp, one elected lane), tensor-memory owner
 //   warps 4-7   softmax backward: thread = key row (tensor-memory lane),
 //               64 query columns
 //   warps 8-11  dQ drain (thread = d index of the half), then the dK/dV
 //               epilogue
+//   warps 12-15 with dropout only: the keep mask of the next tiles (thread =
+//               key row), handed to the softmax through shared memory
 //
 // Tensor memory (512 columns): S^T [0,64) (P^T bf16 pairs over its first 32
 // columns), dP^T [64,128), dQ^T tiles [128,192) and [192,256) alternating,
@@ -61,6 +63,16 @@ constexpr int kDh = 128;  // the half of d one CTA accumulates
 constexpr int kBc = 128;  // keys per CTA (tensor-memory lanes)
 constexpr int kBr = 64;   // queries per tile
 constexpr int kThreads = 384;
+// With dropout the keep mask is drawn by a warpgroup of its own: Philox4x32-10
+// is bound by its 32 x 32 -> 64-bit multiplies (about 1.3 calls per clock per
+// SM measured), and the 2,048 calls of a tile drawn by the four softmax warps
+// themselves (one per SM sub-partition, each call a chain of ten dependent
+// rounds) nearly doubled the tile's time. Registers: 512 threads launch with
+// 128 each; setmaxnreg gives the softmax and drain warps 168, the others 88.
+template <bool DROP>
+constexpr int kThreadsFor = DROP ? 512 : kThreads;
+constexpr int kRegsWideDrop = 168, kRegsNarrowDrop = 88;
+static_assert(256 * kRegsWideDrop + 256 * kRegsNarrowDrop <= 512 * 128, "register pool");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitLimitCycles = 2000000000LL;  // about one second
 
@@ -77,8 +89,11 @@ struct Layout {
   static constexpr int kDQS = 212992;   // dQ staging [32 queries][128 d] fp32, 16 KB
   static constexpr int kLSE = 229376;   // 64 fp32 (-LSE * log2e)
   static constexpr int kDsum = 229632;  // 64 fp32 (D)
-  static constexpr int kBars = 229888;
-  static constexpr int kNumBars = 18;
+  // dropout keep bits of two tiles: [tile parity][key row] x 2 words (bit j
+  // of word w: query 32 w + j of the tile)
+  static constexpr int kMask = 229888;
+  static constexpr int kBars = kMask + 2 * 128 * 8;
+  static constexpr int kNumBars = 22;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kBytes = kAbort + 12;
@@ -105,6 +120,8 @@ enum Bar {
   BAR_DRAIN = 15,     // abort path only
   BAR_QO_FULL = 16,
   BAR_QO_EMPTY = 17,
+  BAR_MASK_FULL = 18,   // + tile parity (dropout): keep bits written
+  BAR_MASK_EMPTY = 20,  // + tile parity: the softmax has read them
 };
 
 struct Params {
@@ -381,13 +398,13 @@ __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t t
 }
 
 // ------------------------------------------------------------------ softmax
-// With DROP, the keep bits of the thread's 64 query columns are drawn in the
-// P phase (one Philox call per four queries of its key) and kept in km[] for
-// the dS phase.
+// With DROP, km[] holds the keep bits of the thread's 64 query columns (bit
+// j of km[w]: query m0 + 32 w + j), drawn by the mask warps; both phases use
+// them.
 template <bool SOFTCAP, bool MASKED, bool DROP>
 __device__ __forceinline__ void softmax_tile(const Params& p, uint8_t* smem, uint32_t sbase,
                                              uint32_t tS, uint32_t tdP, int r, int key, int m0,
-                                             uint64_t (&pk)[32], uint32_t (&km)[2], uint32_t bh,
+                                             uint64_t (&pk)[32], const uint32_t (&km)[2],
                                              bool dp_phase) {
   using L = Layout;
   const float* s_lse = reinterpret_cast<const float*>(smem + L::kLSE);
@@ -403,19 +420,6 @@ __device__ __forceinline__ void softmax_tile(const Params& p, uint8_t* smem, uin
                    mtwo2 = f2_make(-2.f, -2.f);
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
-      if (DROP) {
-        uint32_t bits = 0;
-#pragma unroll
-        for (int g4 = 0; g4 < 8; ++g4) {  // queries m0 + 32 pass + 4 g4 .. + 3
-          const PhiloxOut rr = philox4x32_10(
-              static_cast<uint32_t>((m0 + 32 * pass + 4 * g4) >> 2), static_cast<uint32_t>(key),
-              bh, 0u, p.drop.seed_lo, p.drop.seed_hi);
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            bits |= (rr.w[e] >= p.drop.threshold ? 1u : 0u) << (4 * g4 + e);
-        }
-        km[pass] = bits;
-      }
       uint32_t raw[32];
       tmem_ld32(tS + 32 * pass, raw);
 #pragma unroll
@@ -520,17 +524,25 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8
     int h, m_block;
     tile_coord(w, t, h, m_block);
     const int m0 = m_block * kBr;
-    const uint32_t bh = static_cast<uint32_t>(w.b * p.H + h);
     const bool masked = tile_masked(p, m0, n0);
     const uint32_t ph = t & 1;
+    if (DROP) {  // this tile's keep bits, from the mask warps
+      if (!wait_warp(c, BAR_MASK_FULL + (t & 1), (t >> 1) & 1)) return;
+      const uint2 kb =
+          reinterpret_cast<const uint2*>(smem + Layout::kMask)[(t & 1) * 128 + r];
+      km[0] = kb.x;
+      km[1] = kb.y;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_addr(c, BAR_MASK_EMPTY + (t & 1)));
+    }
     // P phase: LSE and D of the tile arrive with QH_FULL
     if (!wait_warp(c, BAR_QH_FULL, ph)) return;
     if (!wait_warp(c, BAR_S_FULL, ph)) return;
     tc_fence_after();
     if (masked)
-      softmax_tile<SOFTCAP, true, DROP>(p, smem, sbase, tS, tdP, r, key, m0, pk, km, bh, false);
+      softmax_tile<SOFTCAP, true, DROP>(p, smem, sbase, tS, tdP, r, key, m0, pk, km, false);
     else
-      softmax_tile<SOFTCAP, false, DROP>(p, smem, sbase, tS, tdP, r, key, m0, pk, km, bh, false);
+      softmax_tile<SOFTCAP, false, DROP>(p, smem, sbase, tS, tdP, r, key, m0, pk, km, false);
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
@@ -540,13 +552,55 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint8
     if (t > 0 && !wait_warp(c, BAR_DS_FREE, (t - 1) & 1)) return;
     tc_fence_after();
     if (masked)
-      softmax_tile<SOFTCAP, true, DROP>(p, smem, sbase, tS, tdP, r, key, m0, pk, km, bh, true);
+      softmax_tile<SOFTCAP, true, DROP>(p, smem, sbase, tS, tdP, r, key, m0, pk, km, true);
     else
-      softmax_tile<SOFTCAP, false, DROP>(p, smem, sbase, tS, tdP, r, key, m0, pk, km, bh, true);
+      softmax_tile<SOFTCAP, false, DROP>(p, smem, sbase, tS, tdP, r, key, m0, pk, km, true);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_addr(c, BAR_DS_FULL));
+  }
+}
+
+// ------------------------------------------------------------------ keep mask (dropout)
+// Warps 12-15: thread r draws, for every tile of the unit, the 16 Philox calls
+// of key n0 + r (call g: queries m0 + 4 g .. m0 + 4 g + 3, one word each) and
+// writes its two 32-query words to slot t mod 2 once the softmax has read
+// tile t - 2 out of it.
+__device__ void mask_role(const Ctx& c, const Params& p, const Work& w, uint8_t* smem) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int r = ((warp & 3) << 5) + lane;
+  const uint32_t key = static_cast<uint32_t>(w.n_block * kBc + r);
+  uint32_t* mask = reinterpret_cast<uint32_t*>(smem + Layout::kMask);
+  for (int t = 0; t < w.T; ++t) {
+    const int slot = t & 1;
+    if (t >= 2 && !wait(c, BAR_MASK_EMPTY + slot, ((t >> 1) - 1) & 1)) return;
+    int h, m_block;
+    tile_coord(w, t, h, m_block);
+    const uint32_t qgrp = static_cast<uint32_t>(m_block * kBr) >> 2;
+    const uint32_t bh = static_cast<uint32_t>(w.b * p.H + h);
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {  // queries 32 half .. 32 half + 31
+      uint32_t ctr[8][4];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        ctr[g][0] = qgrp + static_cast<uint32_t>(8 * half + g);
+        ctr[g][1] = key;
+        ctr[g][2] = bh;
+        ctr[g][3] = 0u;
+      }
+      philox4x32_10_batch<8, 1>(ctr, p.drop.seed_lo, p.drop.seed_hi);
+      uint32_t bits = 0;
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          bits |= (ctr[g][e] >= p.drop.threshold ? 1u : 0u) << (4 * g + e);
+      mask[(slot * 128 + r) * 2 + half] = bits;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_addr(c, BAR_MASK_FULL + slot));
   }
 }
 
@@ -652,7 +706,7 @@ __device__ void drain_role(const Ctx& c, const Params& p, const Work& w, uint32_
 
 // ------------------------------------------------------------------ kernel
 template <bool SOFTCAP, bool DET, bool DROP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsFor<DROP>, 1)
     attn_bwd256_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
@@ -678,6 +732,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_addr(c, BAR_DS_FULL), 4);
     mbar_init(bar_addr(c, BAR_DQ_EMPTY), 4);  // the 4 drain warps
     mbar_init(bar_addr(c, BAR_DQ_EMPTY + 1), 4);
+    if (DROP) {
+      for (int sl = 0; sl < 2; ++sl) {
+        mbar_init(bar_addr(c, BAR_MASK_FULL + sl), 4);   // the mask warps
+        mbar_init(bar_addr(c, BAR_MASK_EMPTY + sl), 4);  // the softmax warps
+      }
+    }
     *c.abort = 0;
     fence_barrier_init();
   }
@@ -690,14 +750,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
   const Work w = work_of(p);
-  if (warp == 0) {
-    producer_role(c, p, w, smem, sbase, &tm_q, &tm_k, &tm_v, &tm_do);
-  } else if (warp == 1) {
-    mma_role(c, w, sbase, tmem);
-  } else if (warp >= 4 && warp < 8) {
+  if (warp < 4) {
+    if constexpr (DROP) setmaxnreg_dec<kRegsNarrowDrop>();
+    if (warp == 0)
+      producer_role(c, p, w, smem, sbase, &tm_q, &tm_k, &tm_v, &tm_do);
+    else if (warp == 1)
+      mma_role(c, w, sbase, tmem);
+  } else if (warp < 8) {
+    if constexpr (DROP) setmaxnreg_inc<kRegsWideDrop>();
     softmax_role<SOFTCAP, DROP>(c, p, w, smem, sbase, tmem);
-  } else if (warp >= 8) {
+  } else if (warp < 12) {
+    if constexpr (DROP) setmaxnreg_inc<kRegsWideDrop>();
     drain_role<DET>(c, p, w, sbase, tmem, &tm_dq, &tm_dk, &tm_dv);
+  } else {
+    if constexpr (DROP) {
+      setmaxnreg_dec<kRegsNarrowDrop>();
+      mask_role(c, p, w, smem);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -712,8 +781,8 @@ int launch(const CUtensorMap (&m)[7], const Params& p, long long grid, cudaStrea
   auto kern = attn_bwd256_kernel<SOFTCAP, DET, DROP>;
   static std::atomic<bool> configured[kMaxTrackedDevices];
   if (!set_smem_limit_once(kern, Layout::kBytes, configured)) return ATTN_ERR_LAUNCH;
-  kern<<<static_cast<unsigned>(grid), kThreads, Layout::kBytes, s>>>(m[0], m[1], m[2], m[3],
-                                                                       m[4], m[5], m[6], p);
+  kern<<<static_cast<unsigned>(grid), kThreadsFor<DROP>, Layout::kBytes, s>>>(
+      m[0], m[1], m[2], m[3], m[4], m[5], m[6], p);
   return launch_status();
 }
 
@@ -776,10 +845,13 @@ int bwd256_run(const void* q, const void* k, const void* v, const void* dO, cons
       !encode_bf16_3d(&m[5], dk, kD, N, hk, kBc) || !encode_bf16_3d(&m[6], dv, kD, N, hk, kBc))
     return ATTN_ERR_LAUNCH;
   if (p_drop > 0.f)  // not combined with det
-    return cap ? launch<true, false, true>(m, p, grid, s) : launch<false, false, true>(m, p, grid, s);
+    return cap ? launch<true, false, true>(m, p, grid, s)
+               : launch<false, false, true>(m, p, grid, s);
   if (det)
-    return cap ? launch<true, true, false>(m, p, grid, s) : launch<false, true, false>(m, p, grid, s);
-  return cap ? launch<true, false, false>(m, p, grid, s) : launch<false, false, false>(m, p, grid, s);
+    return cap ? launch<true, true, false>(m, p, grid, s)
+               : launch<false, true, false>(m, p, grid, s);
+  return cap ? launch<true, false, false>(m, p, grid, s)
+             : launch<false, false, false>(m, p, grid, s);
 }
 
 }  // namespace attn

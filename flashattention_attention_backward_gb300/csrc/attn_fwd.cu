@@ -869,7 +869,7 @@ __device__ void mask_role(const Ctx& c, const Params& p, const Work& w, uint8_t*
         ctr[u][2] = bh;
         ctr[u][3] = 0u;
       }
-      philox4x32_10_batch<kNB>(ctr, p.drop.seed_lo, p.drop.seed_hi);
+      philox4x32_10_batch<kNB, 10>(ctr, p.drop.seed_lo, p.drop.seed_hi);
 #pragma unroll
       for (int u = 0; u < kNB; ++u)
 #pragma unroll
@@ -909,7 +909,6 @@ __device__ void softmax_role_split(const Ctx& c, const Params& p, const Work& w,
   const int nt = w.nt[0];
   float m_used = -INFINITY, l = 0.f;
   bool ok = true;
-  const uint32_t bh = static_cast<uint32_t>(w.bh);
   const int m0 = w.m0[0];
   for (int t = 0; t < nt; ++t) {
     const int n0 = (w.j0[0] + t) * kBn;

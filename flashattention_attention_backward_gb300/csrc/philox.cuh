@@ -49,16 +49,16 @@ __device__ __forceinline__ PhiloxOut philox4x32_10(uint32_t c0, uint32_t c1, uin
 // NB independent calls of the same key in one pass: rounds outermost, so the
 // multiplies of different calls interleave (one call alone is a chain of ten
 // dependent rounds, and the multiply pipe is the bound). ctr[u] holds call
-// u's counter on entry and its four output words on return.
-template <int NB>
+// u's counter on entry and its four output words on return. UNROLL rounds
+// are unrolled: all ten suit a small batch, whose rounds are too short to
+// hide their own latency; a rolled loop suits a large batch in a kernel
+// whose other warps' loops need the instruction cache (fully unrolled, a
+// batch of eight would take much of it).
+template <int NB, int UNROLL>
 __device__ __forceinline__ void philox4x32_10_batch(uint32_t (&ctr)[NB][4], uint32_t k0,
                                                     uint32_t k1) {
-#pragma unroll
+#pragma unroll(UNROLL)
   for (int rnd = 0; rnd < 10; ++rnd) {
-    if (rnd > 0) {
-      k0 += 0x9E3779B9u;
-      k1 += 0xBB67AE85u;
-    }
 #pragma unroll
     for (int u = 0; u < NB; ++u) {
       const uint32_t hi0 = __umulhi(0xD2511F53u, ctr[u][0]), lo0 = 0xD2511F53u * ctr[u][0];
@@ -69,6 +69,8 @@ __device__ __forceinline__ void philox4x32_10_batch(uint32_t (&ctr)[NB][4], uint
       ctr[u][2] = n2;
       ctr[u][3] = lo0;
     }
+    k0 += 0x9E3779B9u;  // the key of the next round
+    k1 += 0xBB67AE85u;
   }
 }
 
