@@ -31,16 +31,22 @@
 // [256 + d, 256 + 2d).
 //
 // One-tile form (d = 128 and 256; two tiles' S and O would need 768 columns
-// at d = 256). One CTA owns one block of 128 queries. Its key blocks
-// alternate between two S buffers ([0,128) and [128,256)), so S(j + 1) runs
-// on the tensor cores while the softmax works on S(j); O sits at
-// [256, 256 + d). Both softmax warpgroups work on the one tile, warpgroup h
-// on keys 64 h .. 64 h + 63 of each block and on columns h d/2 .. of O; they
+// at d = 256). A tile is one block of 128 queries, and the CTAs are
+// persistent: one per SM, each walking its tiles in snake order. A tile's key
+// blocks alternate between two S buffers ([0,128) and [128,256)), so
+// S(j + 1) runs on the tensor cores while the softmax works on S(j); O sits
+// at [256, 256 + d), and at d = 128 the tiles alternate between two O
+// buffers ([256, 384) and [384, 512)). The next tile's Q (two Q stages at
+// d = 128), K and V blocks load while the current tile finishes, so the
+// launch, the first loads and the epilogue of a tile no longer stand alone.
+// Both softmax warpgroups work on the one tile, warpgroup h on keys
+// 64 h .. 64 h + 63 of each block and on columns h d/2 .. of O; they
 // exchange the half-row maxima through shared memory once per block.
-//   warp 0      Q once; K_j in a ring of 2 stages (d = 128) or 1 (d = 256)
+//   warp 0      Q of each tile; K_j in a ring of 2 stages (d = 128) or 1
 //   warp 2      V_j in the same kind of ring
-//   warp 1      MMA issuer: S(0), then per block S(j + 1), P(j) V
-//   warps 4-11  softmax, then the epilogue (each warpgroup its half of O)
+//   warp 1      MMA issuer: per tile S(0), then per block S(j + 1), P(j) V
+//   warps 4-11  softmax, then the tile's epilogue (each warpgroup its half of
+//               O, staged in the tile's Q stage)
 //   warps 12-19 with dropout only: the keep mask, one key block ahead
 // Every mbarrier wait is bounded, as in attn_bwd.
 #include <cstdint>
@@ -112,11 +118,18 @@ static_assert(256 * kRegsSoftmaxDrop + 384 * kRegsOtherDrop <= 640 * 96, "regist
 template <int D>
 struct LayoutOne {
   static constexpr int kTileBytes = 128 * D * 2;
-  // K and V stages: two where they fit (d <= 128), one at d = 256
+  // K and V stages: two where they fit (d <= 128), one at d = 256. Q stages
+  // likewise: the next tile's Q loads while the current one finishes, and a
+  // tile's Q stage stages its O for the TMA store at the end.
   static constexpr int kStages = D <= 128 ? 2 : 1;
+  static constexpr int kQStages = D <= 128 ? 2 : 1;
+  // O accumulators in tensor memory (after the two S buffers): two at
+  // d = 128, so a tile's P V GEMMs never wait for the previous tile's
+  // epilogue to read O; one at d = 256
+  static constexpr int kOBufs = D <= 128 ? 2 : 1;
   static constexpr int kQ0 = 0;
-  static constexpr int kQ1 = kQ0;  // a single tile
-  static constexpr int kK0 = kQ0 + kTileBytes;
+  static constexpr int kQ1 = kQ0 + (kQStages - 1) * kTileBytes;
+  static constexpr int kK0 = kQ1 + kTileBytes;
   static constexpr int kK1 = kK0 + (kStages - 1) * kTileBytes;
   static constexpr int kV0 = kK1 + kTileBytes;
   static constexpr int kV1 = kV0 + (kStages - 1) * kTileBytes;
@@ -127,13 +140,16 @@ struct LayoutOne {
   // 2 words (bit j of word w: key 64 half + 32 w + j of the block)
   static constexpr int kMask = kXchg + 6 * 128 * 4;
   static constexpr int kBars = kMask + 2 * 2048;
-  static constexpr int kNumBars = 21;
+  static constexpr int kNumBars = 25;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kUsed = kAbort + 12;
   static constexpr int kBytes = kUsed > 120 * 1024 ? kUsed : 120 * 1024;
 };
+static_assert(LayoutOne<128>::kBytes <= 232448, "shared memory budget");
 static_assert(LayoutOne<256>::kBytes <= 232448, "shared memory budget");
+static_assert(2 * 128 + LayoutOne<128>::kOBufs * 128 <= 512, "tensor memory");
+static_assert(2 * 128 + LayoutOne<256>::kOBufs * 256 <= 512, "tensor memory");
 
 template <int D>
 using LayoutFor = std::conditional_t<kOneTile<D>, LayoutOne<D>, Layout<D>>;
@@ -150,6 +166,8 @@ enum Bar {
   BAR_DRAIN = 16,    // abort path only: completion of everything issued
   BAR_MASK_FULL = 17,   // + block parity (one-tile form with dropout): keep bits written
   BAR_MASK_EMPTY = 19,  // + block parity: the softmax has read them
+  BAR_Q_EMPTY = 21,     // + Q stage (one-tile form): the tile's O store has read the stage
+  BAR_O_FREE = 23,      // + O buffer (one-tile form): the tile's epilogue has read O
 };
 
 struct Params {
@@ -249,6 +267,40 @@ __device__ __forceinline__ Work work_of(const Params& p) {
   w.jlo = w.j0[0];
   w.jhi = w.nt[1] > 0 ? w.j0[1] + w.nt[1] - 1 : w.j0[0] + w.nt[0] - 1;
   return w;
+}
+
+// The one-tile form is persistent: min(#SMs, tiles) CTAs, CTA c taking tile
+// index r * grid + c in even passes r and r * grid + (grid - 1 - c) in odd
+// ones (snake order over the tiles, heaviest first for a causal mask), so the
+// next tile's Q and first K, V blocks load and its first S GEMM runs while
+// the current tile finishes. Every per-block barrier keeps one phase per key
+// block across the CTA's tiles (global block index g), the per-tile ones one
+// phase per tile.
+struct TileOne {
+  int bh, kvh, m0, j0, nt;
+};
+
+__device__ __forceinline__ int cta_tile(int r, int n_tiles) {
+  const int grid = static_cast<int>(gridDim.x);
+  const int cta = static_cast<int>(blockIdx.x);
+  const int idx = r * grid + ((r & 1) ? grid - 1 - cta : cta);
+  return idx < n_tiles ? idx : -1;
+}
+
+// Tile idx: query block pair (heaviest first) of head bh.
+__device__ __forceinline__ TileOne tile_one(const Params& p, int idx) {
+  TileOne t;
+  const int heads = p.B * p.H;
+  const int blk = p.pairs - 1 - idx / heads;
+  t.bh = idx - (idx / heads) * heads;
+  const int b = t.bh / p.H, h = t.bh - b * p.H;
+  t.kvh = b * p.H_kv + h / (p.H / p.H_kv);
+  t.m0 = blk * kBm;
+  const int last_block = (p.N + kBn - 1) / kBn - 1;
+  t.j0 = max(0, t.m0 - p.win_left) / kBn;
+  const int j_end = min(last_block, (t.m0 + kBm - 1 + p.win_right) / kBn);
+  t.nt = j_end - t.j0 + 1;  // >= 1: the band holds the diagonal
+  return t;
 }
 
 // ------------------------------------------------------------------ producer
@@ -391,106 +443,130 @@ __device__ void mma_role(const Ctx& c, const Work& w, uint32_t sbase, uint32_t t
 
 // ------------------------------------------------------------------ one-tile roles
 // Loaders of the one-tile form. Warp 0 loads Q and the K blocks, warp 2 the
-// V blocks, each into its own ring of kStages stages: K(t) once S(t - kStages)
-// has read its stage, V(t) once P(t - kStages) V has. Each warp waits on its
-// own barriers in the order the tensor cores finish them, so no load waits
+// V blocks, each into its own ring of kStages stages: K(g) once S(g - kStages)
+// has read its stage, V(g) once P(g - kStages) V has, Q of tile i once the O
+// store of tile i - kQStages has read its stage. Each warp waits on its own
+// barriers in the order the tensor cores finish them, so no load waits
 // behind another operand's.
 template <int D>
-__device__ void loader_role_one(const Ctx& c, const Work& w, uint32_t sbase,
+__device__ void loader_role_one(const Ctx& c, const Params& p, uint32_t sbase,
                                 const CUtensorMap* tq, const CUtensorMap* tkv, bool is_v) {
   using L = LayoutOne<D>;
   constexpr int kBoxes = D / 64;
   constexpr uint32_t kTileBytes = L::kTileBytes;
-  constexpr int kS = L::kStages;
+  constexpr int kS = L::kStages, kQS = L::kQStages;
   const int lane = threadIdx.x & 31;
-  const int nt = w.nt[0];
+  const int n_tiles = p.pairs * p.B * p.H;
   if (lane == 0) {
     prefetch_tmap(tkv);
-    if (!is_v && nt > 0) {
-      prefetch_tmap(tq);
-      mbar_arrive_expect_tx(bar_addr(c, BAR_Q_FULL), kTileBytes);
-      for (int cb = 0; cb < kBoxes; ++cb)
-        tma_load_3d(sbase + L::kQ0 + cb * 16384, tq, bar_addr(c, BAR_Q_FULL), 64 * cb, w.m0[0],
-                    w.bh);
-    }
+    if (!is_v) prefetch_tmap(tq);
   }
   const uint64_t keep = policy_evict_last();  // K, V are read by every query block of the head
   const int bar_full = is_v ? BAR_V_FULL : BAR_K_FULL;
   const int bar_empty = is_v ? BAR_V_EMPTY : BAR_K_EMPTY;
   const uint32_t base = sbase + (is_v ? L::kV0 : L::kK0);
-  int issued = 0;
+  int g = 0, i = 0;  // blocks and tiles issued
   bool ok = true;
-  for (int t = 0; t < nt; ++t) {
-    const int st = t % kS;
-    if (t >= kS && !(ok = wait_warp(c, bar_empty + st, ((t / kS) - 1) & 1))) break;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar_addr(c, bar_full + st), kTileBytes);
-      for (int cb = 0; cb < kBoxes; ++cb)
-        tma_load_3d_hint(base + st * kTileBytes + cb * 16384, tkv, bar_addr(c, bar_full + st),
-                         64 * cb, (w.j0[0] + t) * kBn, w.kvh, keep);
+  for (int r = 0; ok; ++r, ++i) {
+    const int idx = cta_tile(r, n_tiles);
+    if (idx < 0) break;
+    const TileOne tl = tile_one(p, idx);
+    if (!is_v) {
+      const int qs = i % kQS;
+      if (i >= kQS && !(ok = wait_warp(c, BAR_Q_EMPTY + qs, ((i / kQS) - 1) & 1))) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar_addr(c, BAR_Q_FULL + qs), kTileBytes);
+        for (int cb = 0; cb < kBoxes; ++cb)
+          tma_load_3d(sbase + L::kQ0 + qs * kTileBytes + cb * 16384, tq,
+                      bar_addr(c, BAR_Q_FULL + qs), 64 * cb, tl.m0, tl.bh);
+      }
     }
-    issued = t + 1;
-    __syncwarp();
+    for (int t = 0; t < tl.nt; ++t, ++g) {
+      const int st = g % kS;
+      if (g >= kS && !(ok = wait_warp(c, bar_empty + st, ((g / kS) - 1) & 1))) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar_addr(c, bar_full + st), kTileBytes);
+        for (int cb = 0; cb < kBoxes; ++cb)
+          tma_load_3d_hint(base + st * kTileBytes + cb * 16384, tkv, bar_addr(c, bar_full + st),
+                           64 * cb, (tl.j0 + t) * kBn, tl.kvh, keep);
+      }
+      __syncwarp();
+    }
   }
-  // When aborting, the copies in flight must land before the CTA exits.
+  // When aborting, the copies in flight must land before the CTA exits: the
+  // last kStages blocks and the last kQStages Q tiles issued.
   if (!ok || *c.abort) {
-    if (!is_v && nt > 0) wait_drain(c, BAR_Q_FULL, 0);
-    for (int t = issued - kS < 0 ? 0 : issued - kS; t < issued; ++t)
-      wait_drain(c, bar_full + t % kS, (t / kS) & 1);
+    for (int gg = g - kS < 0 ? 0 : g - kS; gg < g; ++gg)
+      wait_drain(c, bar_full + gg % kS, (gg / kS) & 1);
+    if (!is_v)
+      for (int ii = i - kQS < 0 ? 0 : i - kQS; ii < i; ++ii)
+        wait_drain(c, BAR_Q_FULL + ii % kQS, (ii / kQS) & 1);
   }
 }
 
-// MMA issuer of the one-tile form: S(0); then per key block t, S(t + 1) into
-// the other S buffer (its P(t - 1) was read by P(t - 1) V, issued before),
-// then P(t) V once the softmax has written P(t).
+// MMA issuer of the one-tile form, per tile: S(0); then per key block t,
+// S(t + 1) into the other S buffer (its P(t - 1) was read by P(t - 1) V,
+// issued before), then P(t) V into the tile's O buffer once the softmax has
+// written P(t) (the first one once the epilogue of the tile kOBufs before has
+// read that buffer).
 template <int D>
-__device__ void mma_role_one(const Ctx& c, const Work& w, uint32_t sbase, uint32_t tmem) {
+__device__ void mma_role_one(const Ctx& c, const Params& p, uint32_t sbase, uint32_t tmem) {
   using L = LayoutOne<D>;
-  constexpr int kS = L::kStages;
+  constexpr int kS = L::kStages, kQS = L::kQStages, kOB = L::kOBufs;
   const bool leader = elect_one_sync() != 0;
   constexpr uint32_t kIdS = make_idesc_bf16(kBm, kBn, false, false);  // S = Q K^T
   constexpr uint32_t kIdO = make_idesc_bf16(kBm, D, false, true);     // O += P V
-  const uint32_t q_lo = sdesc_lo(sbase + L::kQ0, 16);
   const uint32_t k_lo[2] = {sdesc_lo(sbase + L::kK0, 16), sdesc_lo(sbase + L::kK1, 16)};
   const uint32_t v_mn[2] = {sdesc_lo(sbase + L::kV0, 16384), sdesc_lo(sbase + L::kV1, 16384)};
   auto kmaj = [](int k) { return static_cast<uint32_t>(((k >> 2) * 16384 + (k & 3) * 32) >> 4); };
   auto mnmaj = [](int k) { return static_cast<uint32_t>((2048 * k) >> 4); };
-  const int nt = w.nt[0];
+  const int n_tiles = p.pairs * p.B * p.H;
   bool ok = true;
-  auto issue_s = [&](int t) -> bool {
-    const int st = t % kS;
-    if (!wait_warp(c, BAR_K_FULL + st, (t / kS) & 1)) return false;
-    tc_fence_after();
-    if (leader) {
+  int g = 0;  // global index of the tile's first block
+  for (int r = 0, i = 0; ok; ++r, ++i) {
+    const int idx = cta_tile(r, n_tiles);
+    if (idx < 0) break;
+    const int nt = tile_one(p, idx).nt;
+    const int qs = i % kQS, ob = i % kOB;
+    const uint32_t q_lo = sdesc_lo(sbase + L::kQ0 + qs * L::kTileBytes, 16);
+    const uint32_t t_o = tmem + 256 + ob * D;
+    auto issue_s = [&](int gb) -> bool {
+      const int st = gb % kS;
+      if (!wait_warp(c, BAR_K_FULL + st, (gb / kS) & 1)) return false;
+      tc_fence_after();
+      if (leader) {
 #pragma unroll
-      for (int k = 0; k < D / 16; ++k)
-        mma_ss(tmem + (t & 1) * 128, sdesc_from_lo(q_lo + kmaj(k)),
-               sdesc_from_lo(k_lo[st] + kmaj(k)), kIdS, k > 0);
-      mma_commit(bar_addr(c, BAR_S_FULL + (t & 1)));
-      mma_commit(bar_addr(c, BAR_K_EMPTY + st));
-    }
-    return true;
-  };
-  if (nt > 0) {
-    ok = wait_warp(c, BAR_Q_FULL, 0);
-    if (ok) ok = issue_s(0);
-  }
-  for (int t = 0; ok && t < nt; ++t) {
-    if (t + 1 < nt && !(ok = issue_s(t + 1))) break;
-    if (!(ok = wait_warp(c, BAR_P_FULL + (t & 1), (t >> 1) & 1))) break;
-    const int vs = t % kS;
-    if (!(ok = wait_warp(c, BAR_V_FULL + vs, (t / kS) & 1))) break;
-    tc_fence_after();
-    if (leader) {
-      // A = P (bf16 pairs in the S buffer of block t: keys 0-63 in columns
-      // 0-31, keys 64-127 in columns 64-95, one half per softmax warpgroup)
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(tmem + (gb & 1) * 128, sdesc_from_lo(q_lo + kmaj(k)),
+                 sdesc_from_lo(k_lo[st] + kmaj(k)), kIdS, k > 0);
+        mma_commit(bar_addr(c, BAR_S_FULL + (gb & 1)));
+        mma_commit(bar_addr(c, BAR_K_EMPTY + st));
+      }
+      return true;
+    };
+    ok = wait_warp(c, BAR_Q_FULL + qs, (i / kQS) & 1);
+    if (ok) ok = issue_s(g);
+    for (int t = 0; ok && t < nt; ++t) {
+      const int gb = g + t;
+      if (t + 1 < nt && !(ok = issue_s(gb + 1))) break;
+      if (!(ok = wait_warp(c, BAR_P_FULL + (gb & 1), (gb >> 1) & 1))) break;
+      const int vs = gb % kS;
+      if (!(ok = wait_warp(c, BAR_V_FULL + vs, (gb / kS) & 1))) break;
+      if (t == 0 && i >= kOB && !(ok = wait_warp(c, BAR_O_FREE + ob, ((i / kOB) - 1) & 1)))
+        break;
+      tc_fence_after();
+      if (leader) {
+        // A = P (bf16 pairs in the S buffer of block gb: keys 0-63 in columns
+        // 0-31, keys 64-127 in columns 64-95, one half per softmax warpgroup)
 #pragma unroll
-      for (int k = 0; k < kBn / 16; ++k)
-        mma_ts(tmem + 256, tmem + (t & 1) * 128 + 8 * k + (k >= 4 ? 32 : 0),
-               sdesc_from_lo(v_mn[vs] + mnmaj(k)), kIdO, (t > 0 || k > 0) ? 1u : 0u);
-      mma_commit(bar_addr(c, BAR_O_DONE));
-      mma_commit(bar_addr(c, BAR_V_EMPTY + vs));
+        for (int k = 0; k < kBn / 16; ++k)
+          mma_ts(t_o, tmem + (gb & 1) * 128 + 8 * k + (k >= 4 ? 32 : 0),
+                 sdesc_from_lo(v_mn[vs] + mnmaj(k)), kIdO, (t > 0 || k > 0) ? 1u : 0u);
+        mma_commit(bar_addr(c, BAR_O_DONE));
+        mma_commit(bar_addr(c, BAR_V_EMPTY + vs));
+      }
     }
+    g += nt;
   }
   if (__any_sync(0xffffffffu, !ok || *c.abort != 0)) {
     // completion of everything issued before tensor memory is released
@@ -827,6 +903,63 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint3
         l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
 }
 
+// The keep mask of the one-tile form with dropout (warps 12-19, two per SM
+// sub-partition). For each key block of the CTA's tiles, warp 12 + w and lane
+// q draw the Philox calls of the query quad q (rows 4q .. 4q + 3, counter
+// word 0 = (m0 + 4q) / 4) and of the 16 keys 16 w .. 16 w + 15 of the block:
+// call g gives the four rows' words of key g, so the thread ends with 16 bits
+// of each of its four rows, half of a 32-key word. Block g (counted over
+// the CTA's tiles) goes to slot g mod 2 once the softmax has read block g - 2
+// out of it; the softmax reads block g's words while the one after is drawn.
+template <int D>
+__device__ void mask_role(const Ctx& c, const Params& p, uint8_t* smem) {
+  using L = LayoutOne<D>;
+  const int lane = threadIdx.x & 31;
+  const int mw = (static_cast<int>(threadIdx.x) >> 5) - 12;  // 16-key group of a block
+  uint16_t* mask = reinterpret_cast<uint16_t*>(smem + L::kMask);
+  const int n_tiles = p.pairs * p.B * p.H;
+  int g = 0;  // global block index
+  for (int r = 0;; ++r) {
+    const int idx = cta_tile(r, n_tiles);
+    if (idx < 0) return;
+    const TileOne tl = tile_one(p, idx);
+    const uint32_t qgrp = static_cast<uint32_t>(tl.m0 >> 2) + static_cast<uint32_t>(lane);
+    const uint32_t bh = static_cast<uint32_t>(tl.bh);
+    for (int t = 0; t < tl.nt; ++t, ++g) {
+      const int slot = g & 1;
+      if (g >= 2 && !wait(c, BAR_MASK_EMPTY + slot, ((g >> 1) - 1) & 1)) return;
+      const uint32_t k0 = static_cast<uint32_t>((tl.j0 + t) * kBn + 16 * mw);
+      uint32_t bits[4] = {0u, 0u, 0u, 0u};
+      constexpr int kNB = 4;  // calls in flight
+#pragma unroll 1
+      for (int g0 = 0; g0 < 16; g0 += kNB) {
+        uint32_t ctr[kNB][4];
+#pragma unroll
+        for (int u = 0; u < kNB; ++u) {
+          ctr[u][0] = qgrp;
+          ctr[u][1] = k0 + static_cast<uint32_t>(g0 + u);
+          ctr[u][2] = bh;
+          ctr[u][3] = 0u;
+        }
+        philox4x32_10_batch<kNB, 10>(ctr, p.drop.seed_lo, p.drop.seed_hi);
+#pragma unroll
+        for (int u = 0; u < kNB; ++u)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            bits[e] |= (ctr[u][e] >= p.drop.threshold ? 1u : 0u) << (g0 + u);
+      }
+      // row 4 lane + e: 32-key word mw / 2 (key half mw / 4, word (mw / 2)
+      // mod 2), 16-bit half mw mod 2
+      const int kg = mw >> 1;
+      uint16_t* dst = mask + slot * 1024 + ((kg >> 1) * 256 + (kg & 1)) * 2 + (mw & 1);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dst[(4 * lane + e) * 4] = static_cast<uint16_t>(bits[e]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_addr(c, BAR_MASK_FULL + slot));
+    }
+  }
+}
+
 // Softmax of the one-tile form: the two warpgroups share the tile, warpgroup
 // h taking keys 64 h .. 64 h + 63 of every key block (thread = query row r
 // in both). Per block they exchange the half-row maxima through shared
@@ -836,222 +969,188 @@ __device__ void softmax_role(const Ctx& c, const Params& p, const Work& w, uint3
 // O row. At the end the two row sums are added, and warpgroup h writes
 // columns h d/2 .. of O. Every decision is taken by both warpgroups together
 // (a 256-thread barrier with an AND), so an abort leaves none of them behind.
-// The keep mask of the one-tile form with dropout (warps 12-19, two per SM
-// sub-partition). For each key block of the CTA's tile, warp 12 + w and lane
-// q draw the Philox calls of the query quad q (rows 4q .. 4q + 3, counter
-// word 0 = (m0 + 4q) / 4) and of the 16 keys 16 w .. 16 w + 15 of the block:
-// call g gives the four rows' words of key g, so the thread ends with 16 bits
-// of each of its four rows, half of a 32-key word. Block j goes to slot
-// j mod 2 once the softmax has read block j - 2 out of it; the softmax reads
-// block j's words while the one after is drawn.
-template <int D>
-__device__ void mask_role(const Ctx& c, const Params& p, const Work& w, uint8_t* smem) {
-  using L = LayoutOne<D>;
-  const int lane = threadIdx.x & 31;
-  const int mw = (static_cast<int>(threadIdx.x) >> 5) - 12;  // 16-key group of a block
-  const uint32_t qgrp = static_cast<uint32_t>(w.m0[0] >> 2) + static_cast<uint32_t>(lane);
-  const uint32_t bh = static_cast<uint32_t>(w.bh);
-  uint16_t* mask = reinterpret_cast<uint16_t*>(smem + L::kMask);
-  const int nt = w.nt[0];
-  for (int t = 0; t < nt; ++t) {
-    const int slot = t & 1;
-    if (t >= 2 && !wait(c, BAR_MASK_EMPTY + slot, ((t >> 1) - 1) & 1)) return;
-    const uint32_t k0 = static_cast<uint32_t>((w.j0[0] + t) * kBn + 16 * mw);
-    uint32_t bits[4] = {0u, 0u, 0u, 0u};
-    constexpr int kNB = 4;  // calls in flight
-#pragma unroll 1
-    for (int g0 = 0; g0 < 16; g0 += kNB) {
-      uint32_t ctr[kNB][4];
-#pragma unroll
-      for (int u = 0; u < kNB; ++u) {
-        ctr[u][0] = qgrp;
-        ctr[u][1] = k0 + static_cast<uint32_t>(g0 + u);
-        ctr[u][2] = bh;
-        ctr[u][3] = 0u;
-      }
-      philox4x32_10_batch<kNB, 10>(ctr, p.drop.seed_lo, p.drop.seed_hi);
-#pragma unroll
-      for (int u = 0; u < kNB; ++u)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          bits[e] |= (ctr[u][e] >= p.drop.threshold ? 1u : 0u) << (g0 + u);
-    }
-    // row 4 lane + e: 32-key word mw / 4 (key half mw / 4, word (mw / 2) mod
-    // 2), 16-bit half mw mod 2
-    const int kg = mw >> 1;
-    uint16_t* dst = mask + slot * 1024 + ((kg >> 1) * 256 + (kg & 1)) * 2 + (mw & 1);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) dst[(4 * lane + e) * 4] = static_cast<uint16_t>(bits[e]);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar_addr(c, BAR_MASK_FULL + slot));
-  }
-}
-
 constexpr int kBarBoth = 3;  // named barrier of both softmax warpgroups
 
 template <int D, bool SOFTCAP, bool DROP>
-__device__ void softmax_role_split(const Ctx& c, const Params& p, const Work& w, uint8_t* smem,
-                                   uint32_t sbase, uint32_t tmem, const CUtensorMap* to) {
+__device__ void softmax_role_split(const Ctx& c, const Params& p, uint8_t* smem, uint32_t sbase,
+                                   uint32_t tmem, const CUtensorMap* to) {
   using L = LayoutOne<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int h = (warp - 4) >> 2;  // which half of the keys (and of O's columns)
   const int r = ((warp & 3) << 5) + lane;
   const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
-  const uint32_t tO = tmem + lane_base + 256 + h * (D / 2);
   float* xmax = reinterpret_cast<float*>(smem + L::kXchg);  // [block parity][half][row]
   float* xsum = xmax + 4 * 128;                              // [half][row]
-  const int qrow = w.m0[0] + r;
   const int bar_wg = 1 + h;
   const float c_log2 = p.scale * kLog2e;
   const float cap_in = SOFTCAP ? 2.f * kLog2e * p.scale / p.softcap : 0.f;  // 2 log2e tau/c
   const float cap_out = SOFTCAP ? p.softcap * kLog2e : 0.f;                 // c log2e
-  const int nt = w.nt[0];
-  float m_used = -INFINITY, l = 0.f;
+  const int n_tiles = p.pairs * p.B * p.H;
   bool ok = true;
-  const int m0 = w.m0[0];
-  for (int t = 0; t < nt; ++t) {
-    const int n0 = (w.j0[0] + t) * kBn;
-    const int key0 = n0 + 64 * h;
-    const uint32_t tS = tmem + lane_base + (t & 1) * 128;
-    const uint32_t src = tS + 64 * h;
-    // the keep bits of this half's 64 keys, drawn by the mask warpgroup
-    uint32_t kb0 = 0xFFFFFFFFu, kb1 = 0xFFFFFFFFu;
-    if (DROP) {
-      const int slot = t & 1;
-      if (wait(c, BAR_MASK_FULL + slot, (t >> 1) & 1)) {
-        const uint2 kb = reinterpret_cast<const uint2*>(smem + L::kMask)[slot * 256 + h * 128 + r];
-        kb0 = kb.x;
-        kb1 = kb.y;
-      } else {
-        ok = false;  // voted on at this block's barrier
+  int g = 0;  // global index of the tile's first key block
+  for (int rr = 0, i = 0; ok; ++rr, ++i) {
+    const int idx = cta_tile(rr, n_tiles);
+    if (idx < 0) break;
+    const TileOne tl = tile_one(p, idx);
+    const int nt = tl.nt, m0 = tl.m0, qrow = m0 + r;
+    const int qs = i % L::kQStages, ob = i % L::kOBufs;
+    const uint32_t tO = tmem + lane_base + 256 + ob * D + h * (D / 2);
+    float m_used = -INFINITY, l = 0.f;
+    for (int t = 0; t < nt; ++t) {
+      const int gb = g + t;  // this block over the CTA's tiles
+      const int n0 = (tl.j0 + t) * kBn;
+      const int key0 = n0 + 64 * h;
+      const uint32_t tS = tmem + lane_base + (gb & 1) * 128;
+      const uint32_t src = tS + 64 * h;
+      // the keep bits of this half's 64 keys, drawn by the mask warpgroup
+      uint32_t kb0 = 0xFFFFFFFFu, kb1 = 0xFFFFFFFFu;
+      if (DROP) {
+        const int slot = gb & 1;
+        if (wait(c, BAR_MASK_FULL + slot, (gb >> 1) & 1)) {
+          const uint2 kb =
+              reinterpret_cast<const uint2*>(smem + L::kMask)[slot * 256 + h * 128 + r];
+          kb0 = kb.x;
+          kb1 = kb.y;
+        } else {
+          ok = false;  // voted on at this block's barrier
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_addr(c, BAR_MASK_EMPTY + slot));
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(c, BAR_MASK_EMPTY + slot));
-    }
-    // The scores are read from tensor memory once and kept in registers for
-    // the maximum and P. The one barrier of both warpgroups per block carries
-    // the half-row maxima and the abort decision (a wait that gave up, here
-    // or at the previous block's O rescale).
-    const bool got = wait(c, BAR_S_FULL + (t & 1), (t >> 1) & 1);
-    uint32_t raw[64];
-    if (got) {
-      tc_fence_after();
-      tmem_ld32x2(src, src + 32, raw);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 64; ++e) raw[e] = 0u;
-    }
-    const bool masked =
-        n0 + kBn - 1 - m0 > p.win_right || m0 + kBm - 1 - n0 > p.win_left || n0 + kBn > p.N;
-    const float hmax = masked ? chunk_max_regs<true>(p, raw, key0, qrow)
-                              : chunk_max_regs<false>(p, raw, key0, qrow);
-    float* slot = xmax + (t & 1) * 256;
-    slot[h * 128 + r] = hmax;
-    ok = named_bar_and(kBarBoth, 256, ok && got);
-    if (!ok) break;
-    const float smax = fmaxf(hmax, slot[(1 - h) * 128 + r]);
-    float m_tile = -INFINITY;  // row maximum of x = logit * log2e over this block
-    if (smax > -INFINITY) {
-      if (SOFTCAP) {
-        const float ex = ex2_approx(smax * cap_in);
-        m_tile = (1.f - 2.f * rcp_approx(ex + 1.f)) * cap_out;
+      // The scores are read from tensor memory once and kept in registers for
+      // the maximum and P. The one barrier of both warpgroups per block carries
+      // the half-row maxima and the abort decision (a wait that gave up, here
+      // or at the previous block's O rescale).
+      const bool got = wait(c, BAR_S_FULL + (gb & 1), (gb >> 1) & 1);
+      uint32_t raw[64];
+      if (got) {
+        tc_fence_after();
+        tmem_ld32x2(src, src + 32, raw);
       } else {
-        m_tile = smax * c_log2;
+  #pragma unroll
+        for (int e = 0; e < 64; ++e) raw[e] = 0u;
       }
-    }
-    // move the shift when the maximum outgrows it by more than kRescale (the
-    // same decision in both warpgroups: they see the same maxima)
-    const bool need = m_tile > m_used + kRescale;
-    if (__any_sync(0xffffffffu, need)) {
-      const float m_new = need ? m_tile : m_used;
-      const float f = need ? ex2_approx(m_used - m_new) : 1.f;  // 0 while m_used = -inf
-      // this half of the O row, once P(t - 1) V has completed; a wait that
-      // gives up is voted on at the next barrier
-      if (__any_sync(0xffffffffu, need && m_used > -INFINITY) && t > 0) {
-        if (!wait_warp(c, BAR_O_DONE, (t - 1) & 1)) ok = false;
-        if (ok) {
-          tc_fence_after();
-          const uint64_t f2 = f2_make(f, f);
-#pragma unroll
-          for (int c32 = 0; c32 < D / 64; ++c32) {
-            uint32_t o[32];
-            tmem_ld32(tO + c32 * 32, o);
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              const uint64_t v = f2_mul(f2_make(o[2 * u], o[2 * u + 1]), f2);
-              o[2 * u] = static_cast<uint32_t>(v);
-              o[2 * u + 1] = static_cast<uint32_t>(v >> 32);
-            }
-            uint32_t lo[16], hi[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              lo[u] = o[u];
-              hi[u] = o[16 + u];
-            }
-            tmem_st16(tO + c32 * 32, lo);
-            tmem_st16(tO + c32 * 32 + 16, hi);
-          }
+      const bool masked =
+          n0 + kBn - 1 - m0 > p.win_right || m0 + kBm - 1 - n0 > p.win_left || n0 + kBn > p.N;
+      const float hmax = masked ? chunk_max_regs<true>(p, raw, key0, qrow)
+                                : chunk_max_regs<false>(p, raw, key0, qrow);
+      float* slot = xmax + (gb & 1) * 256;
+      slot[h * 128 + r] = hmax;
+      ok = named_bar_and(kBarBoth, 256, ok && got);
+      if (!ok) break;
+      const float smax = fmaxf(hmax, slot[(1 - h) * 128 + r]);
+      float m_tile = -INFINITY;  // row maximum of x = logit * log2e over this block
+      if (smax > -INFINITY) {
+        if (SOFTCAP) {
+          const float ex = ex2_approx(smax * cap_in);
+          m_tile = (1.f - 2.f * rcp_approx(ex + 1.f)) * cap_out;
+        } else {
+          m_tile = smax * c_log2;
         }
       }
-      l *= f;
-      m_used = m_new;
+      // move the shift when the maximum outgrows it by more than kRescale (the
+      // same decision in both warpgroups: they see the same maxima)
+      const bool need = m_tile > m_used + kRescale;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? m_tile : m_used;
+        const float f = need ? ex2_approx(m_used - m_new) : 1.f;  // 0 while m_used = -inf
+        // this half of the O row, once P(t - 1) V has completed; a wait that
+        // gives up is voted on at the next barrier
+        if (__any_sync(0xffffffffu, need && m_used > -INFINITY) && t > 0) {
+          if (!wait_warp(c, BAR_O_DONE, (gb - 1) & 1)) ok = false;
+          if (ok) {
+            tc_fence_after();
+            const uint64_t f2 = f2_make(f, f);
+  #pragma unroll
+            for (int c32 = 0; c32 < D / 64; ++c32) {
+              uint32_t o[32];
+              tmem_ld32(tO + c32 * 32, o);
+  #pragma unroll
+              for (int u = 0; u < 16; ++u) {
+                const uint64_t v = f2_mul(f2_make(o[2 * u], o[2 * u + 1]), f2);
+                o[2 * u] = static_cast<uint32_t>(v);
+                o[2 * u + 1] = static_cast<uint32_t>(v >> 32);
+              }
+              uint32_t lo[16], hi[16];
+  #pragma unroll
+              for (int u = 0; u < 16; ++u) {
+                lo[u] = o[u];
+                hi[u] = o[16 + u];
+              }
+              tmem_st16(tO + c32 * 32, lo);
+              tmem_st16(tO + c32 * 32 + 16, hi);
+            }
+          }
+        }
+        l *= f;
+        m_used = m_new;
+      }
+      const float shift = m_used > -INFINITY ? m_used : 0.f;
+      const uint32_t dst = tS + 64 * h;  // keys 0-63 -> columns 0-31, 64-127 -> 64-95
+      l += masked ? chunk_p_regs<SOFTCAP, true, DROP>(p, raw, dst, key0, qrow, c_log2, cap_in,
+                                                      cap_out, shift, kb0, kb1)
+                  : chunk_p_regs<SOFTCAP, false, DROP>(p, raw, dst, key0, qrow, c_log2, cap_in,
+                                                       cap_out, shift, kb0, kb1);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_addr(c, BAR_P_FULL + (gb & 1)));  // one arrival per warp
     }
-    const float shift = m_used > -INFINITY ? m_used : 0.f;
-    const uint32_t dst = tS + 64 * h;  // keys 0-63 -> columns 0-31, 64-127 -> 64-95
-    l += masked ? chunk_p_regs<SOFTCAP, true, DROP>(p, raw, dst, key0, qrow, c_log2, cap_in,
-                                                    cap_out, shift, kb0, kb1)
-                : chunk_p_regs<SOFTCAP, false, DROP>(p, raw, dst, key0, qrow, c_log2, cap_in,
-                                                     cap_out, shift, kb0, kb1);
-    tmem_wait_st();
+    // ---- epilogue. S(j + 1) is issued before P(j) V, so P(nt - 2) V may still
+    // run: its phase of O_DONE completes first (a wait on the parity of the
+    // last phase alone would pass while the one before it is still open).
+    if (ok && nt >= 2) ok = wait(c, BAR_O_DONE, (g + nt - 2) & 1);
+    if (ok) ok = wait(c, BAR_O_DONE, (g + nt - 1) & 1);
+    xsum[h * 128 + r] = l;
+    if (!named_bar_and(kBarBoth, 256, ok)) break;
+    tc_fence_after();
+    // with dropout the sums were of P / (1 - p)
+    const float lt = (xsum[r] + xsum[128 + r]) * (DROP ? p.drop.keep : 1.f);
+    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+    const uint64_t inv2 = f2_make(inv, inv);
+    // O / l of this half's columns -> bf16 rows in the tile's Q stage (free
+    // once the last S GEMM is done, which precedes the last P V) -> TMA tensor
+    // stores; O_FREE once tensor memory is read, Q_EMPTY once the stores have
+    // read the stage
+    const uint32_t buf = sbase + L::kQ0 + qs * L::kTileBytes;
+  #pragma unroll
+    for (int c16 = 0; c16 < D / 32; ++c16) {
+      const int col = h * (D / 2) + c16 * 16;  // column of O
+      uint32_t raw[16];
+      tmem_ld16(tO + c16 * 16, raw);
+      uint32_t packed[8];
+  #pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint64_t v = f2_mul(f2_make(raw[2 * u], raw[2 * u + 1]), inv2);
+        packed[u] = pack_bf16x2(f2_lo(v), f2_hi(v));
+      }
+      // columns col .. col + 15: box col / 64, 16-byte chunks (col % 64) / 8, + 1
+      const uint32_t row_addr = buf + (col >> 6) * 16384 + r * 128;
+      const int c0 = (col & 63) >> 3;
+      st_shared_v4(row_addr + ((c0 ^ (r & 7)) << 4), packed[0], packed[1], packed[2], packed[3]);
+      st_shared_v4(row_addr + (((c0 + 1) ^ (r & 7)) << 4), packed[4], packed[5], packed[6],
+                   packed[7]);
+    }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(bar_addr(c, BAR_P_FULL + (t & 1)));  // one arrival per warp
-  }
-  // ---- epilogue. S(j + 1) is issued before P(j) V, so P(nt - 2) V may still
-  // run: its phase of O_DONE completes first (a wait on the parity of the
-  // last phase alone would pass while the one before it is still open).
-  if (ok && nt >= 2) ok = wait(c, BAR_O_DONE, (nt - 2) & 1);
-  if (ok) ok = wait(c, BAR_O_DONE, (nt - 1) & 1);
-  xsum[h * 128 + r] = l;
-  if (!named_bar_and(kBarBoth, 256, ok)) return;
-  tc_fence_after();
-  // with dropout the sums were of P / (1 - p)
-  const float lt = (xsum[r] + xsum[128 + r]) * (DROP ? p.drop.keep : 1.f);
-  const float inv = lt > 0.f ? 1.f / lt : 0.f;
-  const uint64_t inv2 = f2_make(inv, inv);
-  // O / l of this half's columns -> bf16 rows in the Q buffer (free once the
-  // last S GEMM is done, which precedes the last P V) -> TMA tensor stores
-  const uint32_t buf = sbase + L::kQ0;
-#pragma unroll
-  for (int c16 = 0; c16 < D / 32; ++c16) {
-    const int col = h * (D / 2) + c16 * 16;  // column of O
-    uint32_t raw[16];
-    tmem_ld16(tO + c16 * 16, raw);
-    uint32_t packed[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const uint64_t v = f2_mul(f2_make(raw[2 * u], raw[2 * u + 1]), inv2);
-      packed[u] = pack_bf16x2(f2_lo(v), f2_hi(v));
+    if (lane == 0) mbar_arrive(bar_addr(c, BAR_O_FREE + ob));
+    fence_proxy_async_smem();
+    named_bar_sync(bar_wg, 128);
+    if (r == 0) {
+      for (int cb = h * (D / 128); cb < (h + 1) * (D / 128); ++cb)
+        tma_store_3d(to, buf + cb * 16384, 64 * cb, m0, tl.bh);
+      bulk_commit_group();
+      bulk_wait_read_all();
+      mbar_arrive(bar_addr(c, BAR_Q_EMPTY + qs));
     }
-    // columns col .. col + 15: box col / 64, 16-byte chunks (col % 64) / 8, + 1
-    const uint32_t row_addr = buf + (col >> 6) * 16384 + r * 128;
-    const int c0 = (col & 63) >> 3;
-    st_shared_v4(row_addr + ((c0 ^ (r & 7)) << 4), packed[0], packed[1], packed[2], packed[3]);
-    st_shared_v4(row_addr + (((c0 + 1) ^ (r & 7)) << 4), packed[4], packed[5], packed[6],
-                 packed[7]);
+    if (h == 0 && qrow < p.N)
+      p.lse[static_cast<long long>(tl.bh) * p.N + qrow] =
+          lt > 0.f ? (m_used + __log2f(lt)) * kLn2 : -INFINITY;
+    g += nt;
   }
-  fence_proxy_async_smem();
-  named_bar_sync(bar_wg, 128);
-  if (r == 0) {
-    for (int cb = h * (D / 128); cb < (h + 1) * (D / 128); ++cb)
-      tma_store_3d(to, buf + cb * 16384, 64 * cb, m0, w.bh);
-    bulk_commit_group();
-    bulk_wait_all();
-  }
-  if (h == 0 && qrow < p.N)
-    p.lse[static_cast<long long>(w.bh) * p.N + qrow] =
-        lt > 0.f ? (m_used + __log2f(lt)) * kLn2 : -INFINITY;
+  // the O stores complete before the CTA exits
+  if (r == 0) bulk_wait_all();
 }
 
 // ------------------------------------------------------------------ kernel
@@ -1078,6 +1177,12 @@ __global__ void __launch_bounds__(kThreadsFor<D, DROP>, 1)
       mbar_init(bar_addr(c, BAR_P_FULL), 8);
       mbar_init(bar_addr(c, BAR_P_FULL + 1), 8);
     }
+    if (kOneTile<D>) {
+      for (int sl = 0; sl < 2; ++sl) {
+        mbar_init(bar_addr(c, BAR_Q_EMPTY + sl), 2);  // the two O-storing threads
+        mbar_init(bar_addr(c, BAR_O_FREE + sl), 8);   // the softmax warps
+      }
+    }
     if (kMaskRole<D, DROP>) {
       for (int sl = 0; sl < 2; ++sl) {
         mbar_init(bar_addr(c, BAR_MASK_FULL + sl), kMaskWarps);
@@ -1100,27 +1205,27 @@ __global__ void __launch_bounds__(kThreadsFor<D, DROP>, 1)
     if constexpr (kMaskRole<D, DROP>) setmaxnreg_dec<kRegsOtherDrop>();
     if (warp == 0) {
       if constexpr (kOneTile<D>)
-        loader_role_one<D>(c, w, sbase, &tm_q, &tm_k, false);
+        loader_role_one<D>(c, p, sbase, &tm_q, &tm_k, false);
       else
         producer_role<D>(c, w, sbase, &tm_q, &tm_k, &tm_v);
     } else if (warp == 1) {
       if constexpr (kOneTile<D>)
-        mma_role_one<D>(c, w, sbase, tmem);
+        mma_role_one<D>(c, p, sbase, tmem);
       else
         mma_role<D>(c, w, sbase, tmem);
     } else if (warp == 2) {
-      if constexpr (kOneTile<D>) loader_role_one<D>(c, w, sbase, &tm_q, &tm_v, true);
+      if constexpr (kOneTile<D>) loader_role_one<D>(c, p, sbase, &tm_q, &tm_v, true);
     }
   } else if (warp < 12) {
     if constexpr (kMaskRole<D, DROP>) setmaxnreg_inc<kRegsSoftmaxDrop>();
     if constexpr (kOneTile<D>)
-      softmax_role_split<D, SOFTCAP, DROP>(c, p, w, smem, sbase, tmem, &tm_o);
+      softmax_role_split<D, SOFTCAP, DROP>(c, p, smem, sbase, tmem, &tm_o);
     else
       softmax_role<D, SOFTCAP, DROP>(c, p, w, sbase, tmem, &tm_o);
   } else {
     if constexpr (kMaskRole<D, DROP>) {
       setmaxnreg_dec<kRegsOtherDrop>();
-      mask_role<D>(c, p, w, smem);
+      mask_role<D>(c, p, smem);
     }
   }
   tc_fence_before();
@@ -1137,8 +1242,13 @@ int launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
   auto kern = attn_fwd_kernel<D, SOFTCAP, DROP>;
   static std::atomic<bool> configured[kMaxTrackedDevices];
   if (!set_smem_limit_once(kern, LayoutFor<D>::kBytes, configured)) return ATTN_ERR_LAUNCH;
-  const long long grid = static_cast<long long>(p.pairs) * p.B * p.H;
+  long long grid = static_cast<long long>(p.pairs) * p.B * p.H;
   if (grid > 0x7fffffffLL) return ATTN_ERR_TOO_LARGE;
+  if (kOneTile<D>) {  // persistent: one CTA per SM (or per tile, if fewer)
+    const int sms = sm_count();
+    if (sms <= 0) return ATTN_ERR_LAUNCH;
+    if (grid > sms) grid = sms;
+  }
   kern<<<static_cast<unsigned>(grid), kThreadsFor<D, DROP>, LayoutFor<D>::kBytes, stream>>>(
       tq, tk, tv, to, p);
   return launch_status();
