@@ -468,6 +468,10 @@ def d256_timing(dev, peak, iters, warmup):
     x = make_inputs(w)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
     o, lse = runner.forward(q, k, v, w.scale, True)
+    torch.cuda.synchronize(dev)
+    rc, status = attn.attn_device_status(clear=True, stream=stream)
+    if rc != 0 or status != 0:
+        raise RuntimeError("device status %d after the d = 256 forward" % status)
     bufs = runner.BackwardBuffers(q, k)
     ts = []
     for i in range(warmup + iters):

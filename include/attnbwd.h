@@ -119,11 +119,11 @@ int attn_fwd_dropout(const void* q, const void* k, const void* v, void* o, float
  * statistics): a CTA walks the visible key blocks of its queries once; O
  * accumulates un-normalised in fp32 tensor memory, rescaled only when a row
  * maximum grows by more than 2^8, and is divided by the row sum at the end.
- * P enters the PV GEMM as bf16. d = 64: a CTA takes two blocks of 128
- * queries that ping-pong on the tensor cores; d = 128 and 256: one block of
- * 128 queries, its key blocks alternating between two S buffers and its
- * keys split between two softmax warpgroups. scale must be > 0
- * (ATTN_ERR_SHAPE otherwise).
+ * P enters the PV GEMM as bf16. One CTA per SM walks blocks of 128 queries
+ * (persistent, heaviest first); a block's key blocks alternate between two S
+ * buffers and its keys are split between two softmax warpgroups, and the
+ * next block's loads overlap the current one's last GEMMs and epilogue.
+ * scale must be > 0 (ATTN_ERR_SHAPE otherwise).
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
              int H_kv, int N, int d, float scale, int causal, float softcap, void* stream);
