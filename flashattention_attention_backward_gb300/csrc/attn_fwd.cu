@@ -70,6 +70,13 @@ constexpr int kThreadsFor = DROP ? 640 : kThreads;
 constexpr int kMaskWarps = 8;  // two per SM sub-partition
 constexpr int kRegsSoftmaxDrop = 128, kRegsOtherDrop = 72;
 static_assert(256 * kRegsSoftmaxDrop + 384 * kRegsOtherDrop <= 640 * 96, "register pool");
+// Without dropout at d = 256 (384 threads launched at 168 registers), the
+// softmax warps' state does not fit in 168: setmaxnreg moves registers to
+// them from the loaders and the MMA warp.
+constexpr int kRegsSoftmax256 = 200, kRegsCtl256 = 56;
+static_assert(256 * kRegsSoftmax256 + 128 * kRegsCtl256 <= 384 * 168, "register pool");
+template <int D, bool DROP>
+constexpr bool kSplitRegs256 = D == 256 && !DROP;
 
 template <int D>
 struct Layout {
@@ -750,6 +757,7 @@ __global__ void __launch_bounds__(kThreadsFor<DROP>, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
   if (warp < 4) {
     if constexpr (DROP) setmaxnreg_dec<kRegsOtherDrop>();
+    if constexpr (kSplitRegs256<D, DROP>) setmaxnreg_dec<kRegsCtl256>();
     if (warp == 0)
       loader_role<D>(c, p, sbase, &tm_q, &tm_k, false);
     else if (warp == 1)
@@ -758,6 +766,7 @@ __global__ void __launch_bounds__(kThreadsFor<DROP>, 1)
       loader_role<D>(c, p, sbase, &tm_q, &tm_v, true);
   } else if (warp < 12) {
     if constexpr (DROP) setmaxnreg_inc<kRegsSoftmaxDrop>();
+    if constexpr (kSplitRegs256<D, DROP>) setmaxnreg_inc<kRegsSoftmax256>();
     softmax_role<D, SOFTCAP, DROP>(c, p, smem, sbase, tmem, &tm_o);
   } else {
     if constexpr (DROP) {
