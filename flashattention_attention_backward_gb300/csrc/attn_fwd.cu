@@ -542,6 +542,7 @@ __device__ void softmax_role(const Ctx& c, const Params& p, uint8_t* smem, uint3
   const int n_tiles = p.tiles * p.B * p.H;
   bool ok = true;
   int g = 0;  // global index of the tile's first key block
+  int q_empty_pending = 0;  // Q stage + 1 whose O stores this thread has yet to hand back
   for (int rr = 0, i = 0; ok; ++rr, ++i) {
     const int idx = cta_tile(rr, n_tiles);
     if (idx < 0) break;
@@ -649,6 +650,14 @@ __device__ void softmax_role(const Ctx& c, const Params& p, uint8_t* smem, uint3
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_addr(c, BAR_P_FULL + (gb & 1)));  // one arrival per warp
+      // The previous tile's O stores have long read their Q stage: hand it
+      // back now (the loader needs it two tiles on), not at the end of that
+      // tile's epilogue, where the wait held this warp back.
+      if (q_empty_pending) {
+        bulk_wait_read_all();
+        mbar_arrive(bar_addr(c, BAR_Q_EMPTY + q_empty_pending - 1));
+        q_empty_pending = 0;
+      }
     }
     // ---- epilogue, once the tile's last P V has completed. Its own barrier
     // (one phase per tile) is waited on, not O_DONE: by the time the softmax
@@ -703,8 +712,12 @@ __device__ void softmax_role(const Ctx& c, const Params& p, uint8_t* smem, uint3
       for (int cb = h * kBoxesWg; cb < (h + 1) * kBoxesWg; ++cb)
         tma_store_3d(to, buf + cb * 16384, 64 * cb, m0, tl.bh);
       bulk_commit_group();
-      bulk_wait_read_all();
-      mbar_arrive(bar_addr(c, BAR_Q_EMPTY + qs));
+      if (L::kQStages >= 2) {
+        q_empty_pending = qs + 1;  // handed back after the next tile's first block
+      } else {
+        bulk_wait_read_all();
+        mbar_arrive(bar_addr(c, BAR_Q_EMPTY + qs));
+      }
     }
     if (h == 0 && qrow < p.N)
       p.lse[static_cast<long long>(tl.bh) * p.N + qrow] =
@@ -712,6 +725,7 @@ __device__ void softmax_role(const Ctx& c, const Params& p, uint8_t* smem, uint3
     g += nt;
   }
   // the O stores complete before the CTA exits
+  if (q_empty_pending) mbar_arrive(bar_addr(c, BAR_Q_EMPTY + q_empty_pending - 1));
   if (r == 0) bulk_wait_all();
 }
 
