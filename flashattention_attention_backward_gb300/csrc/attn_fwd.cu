@@ -483,7 +483,7 @@ __device__ void mask_role(const Ctx& c, const Params& p, uint8_t* smem) {
       if (g >= 2 && !wait(c, BAR_MASK_EMPTY + slot, ((g >> 1) - 1) & 1)) return;
       const uint32_t k0 = static_cast<uint32_t>((tl.j0 + t) * kBn + 16 * mw);
       uint32_t bits[4] = {0u, 0u, 0u, 0u};
-      constexpr int kNB = 4;  // calls in flight
+      constexpr int kNB = 8;  // calls in flight
 #pragma unroll 1
       for (int g0 = 0; g0 < 16; g0 += kNB) {
         uint32_t ctr[kNB][4];
