@@ -380,6 +380,20 @@ __device__ __forceinline__ float chunk_max_regs(const Params& p, const uint32_t 
   return fmaxf(m0, m1);
 }
 
+// Scores of keys key0 .. key0 + 63 that the band or the sequence's end hides
+// set to -inf, so that the unmasked maximum and P code (exp2(-inf) = 0) then
+// serve the block too. A separate masked copy of that code runs once per
+// tile and was found cold in the instruction cache every time.
+__device__ __forceinline__ void mask_scores(const Params& p, uint32_t (&raw)[64], int key0,
+                                            int qrow) {
+  // key0 + e is visible iff lo <= e <= hi
+  const int hi = min(p.N - 1, qrow + p.win_right) - key0;
+  const int lo = qrow - p.win_left - key0;
+#pragma unroll
+  for (int e = 0; e < 64; ++e)
+    if (e < lo || e > hi) raw[e] = 0xff800000u;  // -inf
+}
+
 // P = 2^(x - shift) of 64 keys (key0 .. key0 + 63, S columns src .. src +
 // 63) as bf16 pairs in columns dst .. dst + 31; returns their sum of P (fp32,
 // before rounding and before dropout). With DROP the bf16 values are
@@ -587,8 +601,12 @@ __device__ void softmax_role(const Ctx& c, const Params& p, uint8_t* smem, uint3
       }
       const bool masked =
           n0 + kBn - 1 - m0 > p.win_right || m0 + kBm - 1 - n0 > p.win_left || n0 + kBn > p.N;
-      const float hmax = masked ? chunk_max_regs<true>(p, raw, key0, qrow)
-                                : chunk_max_regs<false>(p, raw, key0, qrow);
+      // without the softcap, hidden keys become -inf scores (tanh would make
+      // -inf a finite logit, so the softcap keeps its masked code)
+      if (!SOFTCAP && masked) mask_scores(p, raw, key0, qrow);
+      const bool mask_code = SOFTCAP && masked;
+      const float hmax = mask_code ? chunk_max_regs<true>(p, raw, key0, qrow)
+                                   : chunk_max_regs<false>(p, raw, key0, qrow);
       float* slot = xmax + (gb & 1) * 256;
       slot[h * 128 + r] = hmax;
       ok = named_bar_and(kBarBoth, 256, ok && got);
@@ -642,10 +660,10 @@ __device__ void softmax_role(const Ctx& c, const Params& p, uint8_t* smem, uint3
       }
       const float shift = m_used > -INFINITY ? m_used : 0.f;
       const uint32_t dst = tS + 64 * h;  // keys 0-63 -> columns 0-31, 64-127 -> 64-95
-      l += masked ? chunk_p_regs<SOFTCAP, true, DROP>(p, raw, dst, key0, qrow, c_log2, cap_in,
-                                                      cap_out, shift, kb0, kb1)
-                  : chunk_p_regs<SOFTCAP, false, DROP>(p, raw, dst, key0, qrow, c_log2, cap_in,
-                                                       cap_out, shift, kb0, kb1);
+      l += mask_code ? chunk_p_regs<SOFTCAP, true, DROP>(p, raw, dst, key0, qrow, c_log2, cap_in,
+                                                         cap_out, shift, kb0, kb1)
+                     : chunk_p_regs<SOFTCAP, false, DROP>(p, raw, dst, key0, qrow, c_log2,
+                                                          cap_in, cap_out, shift, kb0, kb1);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
